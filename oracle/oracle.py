@@ -1,0 +1,177 @@
+"""ctypes front end of the fp64 CPU oracle (test infrastructure only).
+
+Only the test-suite, the smoke check and the benchmark's CPU-baseline leg may
+import this module.  It takes numpy arrays holding the *stored* input values:
+float32 arrays for fp32 inputs, uint16 arrays of bf16 bit patterns for bf16
+inputs.  Everything is computed in double precision by oracle.c.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+F32, BF16 = 0, 1
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+_I64P = ctypes.POINTER(ctypes.c_int64)
+_F64P = ctypes.POINTER(ctypes.c_double)
+_VP = ctypes.c_void_p
+
+_ERR = {1: "bad arguments", 2: "bad metadata", 3: "out of memory"}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def load(path=None):
+    """Load (building first if needed) an oracle shared library."""
+    path = path or _build.build()
+    lib = ctypes.CDLL(path)
+    lib.oracle_paged_attention_window.argtypes = [
+        _VP, _VP, _VP, ctypes.c_int, _I32P, _I32P, _I32P, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, _I64P, ctypes.c_longlong,
+        _F64P, _F64P]
+    lib.oracle_paged_attention_window.restype = ctypes.c_int
+    lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, _F64P, _F64P, _F64P, _F64P]
+    lib.oracle_lse_merge.restype = ctypes.c_int
+    lib.oracle_mla_decode.argtypes = [
+        _VP, _VP, ctypes.c_int, _I32P, _I32P, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_double, _I64P,
+        ctypes.c_longlong, _F64P]
+    lib.oracle_mla_decode.restype = ctypes.c_int
+    lib.oracle_gather_rows.argtypes = [
+        _VP, ctypes.c_int, ctypes.c_int, _I32P, _I32P, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_longlong, _VP]
+    lib.oracle_gather_rows.restype = ctypes.c_int
+    return lib
+
+
+_LIB = None
+
+
+def _lib():
+    global _LIB
+    if _LIB is None:
+        _LIB = load()
+    return _LIB
+
+
+def _dtype_code(arr):
+    if arr.dtype == np.float32:
+        return F32
+    if arr.dtype == np.uint16:
+        return BF16
+    raise TypeError(f"oracle inputs must be float32 or uint16 (bf16 bits), got {arr.dtype}")
+
+
+def _i32(a):
+    return np.ascontiguousarray(a, dtype=np.int32)
+
+
+def _ptr(a, typ):
+    return a.ctypes.data_as(typ)
+
+
+def _check(rc):
+    if rc != 0:
+        raise OracleError(_ERR.get(rc, f"oracle error {rc}"))
+
+
+def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                    num_heads, num_kv_heads, head_dim, block_size, scale,
+                    rows=None, kv_window=None, lib=None, with_lse=False):
+    """fp64 unified paged attention.  Shapes:
+    q [T, H, D]; k_cache, v_cache [num_blocks, block_size, Hk, D];
+    block_table [S, max_blocks]; seq_lens [S]; query_start_loc [S+1].
+    rows: optional int64 array of flat (token * H + head) indices to compute;
+    rows not listed come back as NaN.  kv_window=(lo, hi) restricts every
+    request to KV positions in [lo, hi) (used to form split-KV partials).
+    Returns out [T, H, D] float64 (and lse [T, H] when with_lse)."""
+    lib = lib or _lib()
+    q = np.ascontiguousarray(q)
+    k_cache = np.ascontiguousarray(k_cache)
+    v_cache = np.ascontiguousarray(v_cache)
+    dt = _dtype_code(q)
+    assert _dtype_code(k_cache) == dt and _dtype_code(v_cache) == dt
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    qsl = _i32(query_start_loc)
+    S = int(sl.shape[0])
+    T = int(q.shape[0])
+    out = np.full((T, num_heads, head_dim), np.nan, dtype=np.float64)
+    lse = np.full((T, num_heads), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        rows_p, nrows = _ptr(rows, _I64P), int(rows.shape[0])
+    else:
+        rows_p, nrows = None, 0
+    lo, hi = (0, 2**62) if kv_window is None else kv_window
+    max_blocks = int(bt.shape[1]) if bt.ndim == 2 else 0
+    rc = lib.oracle_paged_attention_window(
+        q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data, dt,
+        _ptr(bt, _I32P), _ptr(sl, _I32P), _ptr(qsl, _I32P), S, T, num_heads,
+        num_kv_heads, head_dim, block_size, max_blocks, int(k_cache.shape[0]),
+        float(scale), int(lo), int(hi), rows_p, nrows, _ptr(out, _F64P),
+        _ptr(lse, _F64P))
+    _check(rc)
+    return (out, lse) if with_lse else out
+
+
+def lse_merge(partial_out, partial_lse, lib=None):
+    """Merge P partial results of one row: partial_out [P, D], partial_lse [P]."""
+    lib = lib or _lib()
+    po = np.ascontiguousarray(partial_out, dtype=np.float64)
+    pl = np.ascontiguousarray(partial_lse, dtype=np.float64)
+    P, D = po.shape
+    out = np.zeros(D, dtype=np.float64)
+    lse = np.zeros(1, dtype=np.float64)
+    _check(lib.oracle_lse_merge(P, D, _ptr(po, _F64P), _ptr(pl, _F64P), _ptr(out, _F64P),
+                                _ptr(lse, _F64P)))
+    return out, float(lse[0])
+
+
+def mla_decode(q, kv_cache, block_table, seq_lens, kv_lora_rank, rope_dim, block_size,
+               scale, rows=None, lib=None):
+    """fp64 absorbed-MLA decode.  q [S, H, L+R]; kv_cache [num_blocks, bs, L+R];
+    returns out [S, H, L] float64 (rows not listed come back NaN)."""
+    lib = lib or _lib()
+    q = np.ascontiguousarray(q)
+    kv_cache = np.ascontiguousarray(kv_cache)
+    dt = _dtype_code(q)
+    assert _dtype_code(kv_cache) == dt
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    S, H, _ = q.shape
+    out = np.full((S, H, kv_lora_rank), np.nan, dtype=np.float64)
+    if rows is not None:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        rows_p, nrows = _ptr(rows, _I64P), int(rows.shape[0])
+    else:
+        rows_p, nrows = None, 0
+    rc = lib.oracle_mla_decode(q.ctypes.data, kv_cache.ctypes.data, dt, _ptr(bt, _I32P),
+                               _ptr(sl, _I32P), S, H, kv_lora_rank, rope_dim, block_size,
+                               int(bt.shape[1]), int(kv_cache.shape[0]), float(scale),
+                               rows_p, nrows, _ptr(out, _F64P))
+    _check(rc)
+    return out
+
+
+def gather_rows(k_cache, block_table, seq_lens, block_size, max_seq_len):
+    """Dense gather of K rows through the block table: returns
+    [S, max_seq_len, row_elems] with untouched positions zero."""
+    lib = _lib()
+    kc = np.ascontiguousarray(k_cache)
+    nb = kc.shape[0]
+    row_elems = int(np.prod(kc.shape[2:]))
+    bt = _i32(block_table)
+    sl = _i32(seq_lens)
+    S = int(sl.shape[0])
+    dense = np.zeros((S, max_seq_len, row_elems), dtype=kc.dtype)
+    _check(lib.oracle_gather_rows(kc.ctypes.data, kc.dtype.itemsize, row_elems,
+                                  _ptr(bt, _I32P), _ptr(sl, _I32P), S, int(bt.shape[1]), nb,
+                                  block_size, int(max_seq_len), dense.ctypes.data))
+    return dense
