@@ -1,0 +1,467 @@
+"""Benchmark of unified paged attention on GB300 (one JSON line on rank 0).
+
+Headline (`value`): decode KV GB/s of pa_forward on the Llama-3.1-8B-shaped
+GQA decode at batch 64 (32 q heads, 8 KV heads, head_dim 128, block_size 16,
+contexts uniform on [500, 8192], bf16): one step = one pa_forward call over
+the whole batch (planner, row-streaming kernel, log-sum-exp merge); bytes =
+the K and V bytes of every visible position, inputs resident in HBM and far
+larger than L2 (~1.1 GB of KV per step, L2 is 129 MB).
+
+The same run also measures, per step with an L2 flush between steps:
+batch-1 decode at context 500, the Qwen3-235B-shaped mixed batch (TFLOPS),
+the 128K chunked long-context batch and the absorbed MLA decode.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the fp64 CPU oracle on the same workload (a bounded
+sample per step) as the reference arm.  Multi-GPU: N independent replicas
+(weak scaling, no data-path collective); the timed region is bracketed by a
+barrier and the max over ranks is reported.
+"""
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_attention_16_gb300 import inputs  # noqa: E402
+
+METRIC = "decode KV GB/s (% of HBM peak); mixed-batch attention TFLOPS (% of peak)"
+WORKLOAD = ("llama-3.1-8b-shaped GQA decode: batch 64, ctx uniform [500, 8192], 32 q heads, "
+            "8 kv heads, head_dim 128, block_size 16, bf16, random page placement")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kv_bytes(b):
+    es = b.k_cache.element_size()
+    return int(b.seq_lens.to(torch.int64).sum()) * b.num_kv_heads * b.head_dim * es * 2
+
+
+def io_bytes(b):
+    return 2 * b.q.numel() * b.q.element_size()
+
+
+def attn_flops(b):
+    """4 * head_dim flops (QK and PV multiply-adds) per visible (row, key) pair."""
+    qsl = b.query_start_loc.numpy().astype(np.int64)
+    ctx = b.seq_lens.numpy().astype(np.int64)
+    total = 0
+    for s in range(b.num_seqs):
+        ql = qsl[s + 1] - qsl[s]
+        pre = ctx[s] - ql
+        # sum over i < ql of (pre + i + 1)
+        total += ql * pre + ql * (ql + 1) // 2
+    return 4 * b.head_dim * b.num_heads * total
+
+
+def mla_bytes(m):
+    return int(m.seq_lens.to(torch.int64).sum()) * (m.kv_lora_rank + m.rope_dim) * 2
+
+
+def mla_flops(m):
+    return int(m.seq_lens.to(torch.int64).sum()) * m.num_heads * 2 * (
+        2 * m.kv_lora_rank + m.rope_dim)
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.samples = []
+        self.proc = None
+        self.sel = []
+        try:
+            uuid = str(torch.cuda.get_device_properties(device).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+
+    def summary(self, t0, t1):
+        rows = [s for t, s in self.samples if t0 - 0.15 <= t <= t1 + 0.15] or \
+               [s for _, s in self.samples]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [x.strip() for x in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_per_step(fn, steps, flush):
+    """Median device time of `steps` calls, each timed with events on the
+    current stream, with an L2 flush (outside the events) between calls."""
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(st)
+        fn()
+        b.record(st)
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def secondary_workloads(pa, flush, peaks):
+    """Per-workload device times (median over steps, L2 flushed between)."""
+    res = {}
+    hbm = peaks["hbm_gbs"]
+    tfl = peaks["bf16_tflops"]
+
+    b = pa.to_device(inputs.llama_decode(1, poison=False))
+    out = torch.empty_like(b.q)
+    for _ in range(5):
+        pa.forward(b, out=out)
+    ms = time_per_step(lambda: pa.forward(b, out=out), 50, flush)
+    gbs = kv_bytes(b) / ms / 1e6
+    res["llama_decode_b1"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm,
+                              "note": "2 MB of KV: launch-latency bound"}
+    del b, out
+
+    b = pa.to_device(inputs.mixed_qwen3(poison=False))
+    out = torch.empty_like(b.q)
+    pa.forward(b, out=out)
+    ms = time_per_step(lambda: pa.forward(b, out=out), 5, flush)
+    tf = attn_flops(b) / ms / 1e9
+    res["mixed_qwen3"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
+                          "kv_gbs": kv_bytes(b) / ms / 1e6,
+                          "tokens": b.num_tokens, "requests": b.num_seqs}
+    del b, out
+
+    b = pa.to_device(inputs.long_chunked(poison=False))
+    out = torch.empty_like(b.q)
+    pa.forward(b, out=out)
+    ms = time_per_step(lambda: pa.forward(b, out=out), 5, flush)
+    tf = attn_flops(b) / ms / 1e9
+    res["long_chunked"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
+                           "kv_split_tokens": 32768}
+    del b, out
+
+    m = pa.to_device(inputs.mla_decode_batch(poison=False))
+    out = torch.empty((m.num_seqs, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16,
+                      device="cuda")
+    st = pa.pa_mla_decode(m.q, m.kv_cache, m.block_table, m.seq_lens, m.num_heads,
+                          m.kv_lora_rank, m.rope_dim, m.block_size, m.scale, out,
+                          max_seq_len=m.max_seq_len, check=False)
+    if st == pa.PA_OK:
+        ms = time_per_step(lambda: pa.mla_decode(m, out=out), 10, flush)
+        gbs = mla_bytes(m) / ms / 1e6
+        tf = mla_flops(m) / ms / 1e9
+        res["mla_decode"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm, "tflops": tf,
+                             "tensor_frac": tf / tfl}
+    else:
+        res["mla_decode"] = {"unavailable": pa.status_string(st)}
+    return res
+
+
+def cpu_baseline_sample(b, budget_s=12.0):
+    """The fp64 oracle, as it stands, on a bounded sample of the workload:
+    whole requests (all heads) until about budget_s of CPU work."""
+    from oracle import oracle as orc
+    q = inputs.storage_array(b.q)
+    kc = inputs.storage_array(b.k_cache)
+    vc = inputs.storage_array(b.v_cache)
+    bt, sl, qsl = b.block_table.numpy(), b.seq_lens.numpy(), b.query_start_loc.numpy()
+    H = b.num_heads
+    done_bytes, spent, n_req = 0, 0.0, 0
+    for s in range(b.num_seqs):
+        rows = np.arange(qsl[s] * H, qsl[s + 1] * H, dtype=np.int64)
+        t0 = time.perf_counter()
+        orc.paged_attention(q, kc, vc, bt, sl, qsl, H, b.num_kv_heads, b.head_dim,
+                            b.block_size, b.scale, rows=rows)
+        spent += time.perf_counter() - t0
+        done_bytes += int(sl[s]) * b.num_kv_heads * b.head_dim * 2 * 2
+        n_req += 1
+        if spent >= budget_s:
+            break
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n_req} of {b.num_seqs} requests (all {H} heads each), "
+                      f"{done_bytes / 1e6:.0f} MB of KV, {spent:.1f} s"}
+
+
+def run_ours(args):
+    world, rank, local = dist_setup()
+    from paged_kv_attention_16_gb300 import build as pbuild
+    pbuild.build()
+    from paged_kv_attention_16_gb300 import pa
+    peaks, peak_src = load_peaks()
+    dev = torch.cuda.current_device()
+
+    host = inputs.llama_decode(64, poison=False)
+    b = pa.to_device(host)
+    out = torch.empty_like(b.q)
+    step_kv = kv_bytes(b)
+    step_io = io_bytes(b)
+
+    for _ in range(max(args.warmup, 3)):
+        pa.forward(b, out=out)
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev)
+    clocks.start()
+    time.sleep(0.3)
+    pa.pa_profile_enable(True)
+    pa.pa_profile_read()
+    stream = torch.cuda.current_stream()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        pa.forward(b, out=out)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_wall1 = time.time()
+    pa.pa_profile_enable(False)
+    prof = pa.pa_profile_read()
+    time.sleep(0.2)
+    clocks.stop()
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), world)
+    ms_step = ms_total / args.steps
+    value = step_kv * args.steps * world / (ms_total / 1e3) / 1e9
+
+    launches = sum(n for _, n in prof.values())
+    row_ms, row_n = prof.get("row", (0.0, 1))
+    row_avg = row_ms / max(row_n, 1)
+    achieved = (step_kv + step_io) / (row_avg / 1e3) / 1e9
+    hbm = peaks["hbm_gbs"]
+    kernel_share = {k: round(v[0] / max(sum(x[0] for x in prof.values()), 1e-9), 4)
+                    for k, v in prof.items()}
+
+    # ---- end to end through the C ABI with host buffers ---------------------
+    q_h = host.q.pin_memory()
+    bt_h = host.block_table.pin_memory()
+    sl_h = host.seq_lens.pin_memory()
+    qsl_h = host.query_start_loc.pin_memory()
+    out_h = torch.empty(host.q.shape, dtype=host.q.dtype).pin_memory()
+    e2e_steps = min(args.steps, 200)
+
+    def e2e_step():
+        b.q.copy_(q_h, non_blocking=True)
+        b.block_table.copy_(bt_h, non_blocking=True)
+        b.seq_lens.copy_(sl_h, non_blocking=True)
+        b.query_start_loc.copy_(qsl_h, non_blocking=True)
+        pa.forward(b, out=out)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_ms = max_over_ranks(ev0.elapsed_time(ev1), world) / e2e_steps
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, bt_h, sl_h, qsl_h))
+    d2h = out_h.numel() * out_h.element_size()
+
+    secondary = {}
+    if not args.skip_secondary:
+        flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device="cuda")
+        secondary = secondary_workloads(pa, flush, peaks)
+        del flush
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline_sample(host) if not args.skip_cpu else None
+    clk = clocks.summary(t_wall0, t_wall1)
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) values, seeded page placement; no weights needed)",
+        "config": {"workload": WORKLOAD, "batch": 64, "kv_bytes_per_step": step_kv,
+                   "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "hbm_frac": value / hbm,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "row_kernel<bf16,128,4> (decode row streaming)",
+                     "kernel_ms": row_avg, "bytes_per_launch": step_kv + step_io,
+                     "peak_source": f"{peak_src} hbm_gbs (copy read+write)"},
+        "kernel_share": kernel_share,
+        "gpu_launches": launches,
+        "e2e": {"value": step_kv / (e2e_ms / 1e3) / 1e9 * world, "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "note": "per step: q + block_table + seq_lens + query_start_loc copied from "
+                        "pinned host memory, pa_forward, out copied back; the KV cache is "
+                        "resident state"},
+        "clocks": clk,
+        "workloads": secondary,
+        "cpu_baseline": cpu,
+        "peaks": {"hbm_gbs": hbm, "bf16_tflops": peaks["bf16_tflops"], "source": peak_src},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the fp64 oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import oracle as orc
+    host = inputs.llama_decode(64, poison=False)
+    q = inputs.storage_array(host.q)
+    kc = inputs.storage_array(host.k_cache)
+    vc = inputs.storage_array(host.v_cache)
+    bt, sl, qsl = host.block_table.numpy(), host.seq_lens.numpy(), host.query_start_loc.numpy()
+    H = host.num_heads
+
+    def step(i):
+        s = i % host.num_seqs
+        rows = np.arange(qsl[s] * H, qsl[s + 1] * H, dtype=np.int64)
+        orc.paged_attention(q, kc, vc, bt, sl, qsl, H, host.num_kv_heads, host.head_dim,
+                            host.block_size, host.scale, rows=rows)
+        return int(sl[s]) * host.num_kv_heads * host.head_dim * 2 * 2
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    total = 0
+    for i in range(args.steps):
+        total += step(args.warmup + i)
+    dt = time.perf_counter() - t0
+    value = total / dt / 1e9
+    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "GB/s",
+                         "sample": "each step: one request of the batch (all 32 heads), "
+                                   "requests taken in turn"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0}}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--skip-secondary", action="store_true")
+    ap.add_argument("--skip-cpu", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

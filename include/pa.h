@@ -1,0 +1,209 @@
+/*
+ * pa.h -- C ABI of libpa.so: unified paged attention over a continuous batch
+ * on one GB300 (sm_103a), plus the absorbed-MLA decode variant.
+ *
+ * What is computed ("vLLM Triton attention backend deep dive", section
+ * "Technical implementation of paged attention"; "vLLM AMD ROCm attention
+ * backend optimisation", section "Mixed inference workload challenge"):
+ * every query token of every request in one batch -- decode (1 new token),
+ * extend (new tokens on a partly built cache) or prefill (no cached prefix)
+ * -- attends, per query head, to the K/V rows of its own sequence, which live
+ * in fixed-size pages of a shared cache reached through a per-sequence block
+ * table:
+ *
+ *   for request s, query i (0 <= i < q_len_s) at token row r = qsl[s] + i,
+ *   head h, kv head k = h / (num_heads / num_kv_heads):
+ *     prefix = seq_lens[s] - q_len_s;   visible j = 0 .. prefix + i
+ *     K_j = k_cache[block_table[s][j / block_size]][j % block_size][k][:]
+ *     out[r][h][:] = sum_j softmax_j(scale * <q[r][h], K_j>) * V_j
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are device pointers owned by the caller, row-major,
+ *    contiguous, 16-byte aligned.  The library keeps no pointer after return.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *    Calls are asynchronous on it: they never synchronise and never read
+ *    device memory on the host, so pa_forward / pa_mla_decode can be captured
+ *    in a CUDA graph (reserve the workspace first, see pa_reserve).
+ *  - Host-side argument errors return a status and launch nothing.
+ *  - Bad *device* metadata never traps: it sets a bit in the device status word
+ *    (read with pa_get_device_status) and the affected output rows are written
+ *    as zeros:
+ *      PA_DEV_BAD_BLOCK   a block id outside [0, num_blocks) on a visible page;
+ *                         the rows whose visible range covers that page are 0
+ *      PA_DEV_BAD_QLEN    q_len < 0 or q_len > seq_len; the request's rows are 0
+ *      PA_DEV_BAD_SEQLEN  seq_len > max_seq_len (or < 0); the request's rows are 0
+ *      PA_DEV_BAD_QSL     query_start_loc[0] != 0, decreasing, or
+ *                         query_start_loc[num_seqs] != num_tokens; every row is 0
+ *      PA_DEV_OVERFLOW    the plan needs more split partials than the workspace
+ *                         holds (only if seq_lens exceed max_seq_len); every row is 0
+ *      PA_DEV_TIMEOUT     a bounded wait inside a kernel gave up (never expected)
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment ...   */
+  PA_ERR_UNSUPPORTED = 2, /* a shape or dtype this build has no kernel for     */
+  PA_ERR_WORKSPACE = 3,   /* workspace too small while the stream is capturing */
+  PA_ERR_CUDA = 4         /* a CUDA runtime / driver call failed               */
+} pa_status;
+
+/* Device status bits (see above). */
+#define PA_DEV_BAD_BLOCK 0x1u
+#define PA_DEV_BAD_QLEN 0x2u
+#define PA_DEV_BAD_SEQLEN 0x4u
+#define PA_DEV_BAD_QSL 0x8u
+#define PA_DEV_OVERFLOW 0x10u
+#define PA_DEV_TIMEOUT 0x20u
+
+/*
+ * pa_forward -- unified paged attention over a mixed batch.
+ *
+ * Follows "vLLM Triton attention backend deep dive" (sections "Technical
+ * implementation of paged attention", "Q-block optimisation", "Parallel tiled
+ * softmax (3D kernel)", "Persistent kernels and CUDA graphs") and "vLLM AMD
+ * ROCm attention backend optimisation" (sections "Mixed inference workload
+ * challenge", "Three-path routing", "Batch reordering", "Chunked context
+ * processing").  Internally: a one-block planner classifies the requests,
+ * orders the work [decode : extend : prefill] and sizes the KV splits; fixed-
+ * grid persistent kernels (grid = a multiple of the SM count) pull work items
+ * from device counters; split results are combined by a log-sum-exp merge.
+ *
+ *  q               [num_tokens, num_heads, head_dim]                 dtype
+ *  k_cache,v_cache [num_blocks, block_size, num_kv_heads, head_dim]  dtype
+ *  block_table     [num_seqs, max_blocks_per_seq] int32; entries past
+ *                  ceil(seq_len / block_size) are never read (may hold -1)
+ *  seq_lens        [num_seqs] int32: context length INCLUDING this step's
+ *                  new tokens, whose K/V must already be in the cache
+ *  query_start_loc [num_seqs + 1] int32, qsl[0] = 0, non-decreasing,
+ *                  qsl[num_seqs] = num_tokens; q_len_s = qsl[s+1] - qsl[s]
+ *  num_heads % num_kv_heads == 0; num_heads / num_kv_heads in {1,2,4,8,16}
+ *  head_dim in {64, 128}; block_size a multiple of 16, at most 256
+ *  scale           softmax scale (usually 1/sqrt(head_dim))
+ *  out             [num_tokens, num_heads, head_dim] dtype, fully overwritten
+ *  dtype           PA_F32 (fp32 everywhere, CUDA-core FFMA, no TF32) or
+ *                  PA_BF16 (bf16 storage, fp32 accumulation, bf16 output
+ *                  rounded to nearest-even)
+ *  max_seq_len     host-known upper bound on seq_lens (sizes the workspace)
+ *  kv_split_tokens 0 = automatic; otherwise the most KV positions one work
+ *                  item covers (e.g. 32768 for chunked long context), a
+ *                  multiple of 16; splits are merged by log-sum-exp
+ *
+ * Errors: PA_ERR_INVALID_ARG for null pointers with nonzero sizes, negative
+ * sizes, misaligned pointers; PA_ERR_UNSUPPORTED for shapes outside the list
+ * above; PA_ERR_WORKSPACE when the stream is capturing and the reserved
+ * workspace is too small; PA_ERR_CUDA when a launch fails.
+ */
+pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *seq_lens,
+                     const int32_t *query_start_loc, int num_heads,
+                     int num_kv_heads, int head_dim, int block_size,
+                     float scale, void *out, void *stream, pa_dtype dtype,
+                     int num_seqs, int num_tokens, int max_blocks_per_seq,
+                     int num_blocks, int max_seq_len, int kv_split_tokens);
+
+/* Workspace bytes pa_forward needs for these host-known extents. */
+size_t pa_forward_workspace_bytes(pa_dtype dtype, int num_seqs, int num_tokens,
+                                  int num_heads, int num_kv_heads,
+                                  int head_dim, int max_seq_len,
+                                  int kv_split_tokens);
+
+/*
+ * pa_mla_decode -- absorbed multi-head latent attention decode ("vLLM AMD ROCm
+ * attention backend optimisation", section "AITER MLA backend: optimised for
+ * DeepSeek" and its "hybrid processing strategy": decode runs directly on the
+ * 576-wide compressed latent).  One query token per sequence; all heads share
+ * one cached latent row per position:
+ *   score_j = scale * <q[s][h][0:L+R], c_j[0:L+R]>,  out[s][h] = sum_j p_j c_j[0:L]
+ *
+ *  q         [num_seqs, num_heads, kv_lora_rank + rope_dim] bf16
+ *  kv_cache  [num_blocks, block_size, kv_lora_rank + rope_dim] bf16
+ *  block_table, seq_lens as for pa_forward (seq_len >= 1)
+ *  out       [num_seqs, num_heads, kv_lora_rank] bf16
+ *  Supported: num_heads = 128, kv_lora_rank = 512, rope_dim = 64,
+ *  block_size a multiple of 64 (at most 256).
+ */
+pa_status pa_mla_decode(const void *q, const void *kv_cache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        int num_heads, int kv_lora_rank, int rope_dim,
+                        int block_size, float scale, void *out, void *stream,
+                        int num_seqs, int max_blocks_per_seq, int num_blocks,
+                        int max_seq_len, int kv_split_tokens);
+
+size_t pa_mla_decode_workspace_bytes(int num_seqs, int num_heads,
+                                     int kv_lora_rank, int max_seq_len,
+                                     int kv_split_tokens);
+
+/*
+ * pa_reserve -- make sure the calling thread's current device has at least
+ * `bytes` of library-owned workspace (split partials, planner tables, work
+ * counters).  Call it before capturing a graph: during capture the library
+ * never allocates and returns PA_ERR_WORKSPACE instead.  Outside capture,
+ * pa_forward / pa_mla_decode grow the workspace on demand; growing frees the
+ * old buffer, so graphs captured before a growth must be re-captured.
+ * Returns PA_ERR_CUDA if the allocation fails.
+ */
+pa_status pa_reserve(size_t bytes);
+
+/* Synchronises `stream`, copies the device status word of the current device
+ * into *host_flags and clears it.  Not capturable (it synchronises). */
+pa_status pa_get_device_status(void *stream, uint32_t *host_flags);
+
+/* Static, human-readable name of a status code. */
+const char *pa_status_string(pa_status status);
+
+/* Number of SMs of the current device, as the library sizes its grids. */
+int pa_num_sms(void);
+
+/*
+ * pa_debug_gather -- the page-gather indexing alone, for bit-exact tests:
+ *   dense_out[s][j][:] = k_cache[block_table[s][j / bs]][j % bs][0:row_elems]
+ * for j < seq_lens[s] (raw element bits copied, elem_bytes 2 or 4); positions
+ * j >= seq_lens[s] are left untouched.  dense_out is
+ * [num_seqs, max_seq_len, row_elems].  Bad block ids set PA_DEV_BAD_BLOCK and
+ * leave their rows untouched.
+ */
+pa_status pa_debug_gather(const void *k_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, int num_seqs,
+                          int max_blocks_per_seq, int num_blocks,
+                          int block_size, int row_elems, int elem_bytes,
+                          int max_seq_len, void *dense_out, void *stream);
+
+/*
+ * Kernel timing.  While enabled, every kernel that pa_forward, pa_mla_decode
+ * and pa_debug_gather launch is bracketed by a pair of CUDA events recorded
+ * on the caller's stream (nothing is recorded for a stream that is being
+ * captured).  pa_profile_read synchronises on those events, writes for each
+ * kernel id below the summed milliseconds and the launch count (arrays of
+ * PA_K_COUNT entries), and clears the record.  Recording costs two event
+ * records per launch and no synchronisation.
+ */
+enum {
+  PA_K_PLAN = 0,      /* one-block planner                          */
+  PA_K_ROW = 1,       /* row-streaming kernel (decode path)         */
+  PA_K_TILE = 2,      /* tensor-core extend/prefill tile kernel     */
+  PA_K_MERGE = 3,     /* log-sum-exp merge of split partials        */
+  PA_K_MLA = 4,       /* absorbed-MLA decode kernel                 */
+  PA_K_MLA_MERGE = 5, /* MLA log-sum-exp merge                      */
+  PA_K_GATHER = 6,    /* debug gather                               */
+  PA_K_COUNT = 8
+};
+pa_status pa_profile_enable(int on);
+pa_status pa_profile_read(double *total_ms, int *launches);
+const char *pa_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

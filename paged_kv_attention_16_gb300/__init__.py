@@ -5,15 +5,12 @@ The compute lives in a C-ABI CUDA library (libpa.so, header include/pa.h);
 binding is imported lazily so that the seeded input generators
 (`paged_kv_attention_16_gb300.inputs`) can be used without a GPU.
 """
+import importlib
 
-__all__ = ["pa", "inputs"]
+__all__ = ["pa", "inputs", "build"]
 
 
 def __getattr__(name):
-    if name == "pa":
-        from . import pa as _pa
-        return _pa
-    if name == "inputs":
-        from . import inputs as _inputs
-        return _inputs
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

@@ -1,0 +1,715 @@
+// pa_api.cu -- the C ABI of libpa.so (include/pa.h): argument checks,
+// library-owned workspace, TMA tensor maps, and the three small kernels around
+// the attention kernels: the one-block planner, the log-sum-exp merge and the
+// debug gather.
+//
+// Planner ("vLLM AMD ROCm attention backend optimisation", sections "Mixed
+// inference workload challenge" and "Batch reordering"; "vLLM Triton
+// attention backend deep dive", section "Persistent kernels and CUDA graphs"):
+// reads seq_lens / query_start_loc on the device, classifies each request as
+// decode (1 new token), prefill (no cached prefix) or extend, stably orders
+// the requests [decode : extend : prefill], sizes the KV splits, and lays the
+// work lists over that order as prefix sums.  The host never reads device
+// metadata, so the whole call is capturable in a CUDA graph and the grids
+// are fixed (a multiple of the SM count).
+//
+// Merge ("vLLM Triton attention backend deep dive", section "Parallel tiled
+// softmax (3D kernel)": a second launch reduces the partial results;
+// "vLLM AMD ROCm attention backend optimisation", section "Chunked context
+// processing": LSE-based merge): out = sum_p w_p O_p with
+// w_p = 2^(lse_p - M) / sum_q 2^(lse_q - M), M = max_p lse_p (base 2).
+#include <mutex>
+
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+constexpr int kMergeThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// planner
+// ---------------------------------------------------------------------------
+
+struct ReqScalars {
+  int q_start, q_len, ctx, cls;
+  bool valid;
+};
+
+__device__ inline ReqScalars read_req(const FwdParams &p, int s, bool qsl_bad) {
+  ReqScalars r;
+  r.q_start = p.qsl[s];
+  r.q_len = p.qsl[s + 1] - r.q_start;
+  r.ctx = p.seq_lens[s];
+  r.valid = !qsl_bad && r.q_len >= 0 && r.ctx >= 0 && r.q_len <= r.ctx &&
+            r.ctx <= p.max_seq_len &&
+            ceil_div_ll(r.ctx, p.block_size) <= (long long)p.max_blocks_per_seq;
+  if (r.q_len == 1) r.cls = kDecode;
+  else if (r.q_len == r.ctx) r.cls = kPrefill;
+  else r.cls = kExtend;
+  if (!r.valid || r.q_len <= 0) r.cls = kDecode;  // no work; position is irrelevant
+  return r;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
+  __shared__ long long scratch[33];
+  const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x;
+  const int Hk = p.num_kv_heads, G = p.num_heads / p.num_kv_heads, H = p.num_heads;
+
+  // -- global query_start_loc checks -------------------------------------------
+  int bad = 0;
+  if (tid == 0 && (p.qsl[0] != 0 || p.qsl[S] != T)) bad = 1;
+  for (int s = tid; s < S; s += kPlanThreads)
+    if (p.qsl[s + 1] < p.qsl[s]) bad = 1;
+  const bool qsl_bad = __syncthreads_or(bad) != 0;
+
+  // -- pass 1: class counts and the decode KV work (split sizing) --------------
+  long long packed = 0, dec_work = 0;
+  int metabad = 0;
+  for (int s = tid; s < S; s += kPlanThreads) {
+    const ReqScalars r = read_req(p, s, qsl_bad);
+    packed += 1ll << (21 * r.cls);
+    if (r.valid && r.q_len == 1) dec_work += r.ctx;
+    if (!qsl_bad && !r.valid) {
+      if (r.q_len < 0 || r.q_len > r.ctx) metabad |= PA_DEV_BAD_QLEN;
+      if (r.ctx < 0 || r.ctx > p.max_seq_len ||
+          ceil_div_ll(r.ctx, p.block_size) > (long long)p.max_blocks_per_seq)
+        metabad |= PA_DEV_BAD_SEQLEN;
+    }
+  }
+  if (metabad) atomicOr(p.status, (unsigned)metabad);
+  if (tid == 0 && qsl_bad) atomicOr(p.status, PA_DEV_BAD_QSL);
+  long long class_tot, work_tot;
+  block_inclusive_scan(packed, scratch, &class_tot);
+  block_inclusive_scan(dec_work, scratch, &work_tot);
+  const long long mask21 = (1ll << 21) - 1;
+  const long long n_dec = class_tot & mask21, n_ext = (class_tot >> 21) & mask21;
+
+  // Decode split: the smallest power of two >= kRowMinSplit that keeps the
+  // item count near 8 items per resident CTA.
+  const long long target = 8ll * (p.row_ctas > 0 ? p.row_ctas : 1);
+  const long long kv_work = work_tot * Hk;
+  int L = kRowMinSplit;
+  while (L < kRowMaxSplit && kv_work > (long long)L * target) L <<= 1;
+  if (p.kv_split_tokens > 0 && p.kv_split_tokens < L) L = p.kv_split_tokens;
+  // Extend/prefill rows on the row path: at most ~4 splits per row.
+  int Lr = (int)ceil_div_ll(ceil_div_ll(p.max_seq_len, 4), 16) * 16;
+  if (Lr < L) Lr = L;
+  if (Lr > kRowMaxSplit) Lr = kRowMaxSplit;
+  if (p.kv_split_tokens > 0 && p.kv_split_tokens < Lr) Lr = p.kv_split_tokens;
+
+  // -- pass 2: stable partition into [decode : extend : prefill] ---------------
+  long long carry = 0;
+  for (int base = 0; base < S; base += kPlanThreads) {
+    const int s = base + tid;
+    long long v = 0;
+    int cls = 0;
+    if (s < S) {
+      cls = read_req(p, s, qsl_bad).cls;
+      v = 1ll << (21 * cls);
+    }
+    long long chunk_tot;
+    const long long incl = block_inclusive_scan(v, scratch, &chunk_tot) + carry;
+    if (s < S) {
+      const long long before = ((incl >> (21 * cls)) & mask21) - 1;
+      const long long off = cls == kDecode ? 0 : cls == kExtend ? n_dec : n_dec + n_ext;
+      p.ord[off + before] = s;
+    }
+    carry += chunk_tot;
+  }
+  __syncthreads();
+
+  // -- pass 3: per-request plan and list prefix sums in reordered order --------
+  long long run[kNumLists] = {0, 0, 0, 0}, run_part = 0;
+  for (int base = 0; base < S; base += kPlanThreads) {
+    const int k = base + tid;
+    long long cnt[kNumLists] = {0, 0, 0, 0}, part = 0;
+    int s = -1;
+    ReqInfo info{};
+    if (k < S) {
+      s = p.ord[k];
+      const ReqScalars r = read_req(p, s, qsl_bad);
+      const bool row_path = r.cls == kDecode || !p.tile_ok;
+      int len = r.cls == kDecode ? L : (row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens
+                                                                               : (r.ctx > 0 ? r.ctx : 1)));
+      int nsplit = (int)ceil_div_ll(r.ctx > 0 ? r.ctx : 1, len);
+      if (nsplit < 1) nsplit = 1;
+      info.q_start = r.q_start;
+      info.q_len = r.q_len;
+      info.ctx = r.ctx;
+      info.flags = r.cls | (r.valid ? kFlagValid : 0) | (row_path ? kFlagRowPath : 0);
+      info.nsplit = nsplit;
+      info.split_len = len;
+      if (r.valid && r.q_len > 0) {
+        if (row_path) cnt[kListRow] = (long long)Hk * r.q_len * nsplit;
+        else cnt[kListTile] = (long long)Hk * ceil_div_ll((long long)r.q_len * G, kTileRows) * nsplit;
+        if (nsplit > 1) {
+          cnt[kListMerge] = (long long)r.q_len * H;
+          part = (long long)r.q_len * H * nsplit;
+        }
+      } else if (!qsl_bad && r.q_len > 0) {
+        cnt[kListZero] = (long long)r.q_len * H;
+      }
+    }
+    long long tot;
+    const long long part_incl = block_inclusive_scan(part, scratch, &tot) + run_part;
+    info.partial_base = part_incl - part;
+    run_part += tot;
+#pragma unroll
+    for (int x = 0; x < kNumLists; ++x) {
+      const long long incl = block_inclusive_scan(cnt[x], scratch, &tot) + run[x];
+      if (k < S) p.list_end[(size_t)x * S + k] = incl;
+      run[x] += tot;
+    }
+    if (k < S) p.req[s] = info;
+  }
+  if (tid == 0) {
+    const bool overflow = run_part > p.part_cap;
+    if (overflow) atomicOr(p.status, PA_DEV_OVERFLOW);
+    const bool zero_all = qsl_bad || overflow;
+    for (int x = 0; x < kNumLists; ++x) p.plan->n[x] = zero_all ? 0 : run[x];
+    for (int x = 0; x < 8; ++x) p.plan->counter[x] = 0;
+    p.plan->qsl_bad = zero_all ? 1 : 0;
+    p.plan->split_len_decode = L;
+    p.plan->partial_rows = run_part;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// log-sum-exp merge of split partials (one CTA per row)
+// ---------------------------------------------------------------------------
+
+template <typename T>
+__device__ inline void store_out(T *dst, float v);
+template <>
+__device__ inline void store_out<float>(float *dst, float v) { *dst = v; }
+template <>
+__device__ inline void store_out<__nv_bfloat16>(__nv_bfloat16 *dst, float v) {
+  *dst = __float2bfloat16_rn(v);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p) {
+  __shared__ float s_red[kMergeThreads / 32][128];
+  __shared__ float s_wl[kMergeThreads / 32];
+  __shared__ float s_m[kMergeThreads / 32];
+  __shared__ int s_bad[kMergeThreads / 32];
+  const int S = p.num_seqs, H = p.num_heads, D = p.head_dim;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int NW = kMergeThreads / 32;
+  T *out = reinterpret_cast<T *>(p.out);
+
+  if (p.plan->qsl_bad) {
+    const size_t n = (size_t)p.num_tokens * H * D;
+    for (size_t e = (size_t)blockIdx.x * blockDim.x + tid; e < n; e += (size_t)gridDim.x * blockDim.x)
+      store_out<T>(out + e, 0.f);
+    return;
+  }
+
+  // rows of requests whose metadata failed: zeros
+  {
+    const long long *zend = p.list_end + (size_t)kListZero * S;
+    const long long nz = p.plan->n[kListZero];
+    const long long gw = ((long long)blockIdx.x * blockDim.x + tid) >> 5;
+    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+    for (long long row = gw; row < nz; row += nw) {
+      const int k = list_find(zend, S, row);
+      const long long local = row - (k ? zend[k - 1] : 0);
+      const ReqInfo r = p.req[p.ord[k]];
+      const long long tok = r.q_start + local / H;
+      const int h = (int)(local % H);
+      for (int d = lane; d < D; d += 32) store_out<T>(out + ((size_t)tok * H + h) * D + d, 0.f);
+    }
+  }
+
+  const long long *mend = p.list_end + (size_t)kListMerge * S;
+  const long long nm = p.plan->n[kListMerge];
+  const int dpl = D / 32;  // dims per lane: 2 or 4
+  for (long long row = blockIdx.x; row < nm; row += gridDim.x) {
+    const int k = list_find(mend, S, row);
+    const long long local = row - (k ? mend[k - 1] : 0);
+    const ReqInfo r = p.req[p.ord[k]];
+    const int i = (int)(local / H), h = (int)(local % H);
+    const long long tok = r.q_start + i;
+    const int kv_row_hi = r.ctx - r.q_len + i + 1;
+    const int nn = (int)ceil_div_ll(kv_row_hi, r.split_len);  // non-empty splits of this row
+    if (nn <= 1) continue;  // the attention kernel wrote this row directly (uniform per CTA)
+    const long long base = r.partial_base + ((long long)i * H + h) * r.nsplit;
+    // max lse and bad-split check
+    float M = -INFINITY;
+    int bad = 0;
+    for (int q = tid; q < nn; q += kMergeThreads) {
+      const float v = p.part_lse[base + q];
+      if (isnan(v)) bad = 1; else M = fmaxf(M, v);
+    }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    if (lane == 0) {
+      s_m[warp] = M;
+      s_bad[warp] = bad;
+    }
+    __syncthreads();
+    M = s_m[0];
+    bad = s_bad[0];
+    for (int w = 1; w < NW; ++w) {
+      M = fmaxf(M, s_m[w]);
+      bad |= s_bad[w];
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float wl = 0.f;
+    if (!bad && M != -INFINITY) {
+      for (int q = warp; q < nn; q += NW) {
+        const float w = fast_exp2(p.part_lse[base + q] - M);
+        wl += w;
+        const float *src = p.part_o + (size_t)(base + q) * D + lane * dpl;
+        if (dpl == 4) {
+          const float4 v = *reinterpret_cast<const float4 *>(src);
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+          acc[2] = fmaf(w, v.z, acc[2]);
+          acc[3] = fmaf(w, v.w, acc[3]);
+        } else {
+          const float2 v = *reinterpret_cast<const float2 *>(src);
+          acc[0] = fmaf(w, v.x, acc[0]);
+          acc[1] = fmaf(w, v.y, acc[1]);
+        }
+      }
+    }
+    for (int x = 0; x < dpl; ++x) s_red[warp][lane * dpl + x] = acc[x];
+    if (lane == 0) s_wl[warp] = wl;
+    __syncthreads();
+    if (tid < D) {
+      float a = 0.f, L = 0.f;
+      for (int w = 0; w < NW; ++w) {
+        a += s_red[w][tid];
+        L += s_wl[w];
+      }
+      const float v = (bad || !(L > 0.f)) ? 0.f : a / L;
+      store_out<T>(out + ((size_t)tok * H + h) * D + tid, v);
+    }
+    __syncthreads();
+  }
+}
+
+// ---------------------------------------------------------------------------
+// debug gather: dense[s][j][:] = cache row (block_table[s][j / bs], j % bs)
+// ---------------------------------------------------------------------------
+
+__global__ void gather_kernel(const uint8_t *cache, const int32_t *bt, const int32_t *seq_lens,
+                              int num_seqs, int mbps, int num_blocks, int bs, int row_bytes,
+                              int max_seq_len, uint8_t *dense, unsigned int *status) {
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const long long n = (long long)num_seqs * max_seq_len;
+  for (long long w = gw; w < n; w += nw) {
+    const int s = (int)(w / max_seq_len), j = (int)(w % max_seq_len);
+    if (j >= seq_lens[s]) continue;
+    const int lp = j / bs;
+    const int page = lp < mbps ? bt[(size_t)s * mbps + lp] : -1;
+    if (page < 0 || page >= num_blocks) {
+      if (lane == 0) atomicOr(status, PA_DEV_BAD_BLOCK);
+      continue;
+    }
+    const uint8_t *src = cache + ((size_t)page * bs + (j % bs)) * row_bytes;
+    uint8_t *dst = dense + ((size_t)s * max_seq_len + j) * row_bytes;
+    if ((row_bytes & 15) == 0) {
+      for (int b = lane * 16; b < row_bytes; b += 32 * 16)
+        *reinterpret_cast<uint4 *>(dst + b) = *reinterpret_cast<const uint4 *>(src + b);
+    } else {
+      for (int b = lane * 2; b < row_bytes; b += 64)
+        *reinterpret_cast<uint16_t *>(dst + b) = *reinterpret_cast<const uint16_t *>(src + b);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host state
+// ---------------------------------------------------------------------------
+
+struct DeviceState {
+  bool init = false;
+  int num_sms = 0;
+  unsigned int *status = nullptr;
+  void *ws = nullptr;
+  size_t ws_bytes = 0;
+};
+
+std::mutex g_mu;
+DeviceState g_dev[64];
+
+bool stream_capturing(cudaStream_t stream) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) return false;
+  return st != cudaStreamCaptureStatusNone;
+}
+
+// Device state of the current device; initialises it outside capture.
+pa_status device_state(cudaStream_t stream, DeviceState **out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState &d = g_dev[dev];
+  if (!d.init) {
+    if (stream_capturing(stream)) return PA_ERR_WORKSPACE;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return PA_ERR_CUDA;
+    if (cudaMalloc(&d.status, 256) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaMemset(d.status, 0, 256) != cudaSuccess) return PA_ERR_CUDA;
+    d.init = true;
+  }
+  *out = &d;
+  return PA_OK;
+}
+
+pa_status ensure_workspace(DeviceState *d, size_t bytes, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (d->ws_bytes >= bytes) return PA_OK;
+  if (stream_capturing(stream)) return PA_ERR_WORKSPACE;
+  if (d->ws) {
+    cudaFree(d->ws);  // synchronises the device: no call still uses the old buffer
+    d->ws = nullptr;
+    d->ws_bytes = 0;
+  }
+  size_t want = bytes + bytes / 4;
+  if (cudaMalloc(&d->ws, want) != cudaSuccess) {
+    cudaGetLastError();
+    if (cudaMalloc(&d->ws, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
+    want = bytes;
+  }
+  d->ws_bytes = want;
+  return PA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct FwdLayout {
+  size_t plan, req, ord, list_end, part_o, part_lse, total;
+  long long part_cap;
+};
+
+long long ceil_div_h(long long a, long long b) { return (a + b - 1) / b; }
+
+// Upper bound on the split partial rows pa_forward may need; mirrors the
+// planner's split rules using only host-known extents.
+long long partial_capacity(int num_seqs, int num_tokens, int num_heads, int max_seq_len,
+                           int kvs, bool tile_ok) {
+  const long long msl = max_seq_len > 0 ? max_seq_len : 1;
+  const long long kvs_or_inf = kvs > 0 ? kvs : (1ll << 40);
+  // decode rows: at most min(S, T) requests with one row each
+  const long long l_dec = kRowMinSplit < kvs_or_inf ? kRowMinSplit : kvs_or_inf;
+  const long long n_dec = ceil_div_h(msl, l_dec);
+  const long long dec_rows = (long long)(num_seqs < num_tokens ? num_seqs : num_tokens);
+  long long cap = n_dec > 1 ? dec_rows * num_heads * n_dec : 0;
+  long long n_other;
+  if (tile_ok) {
+    n_other = kvs > 0 ? ceil_div_h(msl, kvs) : 1;
+  } else {
+    long long lr = ceil_div_h(ceil_div_h(msl, 4), 16) * 16;
+    if (lr < kRowMinSplit) lr = kRowMinSplit;
+    if (lr > kRowMaxSplit) lr = kRowMaxSplit;
+    if (kvs_or_inf < lr) lr = kvs_or_inf;
+    n_other = ceil_div_h(msl, lr);
+  }
+  if (n_other > 1) cap += (long long)num_tokens * num_heads * n_other;
+  return cap;
+}
+
+FwdLayout fwd_layout(int num_seqs, int num_tokens, int num_heads, int head_dim,
+                     int max_seq_len, int kvs, bool tile_ok) {
+  FwdLayout l{};
+  const size_t S = num_seqs > 0 ? num_seqs : 1;
+  size_t off = 0;
+  l.plan = off;
+  off = align256(off + sizeof(PlanHeader));
+  l.req = off;
+  off = align256(off + S * sizeof(ReqInfo));
+  l.ord = off;
+  off = align256(off + S * sizeof(int));
+  l.list_end = off;
+  off = align256(off + S * kNumLists * sizeof(long long));
+  l.part_cap = partial_capacity(num_seqs, num_tokens, num_heads, max_seq_len, kvs, tile_ok);
+  l.part_o = off;
+  off = align256(off + (size_t)l.part_cap * head_dim * sizeof(float));
+  l.part_lse = off;
+  off = align256(off + (size_t)l.part_cap * sizeof(float));
+  l.total = off;
+  return l;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no -lcuda).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                         cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Tensor map over a paged cache [num_blocks, block_size, heads, dim] with a
+// box of {dim, 1, box_slots, 1}: one (page, kv head) run of slots per copy.
+bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
+                      int block_size, int heads, int dim, int box_dim0, int box_slots,
+                      CUtensorMapSwizzle swz) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const size_t es = dtype == PA_F32 ? 4 : 2;
+  cuuint64_t dims[4] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)block_size,
+                        (cuuint64_t)num_blocks};
+  cuuint64_t strides[3] = {(cuuint64_t)(dim * es), (cuuint64_t)(heads * dim * es),
+                           (cuuint64_t)((size_t)block_size * heads * dim * es)};
+  cuuint32_t box[4] = {(cuuint32_t)box_dim0, 1, (cuuint32_t)box_slots, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType t =
+      dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return fn(map, t, 4, const_cast<void *>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+bool group_ok(int g) { return g == 1 || g == 2 || g == 4 || g == 8 || g == 16; }
+
+// Resident CTAs per SM of the row kernel, cached per (device, dtype, dim, group).
+int row_ctas_per_sm_cached(int dtype, int head_dim, int group) {
+  static std::mutex mu;
+  static int cache[64][2][2][5];
+  static bool have[64][2][2][5];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int a = dtype == PA_BF16 ? 1 : 0, b = head_dim == 128 ? 1 : 0;
+  const int c = group == 1 ? 0 : group == 2 ? 1 : group == 4 ? 2 : group == 8 ? 3 : 4;
+  std::lock_guard<std::mutex> lock(mu);
+  if (dev < 0 || dev >= 64) return 1;
+  if (!have[dev][a][b][c]) {
+    cache[dev][a][b][c] = row_kernel_ctas_per_sm(dtype, head_dim, group);
+    have[dev][a][b][c] = true;
+  }
+  return cache[dev][a][b][c] > 0 ? cache[dev][a][b][c] : 1;
+}
+
+bool tile_path_ok(int dtype, int head_dim, int group) {
+  return tile_kernel_supported(dtype, head_dim, group);
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_status_string(pa_status status) {
+  switch (status) {
+    case PA_OK: return "ok";
+    case PA_ERR_INVALID_ARG: return "invalid argument";
+    case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PA_ERR_WORKSPACE: return "workspace too small during stream capture";
+    case PA_ERR_CUDA: return "CUDA error";
+  }
+  return "unknown status";
+}
+
+int pa_num_sms(void) {
+  DeviceState *d = nullptr;
+  if (device_state(nullptr, &d) != PA_OK) return 0;
+  return d->num_sms;
+}
+
+size_t pa_forward_workspace_bytes(pa_dtype dtype, int num_seqs, int num_tokens, int num_heads,
+                                  int num_kv_heads, int head_dim, int max_seq_len,
+                                  int kv_split_tokens) {
+  if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads) return 0;
+  const bool tile_ok = tile_path_ok(dtype, head_dim, num_heads / num_kv_heads);
+  return fwd_layout(num_seqs, num_tokens, num_heads, head_dim, max_seq_len, kv_split_tokens,
+                    tile_ok)
+      .total;
+}
+
+pa_status pa_reserve(size_t bytes) {
+  DeviceState *d = nullptr;
+  pa_status st = device_state(nullptr, &d);
+  if (st != PA_OK) return st;
+  return ensure_workspace(d, bytes, nullptr);
+}
+
+pa_status pa_get_device_status(void *stream, uint32_t *host_flags) {
+  if (!host_flags) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState *d = nullptr;
+  pa_status s = device_state(st, &d);
+  if (s != PA_OK) return s;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, d->status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (cudaMemset(d->status, 0, sizeof(v)) != cudaSuccess) return PA_ERR_CUDA;
+  *host_flags = v;
+  return PA_OK;
+}
+
+pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
+                     const int32_t *block_table, const int32_t *seq_lens,
+                     const int32_t *query_start_loc, int num_heads, int num_kv_heads,
+                     int head_dim, int block_size, float scale, void *out, void *stream,
+                     pa_dtype dtype, int num_seqs, int num_tokens, int max_blocks_per_seq,
+                     int num_blocks, int max_seq_len, int kv_split_tokens) {
+  // ---- host argument checks ---------------------------------------------------
+  if (num_seqs < 0 || num_tokens < 0 || max_seq_len < 0 || kv_split_tokens < 0 ||
+      num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  const int group = num_heads / num_kv_heads;
+  if (!group_ok(group) || (head_dim != 64 && head_dim != 128) || block_size % 16 != 0 ||
+      block_size > 256 || kv_split_tokens % 16 != 0)
+    return PA_ERR_UNSUPPORTED;
+  if (num_tokens == 0) return PA_OK;  // no output rows
+  if (!q || !out || !query_start_loc || (num_seqs > 0 && (!seq_lens || !block_table)))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs > 0 && (!k_cache || !v_cache || num_blocks <= 0 || max_blocks_per_seq <= 0))
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(out) || (num_seqs > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
+    return PA_ERR_INVALID_ARG;
+  if ((long long)num_tokens * num_heads * head_dim > (1ll << 40)) return PA_ERR_UNSUPPORTED;
+
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState *d = nullptr;
+  pa_status s = device_state(st, &d);
+  if (s != PA_OK) return s;
+  const bool tile_ok = tile_path_ok(dtype, head_dim, group);
+  const FwdLayout lay = fwd_layout(num_seqs, num_tokens, num_heads, head_dim, max_seq_len,
+                                   kv_split_tokens, tile_ok);
+  s = ensure_workspace(d, lay.total, st);
+  if (s != PA_OK) return s;
+
+  const int row_ctas = row_ctas_per_sm_cached(dtype, head_dim, group) * d->num_sms;
+  uint8_t *ws = reinterpret_cast<uint8_t *>(d->ws);
+  FwdParams p{};
+  p.q = q;
+  p.out = out;
+  p.block_table = block_table;
+  p.seq_lens = seq_lens;
+  p.qsl = query_start_loc;
+  p.num_seqs = num_seqs;
+  p.num_tokens = num_tokens;
+  p.num_heads = num_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  p.block_size = block_size;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_blocks = num_blocks;
+  p.max_seq_len = max_seq_len;
+  p.kv_split_tokens = kv_split_tokens;
+  p.scale = scale;
+  p.scale_log2 = scale * kLog2e;
+  p.tile_ok = tile_ok ? 1 : 0;
+  p.row_ctas = row_ctas;
+  p.dtype = dtype;
+  p.plan = reinterpret_cast<PlanHeader *>(ws + lay.plan);
+  p.req = reinterpret_cast<ReqInfo *>(ws + lay.req);
+  p.ord = reinterpret_cast<int *>(ws + lay.ord);
+  p.list_end = reinterpret_cast<long long *>(ws + lay.list_end);
+  p.part_o = reinterpret_cast<float *>(ws + lay.part_o);
+  p.part_lse = reinterpret_cast<float *>(ws + lay.part_lse);
+  p.part_cap = lay.part_cap;
+  p.status = d->status;
+
+  int slot = prof_begin(PA_K_PLAN, st);
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+  prof_end(slot, st);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+  if (num_seqs > 0) {
+    CUtensorMap tm_k, tm_v;
+    if (!encode_cache_map(&tm_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                          head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_cache_map(&tm_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                          head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return PA_ERR_CUDA;
+    slot = prof_begin(PA_K_ROW, st);
+    const cudaError_t row_err = launch_row_kernel(p, tm_k, tm_v, row_ctas, st);
+    prof_end(slot, st);
+    if (row_err != cudaSuccess) return PA_ERR_CUDA;
+    if (tile_ok) {
+      CUtensorMap tm_q, tm_kt, tm_vt;
+      // Q as [tokens, heads, dim] with 64-element (128-byte) swizzled boxes of
+      // G heads x (128 / G) tokens; K/V pages as 64-element swizzled boxes.
+      EncodeTiledFn fn = encode_fn();
+      cuuint64_t qd[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)num_tokens};
+      cuuint64_t qs[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
+      cuuint32_t qb[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileRows / group)};
+      cuuint32_t qe[3] = {1, 1, 1};
+      if (!fn ||
+          fn(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), qd, qs, qb, qe,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+          !encode_cache_map(&tm_kt, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                            64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_cache_map(&tm_vt, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
+                            64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+        return PA_ERR_CUDA;
+      slot = prof_begin(PA_K_TILE, st);
+      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vt, d->num_sms, st);
+      prof_end(slot, st);
+      if (tile_err != cudaSuccess) return PA_ERR_CUDA;
+    }
+  }
+  slot = prof_begin(PA_K_MERGE, st);
+  if (dtype == PA_BF16)
+    merge_kernel<__nv_bfloat16><<<d->num_sms * 4, kMergeThreads, 0, st>>>(p);
+  else
+    merge_kernel<float><<<d->num_sms * 4, kMergeThreads, 0, st>>>(p);
+  prof_end(slot, st);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+pa_status pa_debug_gather(const void *k_cache, const int32_t *block_table,
+                          const int32_t *seq_lens, int num_seqs, int max_blocks_per_seq,
+                          int num_blocks, int block_size, int row_elems, int elem_bytes,
+                          int max_seq_len, void *dense_out, void *stream) {
+  if (num_seqs < 0 || max_seq_len < 0 || row_elems <= 0 || block_size <= 0 ||
+      (elem_bytes != 2 && elem_bytes != 4))
+    return PA_ERR_INVALID_ARG;
+  if (num_seqs == 0 || max_seq_len == 0) return PA_OK;
+  if (!k_cache || !block_table || !seq_lens || !dense_out || num_blocks <= 0 ||
+      max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  const int row_bytes = row_elems * elem_bytes;
+  if ((row_bytes & 15) == 0 && (!aligned16(k_cache) || !aligned16(dense_out)))
+    return PA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState *d = nullptr;
+  pa_status s = device_state(st, &d);
+  if (s != PA_OK) return s;
+  const int slot = prof_begin(PA_K_GATHER, st);
+  gather_kernel<<<d->num_sms * 8, 256, 0, st>>>(
+      reinterpret_cast<const uint8_t *>(k_cache), block_table, seq_lens, num_seqs,
+      max_blocks_per_seq, num_blocks, block_size, row_bytes, max_seq_len,
+      reinterpret_cast<uint8_t *>(dense_out), d->status);
+  prof_end(slot, st);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // extern "C"

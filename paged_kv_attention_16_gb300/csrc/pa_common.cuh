@@ -1,0 +1,235 @@
+// pa_common.cuh -- device-side building blocks shared by the kernels of
+// libpa.so: plan structures written by the planner, inline-PTX wrappers for
+// mbarriers, TMA tensor copies and proxy fences, bounded waits, warp scans.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ---------------------------------------------------------------------------
+// Plan: what the one-block planner writes for the consumer kernels.
+// ---------------------------------------------------------------------------
+
+enum ReqClass : int { kDecode = 0, kExtend = 1, kPrefill = 2 };
+
+enum ReqFlags : int {
+  kFlagValid = 1 << 4,   // metadata checks passed
+  kFlagRowPath = 1 << 5, // rows go through the row-streaming kernel
+};
+
+// Per request (original index s).
+struct ReqInfo {
+  int q_start;        // query_start_loc[s]
+  int q_len;          // new tokens
+  int ctx;            // seq_lens[s]: KV positions including the new tokens
+  int flags;          // ReqClass in bits 0..3, ReqFlags above
+  int nsplit;         // KV splits per row (>= 1)
+  int split_len;      // KV positions per split
+  long long partial_base;  // first partial row of this request (nsplit > 1)
+};
+
+// Work lists are never materialised: every list is a virtual index space
+// [0, n) laid over the requests in [decode : extend : prefill] order, with
+// end[k] = inclusive prefix of the per-request counts.  A consumer maps an
+// index to its request with a binary search over end[].
+enum ListId : int { kListRow = 0, kListTile = 1, kListMerge = 2, kListZero = 3, kNumLists = 4 };
+
+struct PlanHeader {
+  long long n[kNumLists];       // total entries per list
+  unsigned long long counter[8];  // dynamic work counters, reset by the planner
+  int qsl_bad;                  // query_start_loc failed its checks
+  int split_len_decode;         // chosen decode split length
+  long long partial_rows;       // partial rows the plan uses
+};
+
+// Device pointers into the workspace plus the call's scalars.
+struct FwdParams {
+  const void *q;
+  void *out;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const int32_t *qsl;
+  int num_seqs, num_tokens, num_heads, num_kv_heads, head_dim, block_size;
+  int max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
+  float scale;
+  float scale_log2;   // scale * log2(e): scores kept in the base-2 domain
+  int tile_ok;        // extend/prefill rows go to the tensor-core tile kernel
+  int row_ctas;       // resident CTAs of the row kernel (split sizing)
+  int dtype;          // pa_dtype
+  // workspace
+  PlanHeader *plan;
+  ReqInfo *req;
+  int *ord;                 // [num_seqs] request index at each reordered position
+  long long *list_end;      // [kNumLists][num_seqs]
+  float *part_o;            // [part_cap][head_dim]
+  float *part_lse;          // [part_cap] (base-2 log-sum-exp; NaN marks a bad split)
+  long long part_cap;
+  unsigned int *status;
+};
+
+// Largest split length of the row kernel (bounds its per-item page list).
+constexpr int kRowMaxSplit = 8192;
+constexpr int kRowMinSplit = 256;
+// Rows per tensor-core tile of the extend/prefill kernel.
+constexpr int kTileRows = 128;
+
+__host__ __device__ inline long long ceil_div_ll(long long a, long long b) {
+  return (a + b - 1) / b;
+}
+
+// Index of the list entry: first k with end[k] > idx (end is non-decreasing).
+__device__ inline int list_find(const long long *end, int n, long long idx) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (__ldg(end + mid) > idx) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ inline uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ inline void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ inline void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ inline void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ inline void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+__device__ inline void mbar_arrive(uint64_t *bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ inline bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ inline uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wall-clock limit of one bounded wait.  A wait that runs out sets
+// PA_DEV_TIMEOUT and the caller carries on (results are then flagged as
+// garbage by the status word); `dead` makes every later wait of the same
+// thread return at once so a kernel whose copies never land still ends.
+constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+
+__device__ inline void mbar_wait(uint64_t *bar, uint32_t parity, bool &dead,
+                                 unsigned int *status) {
+  if (dead) return;
+  if (mbar_try_wait(bar, parity)) return;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return;
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, PA_DEV_TIMEOUT);
+      dead = true;
+      return;
+    }
+  }
+}
+
+// 4-D tiled TMA load global -> shared, completion counted on `bar`.
+__device__ inline void tma_load_4d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                   int c3, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ inline void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                   uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ inline void prefetch_tensor_map(const CUtensorMap *map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// Hardware base-2 exponential (MUFU), used for softmax weights.
+__device__ inline float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// bf16x2 packed in a 32-bit word -> two floats (bf16 is the top half of fp32).
+__device__ inline float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ inline float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// ---------------------------------------------------------------------------
+// Block-wide inclusive scan of 64-bit counts (blockDim.x a multiple of 32,
+// at most 1024).  `scratch` holds 33 long longs.  Returns the inclusive
+// prefix of `v`; *total receives the block total.  All threads must call.
+// ---------------------------------------------------------------------------
+__device__ inline long long block_inclusive_scan(long long v, long long *scratch,
+                                                 long long *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+  long long x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    long long y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    long long w = lane < nwarps ? scratch[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      long long y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < nwarps) scratch[lane] = w;
+    if (lane == nwarps - 1) scratch[32] = w;
+  }
+  __syncthreads();
+  if (warp > 0) x += scratch[warp - 1];
+  *total = scratch[32];
+  __syncthreads();
+  return x;
+}
+
+}  // namespace pa

@@ -1,0 +1,449 @@
+// pa_rows.cu -- the row-streaming kernel: one work item is one query token of
+// one request, all G query heads of one KV head (the GQA group), over one KV
+// split.  It carries the decode path, which is bound by HBM bandwidth
+// ("vLLM AMD ROCm attention backend optimisation", section "Mixed inference
+// workload challenge": decode is memory-bound; "vLLM Triton attention backend
+// deep dive", section "Parallel tiled softmax (3D kernel)": the KV walk of a
+// single-token query is split across instances that write partial results).
+//
+// Design (GB300):
+//  * Page-gather loader: one thread issues 4-D TMA box copies
+//    {head_dim x 1 kv head x 16 slots x 1 page} of K and V straight from the
+//    page named by the block table into a ring of shared-memory stages (16-byte
+//    aligned rows, fully coalesced HBM reads), completion counted on mbarriers.
+//  * GQA packer: the G heads of a KV head live in the same CTA, so every K/V
+//    byte fetched from HBM feeds all G heads.
+//  * Compute: CUDA-core FFMA in fp32.  Thread (token slot, head group, lane c)
+//    holds HPT heads x DPT dims of q and of its output accumulator; the LPT
+//    lanes of a token reduce their partial dot products with a transpose-
+//    reduce of warp shuffles (HPT-1 + log2(LPT/HPT) shuffles, then HPT
+//    broadcasts) instead of HPT full butterflies.
+//  * Online softmax per thread over the tokens of its slot, in base 2, with
+//    lazy rescaling: the running max moves only when a score exceeds it by
+//    more than 8 (weights stay <= 256), so the O(HPT*DPT) rescale is rare.
+//  * End of item: the token slots' (m, l, O) are merged through shared memory
+//    (a log-sum-exp merge inside the CTA) and written either straight to the
+//    output (the row's KV fits one split) or as a split partial.
+//  * Persistent fixed grid; items come from a device counter.
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr float kLazyRescale = 8.0f;  // base-2 headroom before the max moves
+
+__device__ inline void load_vec(const float *src, float *f) {
+  const float4 v = *reinterpret_cast<const float4 *>(src);
+  f[0] = v.x;
+  f[1] = v.y;
+  f[2] = v.z;
+  f[3] = v.w;
+}
+
+__device__ inline void load_vec(const __nv_bfloat16 *src, float *f) {
+  const uint4 v = *reinterpret_cast<const uint4 *>(src);
+  f[0] = bf16lo(v.x);
+  f[1] = bf16hi(v.x);
+  f[2] = bf16lo(v.y);
+  f[3] = bf16hi(v.y);
+  f[4] = bf16lo(v.z);
+  f[5] = bf16hi(v.z);
+  f[6] = bf16lo(v.w);
+  f[7] = bf16hi(v.w);
+}
+
+__device__ inline void store_elem(float *dst, float v) { *dst = v; }
+__device__ inline void store_elem(__nv_bfloat16 *dst, float v) { *dst = __float2bfloat16_rn(v); }
+
+template <typename T, int D, int G>
+struct RowCfg {
+  static constexpr int E = 16 / static_cast<int>(sizeof(T));  // elements per 16-B vector
+  static constexpr int HPT = G < 8 ? G : 8;                    // heads per thread
+  static constexpr int HG = G / HPT;                           // head groups per token
+  static constexpr int DPT0 = (64 / HPT) < (D / 4) ? (64 / HPT) : (D / 4);
+  static constexpr int DPT = DPT0 > E ? DPT0 : E;              // dims per thread
+  static constexpr int VPT = DPT / E;                          // vectors per thread
+  static constexpr int LPT = D / DPT;                          // lanes per (token, head group)
+  static constexpr int LANES_TOK = LPT * HG;                   // lanes per token
+  static constexpr int TPW = 32 / LANES_TOK;                   // tokens per warp
+  static constexpr int NWARP = 4;
+  static constexpr int NTHREADS = 32 * NWARP;
+  static constexpr int TPS = TPW * NWARP;                      // tokens per step
+  static constexpr int BOX = 16;                               // slots per TMA box
+  static constexpr int ST = TPS > BOX ? TPS : BOX;             // tokens per stage
+  static constexpr int NBOX = ST / BOX;
+  static constexpr int ROWB = D * static_cast<int>(sizeof(T));
+  static constexpr int HALF_STAGE = ST * ROWB;
+  static constexpr int STAGE_BYTES = 2 * HALF_STAGE;
+  static constexpr int NSTAGE = (48 * 1024 / STAGE_BYTES) < 3 ? 3 : (48 * 1024 / STAGE_BYTES);
+  static constexpr int SCRATCH_O = TPS * G * D * 4;
+  static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
+  static constexpr int ALIAS_BYTES = RING_BYTES > SCRATCH_O ? RING_BYTES : SCRATCH_O;
+  static constexpr int MAX_PAGES = kRowMaxSplit / BOX + 2;
+  static constexpr int OFF_ML = ALIAS_BYTES;
+  static constexpr int OFF_PAGES = OFF_ML + 2 * TPS * G * 4;
+  static constexpr int OFF_BAR = (OFF_PAGES + MAX_PAGES * 4 + 15) / 16 * 16;
+  static constexpr int OFF_MISC = OFF_BAR + 2 * NSTAGE * 8;
+  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr int OPT = (G * D + NTHREADS - 1) / NTHREADS;  // outputs per thread
+  static constexpr int LOG2_HPT = HPT == 1 ? 0 : HPT == 2 ? 1 : HPT == 4 ? 2 : 3;
+  static_assert(LPT >= HPT, "transpose-reduce needs at least HPT lanes per token");
+  static_assert(32 % LANES_TOK == 0, "token groups must tile a warp");
+  static_assert(DPT % E == 0 && D % DPT == 0, "dims must split into 16-byte vectors");
+  static_assert(HPT * DPT <= 64, "register budget");
+  static_assert(D % OPT == 0 || G * D <= NTHREADS, "outputs per thread must not straddle heads");
+};
+
+// Sum the HPT partial dot products of the LPT lanes of one (token, head
+// group) and hand every lane all HPT totals.
+template <int HPT, int LPT, int LOG2_HPT>
+__device__ inline void reduce_scores(const float (&part)[HPT], float (&score)[HPT], int lane,
+                                     int c) {
+  float v[HPT];
+#pragma unroll
+  for (int h = 0; h < HPT; ++h) v[h] = part[h];
+#pragma unroll
+  for (int lvl = 0; lvl < LOG2_HPT; ++lvl) {
+    const int o = LPT >> (lvl + 1);
+    const int n = HPT >> lvl;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+#pragma unroll
+  for (int o = LPT / HPT / 2; o >= 1; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+  // Lane c now holds the total of head c / (LPT / HPT).
+  const int base = lane - c;
+#pragma unroll
+  for (int h = 0; h < HPT; ++h)
+    score[h] = __shfl_sync(0xffffffffu, v[0], base + h * (LPT / HPT));
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(128) row_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                  const __grid_constant__ CUtensorMap tm_v,
+                                                  const FwdParams p) {
+  using C = RowCfg<T, D, G>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  uint8_t *ring = smem;
+  float *s_m = reinterpret_cast<float *>(smem + C::OFF_ML);
+  float *s_l = s_m + C::TPS * G;
+  int *s_pages = reinterpret_cast<int *>(smem + C::OFF_PAGES);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *empty = full + C::NSTAGE;
+  long long *s_item = reinterpret_cast<long long *>(smem + C::OFF_MISC);
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = warp * C::TPW + lane / C::LANES_TOK;
+  const int hg = (lane % C::LANES_TOK) / C::LPT;
+  const int c = lane % C::LPT;
+
+  if (tid == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], C::NWARP);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  bool dead = false;
+  uint32_t g0 = 0;  // global index of the current item's first stage
+  const long long n_items = p.plan->n[kListRow];
+  const int S = p.num_seqs, H = p.num_heads, bs = p.block_size;
+  const long long *row_end = p.list_end + (size_t)kListRow * S;
+
+  for (uint32_t iter = 0;; ++iter) {
+    // Double-buffered broadcast: a slot is rewritten only two iterations
+    // later, after every thread has passed the barrier in between.
+    if (tid == 0) s_item[iter & 1] = (long long)atomicAdd(&p.plan->counter[kListRow], 1ull);
+    __syncthreads();
+    const long long item = s_item[iter & 1];
+    if (item >= n_items) break;
+
+    // ---- decode the work item -------------------------------------------
+    const int k = list_find(row_end, S, item);
+    const long long start = k ? row_end[k - 1] : 0;
+    const int s = p.ord[k];
+    const ReqInfo r = p.req[s];
+    const long long local = item - start;
+    const long long per_kvh = (long long)r.nsplit * r.q_len;
+    const int kvh = (int)(local / per_kvh);
+    const int rem = (int)(local % per_kvh);
+    const int split = rem / r.q_len;
+    const int i = rem % r.q_len;
+    const int tok = r.q_start + i;
+    const int kv_row_hi = r.ctx - r.q_len + i + 1;  // causal: positions 0 .. prefix + i
+    const int kv_lo = split * r.split_len;
+    const int kv_hi = min(kv_row_hi, kv_lo + r.split_len);
+    if (kv_lo >= kv_hi) continue;  // this split lies past the row's causal bound
+    const bool direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
+    const long long prow0 = r.partial_base + ((long long)i * H + kvh * G) * r.nsplit + split;
+
+    // ---- page list of the split ------------------------------------------
+    const int pfirst = kv_lo / bs;
+    const int npages = (kv_hi - 1) / bs - pfirst + 1;
+    const int32_t *bt = p.block_table + (size_t)s * p.max_blocks_per_seq;
+    int bad = 0;
+    for (int j = tid; j < npages; j += C::NTHREADS) {
+      const int lp = pfirst + j;
+      const int pid = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
+      if (pid < 0 || pid >= p.num_blocks) bad = 1;
+      s_pages[j] = pid;
+    }
+    bad = __syncthreads_or(bad);
+    if (bad) {
+      if (tid == 0) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+      for (int e = tid; e < G * D; e += C::NTHREADS) {
+        const int h = e / D, d = e % D;
+        if (direct) {
+          store_elem(reinterpret_cast<T *>(p.out) + ((size_t)tok * H + kvh * G + h) * D + d, 0.f);
+        } else {
+          const long long prow = prow0 + (long long)h * r.nsplit;
+          p.part_o[prow * D + d] = 0.f;
+          if (d == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
+        }
+      }
+      continue;
+    }
+
+    // ---- q of this thread's heads and dims, pre-scaled to base 2 -----------
+    float qv[C::HPT][C::DPT];
+    const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)tok * H + kvh * G + hg * C::HPT) * D;
+#pragma unroll
+    for (int h = 0; h < C::HPT; ++h)
+#pragma unroll
+      for (int v = 0; v < C::VPT; ++v) {
+        load_vec(qrow + h * D + (c + v * C::LPT) * C::E, &qv[h][v * C::E]);
+#pragma unroll
+        for (int e = 0; e < C::E; ++e) qv[h][v * C::E + e] *= p.scale_log2;
+      }
+    float m[C::HPT], l[C::HPT], o[C::HPT][C::DPT];
+#pragma unroll
+    for (int h = 0; h < C::HPT; ++h) {
+      m[h] = -INFINITY;
+      l[h] = 0.f;
+#pragma unroll
+      for (int d = 0; d < C::DPT; ++d) o[h][d] = 0.f;
+    }
+
+    // ---- TMA pipeline over the split's stages ------------------------------
+    const int nst = (kv_hi - kv_lo + C::ST - 1) / C::ST;
+    auto issue = [&](int j) {
+      const uint32_t g = g0 + j;
+      const int b = g % C::NSTAGE;
+      if (g >= C::NSTAGE) mbar_wait(&empty[b], ((g / C::NSTAGE) - 1) & 1, dead, p.status);
+      const int pos0 = kv_lo + j * C::ST;
+      int nbox = 0;
+#pragma unroll
+      for (int x = 0; x < C::NBOX; ++x) nbox += (pos0 + x * C::BOX < kv_hi) ? 1 : 0;
+      mbar_arrive_expect_tx(&full[b], nbox * 2 * C::BOX * C::ROWB);
+      uint8_t *kb = ring + b * C::STAGE_BYTES;
+      uint8_t *vb = kb + C::HALF_STAGE;
+      for (int x = 0; x < nbox; ++x) {
+        const int pos = pos0 + x * C::BOX;
+        const int page = s_pages[pos / bs - pfirst];
+        const int slot0 = pos % bs;
+        tma_load_4d(kb + x * C::BOX * C::ROWB, &tm_k, 0, kvh, slot0, page, &full[b]);
+        tma_load_4d(vb + x * C::BOX * C::ROWB, &tm_v, 0, kvh, slot0, page, &full[b]);
+      }
+    };
+    if (tid == 0) {
+      fence_proxy_async();
+      const int pre = nst < C::NSTAGE - 1 ? nst : C::NSTAGE - 1;
+      for (int j = 0; j < pre; ++j) issue(j);
+    }
+
+    for (int j = 0; j < nst; ++j) {
+      if (tid == 0 && j + C::NSTAGE - 1 < nst) issue(j + C::NSTAGE - 1);
+      const uint32_t g = g0 + j;
+      const int b = g % C::NSTAGE;
+      mbar_wait(&full[b], (g / C::NSTAGE) & 1, dead, p.status);
+      const T *kb = reinterpret_cast<const T *>(ring + b * C::STAGE_BYTES);
+      const T *vb = kb + C::ST * D;
+#pragma unroll
+      for (int sub = 0; sub < C::ST / C::TPS; ++sub) {
+        const int tl = sub * C::TPS + slot;
+        const bool valid = kv_lo + j * C::ST + tl < kv_hi;
+        float kf[C::DPT];
+#pragma unroll
+        for (int v = 0; v < C::VPT; ++v)
+          load_vec(kb + tl * D + (c + v * C::LPT) * C::E, &kf[v * C::E]);
+        float part[C::HPT];
+#pragma unroll
+        for (int h = 0; h < C::HPT; ++h) {
+          float acc = 0.f;
+#pragma unroll
+          for (int d = 0; d < C::DPT; ++d) acc = fmaf(qv[h][d], kf[d], acc);
+          part[h] = acc;
+        }
+        float sc[C::HPT];
+        reduce_scores<C::HPT, C::LPT, C::LOG2_HPT>(part, sc, lane, c);
+        if (valid) {
+          float vf[C::DPT];
+#pragma unroll
+          for (int v = 0; v < C::VPT; ++v)
+            load_vec(vb + tl * D + (c + v * C::LPT) * C::E, &vf[v * C::E]);
+#pragma unroll
+          for (int h = 0; h < C::HPT; ++h) {
+            if (sc[h] > m[h] + kLazyRescale) {
+              const float a = fast_exp2(m[h] - sc[h]);
+              l[h] *= a;
+#pragma unroll
+              for (int d = 0; d < C::DPT; ++d) o[h][d] *= a;
+              m[h] = sc[h];
+            }
+            const float pr = fast_exp2(sc[h] - m[h]);
+            l[h] += pr;
+#pragma unroll
+            for (int d = 0; d < C::DPT; ++d) o[h][d] = fmaf(pr, vf[d], o[h][d]);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[b]);
+    }
+    g0 += nst;
+
+    // ---- merge the token slots and write ------------------------------------
+    __syncthreads();  // the ring is free; it becomes merge scratch
+    float *s_o = reinterpret_cast<float *>(ring);
+#pragma unroll
+    for (int h = 0; h < C::HPT; ++h) {
+      const int head = hg * C::HPT + h;
+#pragma unroll
+      for (int v = 0; v < C::VPT; ++v)
+#pragma unroll
+        for (int e = 0; e < C::E; ++e)
+          s_o[(slot * G + head) * D + (c + v * C::LPT) * C::E + e] = o[h][v * C::E + e];
+      if (c == 0) {
+        s_m[slot * G + head] = m[h];
+        s_l[slot * G + head] = l[h];
+      }
+    }
+    __syncthreads();
+    const int e0 = tid * C::OPT;
+    if (e0 < G * D) {
+      const int h = e0 / D, d0 = e0 % D;
+      float M = -INFINITY;
+      for (int sl = 0; sl < C::TPS; ++sl) M = fmaxf(M, s_m[sl * G + h]);
+      float L = 0.f, acc[C::OPT];
+#pragma unroll
+      for (int x = 0; x < C::OPT; ++x) acc[x] = 0.f;
+      for (int sl = 0; sl < C::TPS; ++sl) {
+        const float ms = s_m[sl * G + h];
+        if (ms == -INFINITY) continue;
+        const float w = fast_exp2(ms - M);
+        L = fmaf(s_l[sl * G + h], w, L);
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) acc[x] = fmaf(s_o[(sl * G + h) * D + d0 + x], w, acc[x]);
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      if (direct) {
+        T *dst = reinterpret_cast<T *>(p.out) + ((size_t)tok * H + kvh * G + h) * D + d0;
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) store_elem(dst + x, acc[x] * inv);
+      } else {
+        const long long prow = prow0 + (long long)h * r.nsplit;
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) p.part_o[prow * D + d0 + x] = acc[x] * inv;
+        if (d0 == 0) p.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
+      }
+    }
+    fence_proxy_async();  // generic use of the ring ends before TMA refills it
+    __syncthreads();
+  }
+}
+
+template <typename T, int D, int G>
+cudaError_t launch_one(const FwdParams &p, const CUtensorMap &tk, const CUtensorMap &tv,
+                       int grid, cudaStream_t stream) {
+  using C = RowCfg<T, D, G>;
+  cudaError_t err = cudaFuncSetAttribute(row_kernel<T, D, G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (err != cudaSuccess) return err;
+  row_kernel<T, D, G><<<grid, C::NTHREADS, C::SMEM, stream>>>(tk, tv, p);
+  return cudaGetLastError();
+}
+
+template <typename T, int D, int G>
+int occupancy_one() {
+  using C = RowCfg<T, D, G>;
+  if (cudaFuncSetAttribute(row_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           C::SMEM) != cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_kernel<T, D, G>, C::NTHREADS,
+                                                    C::SMEM) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+// Dispatch over (dtype, head_dim, group); Fn is called with the instantiation.
+template <typename Fn>
+bool dispatch(int dtype, int head_dim, int group, Fn &&fn) {
+#define PA_ROW_CASE(T, D, G) \
+  if (head_dim == D && group == G) { fn.template operator()<T, D, G>(); return true; }
+#define PA_ROW_GROUPS(T, D) \
+  PA_ROW_CASE(T, D, 1) PA_ROW_CASE(T, D, 2) PA_ROW_CASE(T, D, 4) PA_ROW_CASE(T, D, 8) \
+  PA_ROW_CASE(T, D, 16)
+  if (dtype == PA_BF16) {
+    PA_ROW_GROUPS(__nv_bfloat16, 64)
+    PA_ROW_GROUPS(__nv_bfloat16, 128)
+  } else if (dtype == PA_F32) {
+    PA_ROW_GROUPS(float, 64)
+    PA_ROW_GROUPS(float, 128)
+  }
+#undef PA_ROW_GROUPS
+#undef PA_ROW_CASE
+  return false;
+}
+
+struct NopFn {
+  template <typename T, int D, int G>
+  void operator()() {}
+};
+
+struct OccFn {
+  int n = 0;
+  template <typename T, int D, int G>
+  void operator()() { n = occupancy_one<T, D, G>(); }
+};
+
+struct LaunchFn {
+  const FwdParams &p;
+  const CUtensorMap &tk, &tv;
+  int grid;
+  cudaStream_t stream;
+  cudaError_t err;
+  template <typename T, int D, int G>
+  void operator()() { err = launch_one<T, D, G>(p, tk, tv, grid, stream); }
+};
+
+}  // namespace
+
+bool row_kernel_supported(int dtype, int head_dim, int group) {
+  NopFn nop;
+  return dispatch(dtype, head_dim, group, nop);
+}
+
+int row_kernel_ctas_per_sm(int dtype, int head_dim, int group) {
+  OccFn occ;
+  dispatch(dtype, head_dim, group, occ);
+  return occ.n;
+}
+
+cudaError_t launch_row_kernel(const FwdParams &p, const CUtensorMap &tm_k,
+                              const CUtensorMap &tm_v, int grid, cudaStream_t stream) {
+  LaunchFn l{p, tm_k, tm_v, grid, stream, cudaErrorInvalidValue};
+  dispatch(p.dtype, p.head_dim, p.num_heads / p.num_kv_heads, l);
+  return l.err;
+}
+
+}  // namespace pa

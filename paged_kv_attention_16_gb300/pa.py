@@ -1,0 +1,239 @@
+"""Thin ctypes binding over libpa.so (include/pa.h).
+
+Argument marshalling only: every step of the attention runs in the CUDA
+library.  Functions keep the C names and argument order; tensors are passed
+as torch tensors (their device pointers are handed to the library) or raw
+integer addresses.  There is no fallback: if libpa.so is missing or fails to
+load, every call raises.
+"""
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
+
+PA_F32, PA_BF16 = 0, 1
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_DEV_BAD_BLOCK = 0x1
+PA_DEV_BAD_QLEN = 0x2
+PA_DEV_BAD_SEQLEN = 0x4
+PA_DEV_BAD_QSL = 0x8
+PA_DEV_OVERFLOW = 0x10
+PA_DEV_TIMEOUT = 0x20
+
+# Every entry point declared in include/pa.h.
+EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode",
+           "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
+           "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
+           "pa_profile_read", "pa_kernel_name")
+PA_K_COUNT = 8
+
+
+class PaError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+
+
+def lib():
+    """The loaded libpa.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(f"libpa.so not found at {_LIB_PATH}; build it with "
+                               "paged_kv_attention_16_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32p, c_int, c_float = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        L.pa_forward.argtypes = [vp, vp, vp, i32p, i32p, i32p, c_int, c_int, c_int, c_int,
+                                 c_float, vp, vp, c_int, c_int, c_int, c_int, c_int, c_int, c_int]
+        L.pa_forward.restype = c_int
+        L.pa_forward_workspace_bytes.argtypes = [c_int] * 8
+        L.pa_forward_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_mla_decode.argtypes = [vp, vp, i32p, i32p, c_int, c_int, c_int, c_int, c_float, vp,
+                                    vp, c_int, c_int, c_int, c_int, c_int]
+        L.pa_mla_decode.restype = c_int
+        L.pa_mla_decode_workspace_bytes.argtypes = [c_int] * 5
+        L.pa_mla_decode_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_reserve.argtypes = [ctypes.c_size_t]
+        L.pa_reserve.restype = c_int
+        L.pa_get_device_status.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+        L.pa_get_device_status.restype = c_int
+        L.pa_status_string.argtypes = [c_int]
+        L.pa_status_string.restype = ctypes.c_char_p
+        L.pa_num_sms.argtypes = []
+        L.pa_num_sms.restype = c_int
+        L.pa_debug_gather.argtypes = [vp, i32p, i32p, c_int, c_int, c_int, c_int, c_int, c_int,
+                                      c_int, vp, vp]
+        L.pa_debug_gather.restype = c_int
+        L.pa_profile_enable.argtypes = [c_int]
+        L.pa_profile_enable.restype = c_int
+        L.pa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)]
+        L.pa_profile_read.restype = c_int
+        L.pa_kernel_name.argtypes = [c_int]
+        L.pa_kernel_name.restype = ctypes.c_char_p
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t):
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _check(status, where):
+    if status != PA_OK:
+        raise PaError(status, where)
+
+
+def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
+               num_kv_heads, head_dim, block_size, scale, out, stream=None, *, max_seq_len,
+               kv_split_tokens=0, num_blocks=None, check=True):
+    """Unified paged attention (see include/pa.h).  Shapes are read from the
+    tensors; max_seq_len is the host-known bound on seq_lens."""
+    st = lib().pa_forward(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(query_start_loc), int(num_heads), int(num_kv_heads), int(head_dim),
+        int(block_size), float(scale), _ptr(out), _stream_ptr(stream), _dtype_code(q),
+        int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
+        int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
+        int(kv_split_tokens))
+    if check:
+        _check(st, "pa_forward")
+    return st
+
+
+def pa_forward_workspace_bytes(dtype, num_seqs, num_tokens, num_heads, num_kv_heads, head_dim,
+                               max_seq_len, kv_split_tokens=0):
+    return lib().pa_forward_workspace_bytes(int(dtype), int(num_seqs), int(num_tokens),
+                                            int(num_heads), int(num_kv_heads), int(head_dim),
+                                            int(max_seq_len), int(kv_split_tokens))
+
+
+def pa_mla_decode(q, kv_cache, block_table, seq_lens, num_heads, kv_lora_rank, rope_dim,
+                  block_size, scale, out, stream=None, *, max_seq_len, kv_split_tokens=0,
+                  check=True):
+    st = lib().pa_mla_decode(
+        _ptr(q), _ptr(kv_cache), _ptr(block_table), _ptr(seq_lens), int(num_heads),
+        int(kv_lora_rank), int(rope_dim), int(block_size), float(scale), _ptr(out),
+        _stream_ptr(stream), int(seq_lens.shape[0]), int(block_table.shape[1]),
+        int(kv_cache.shape[0]), int(max_seq_len), int(kv_split_tokens))
+    if check:
+        _check(st, "pa_mla_decode")
+    return st
+
+
+def pa_mla_decode_workspace_bytes(num_seqs, num_heads, kv_lora_rank, max_seq_len,
+                                  kv_split_tokens=0):
+    return lib().pa_mla_decode_workspace_bytes(int(num_seqs), int(num_heads),
+                                               int(kv_lora_rank), int(max_seq_len),
+                                               int(kv_split_tokens))
+
+
+def pa_reserve(nbytes):
+    _check(lib().pa_reserve(int(nbytes)), "pa_reserve")
+
+
+def pa_get_device_status(stream=None):
+    v = ctypes.c_uint32(0)
+    _check(lib().pa_get_device_status(_stream_ptr(stream), ctypes.byref(v)),
+           "pa_get_device_status")
+    return int(v.value)
+
+
+def pa_profile_enable(on=True):
+    _check(lib().pa_profile_enable(1 if on else 0), "pa_profile_enable")
+
+
+def pa_profile_read():
+    """{kernel name: (total ms, launches)} of the launches timed since the
+    last read (synchronises)."""
+    ms = (ctypes.c_double * PA_K_COUNT)()
+    n = (ctypes.c_int * PA_K_COUNT)()
+    _check(lib().pa_profile_read(ms, n), "pa_profile_read")
+    out = {}
+    for i in range(PA_K_COUNT):
+        if n[i]:
+            out[pa_kernel_name(i)] = (float(ms[i]), int(n[i]))
+    return out
+
+
+def pa_kernel_name(kernel_id):
+    return lib().pa_kernel_name(int(kernel_id)).decode()
+
+
+def pa_num_sms():
+    return int(lib().pa_num_sms())
+
+
+def pa_debug_gather(k_cache, block_table, seq_lens, block_size, max_seq_len, dense_out,
+                    stream=None):
+    row_elems = int(k_cache[0, 0].numel())
+    st = lib().pa_debug_gather(_ptr(k_cache), _ptr(block_table), _ptr(seq_lens),
+                               int(seq_lens.shape[0]), int(block_table.shape[1]),
+                               int(k_cache.shape[0]), int(block_size), row_elems,
+                               int(k_cache.element_size()), int(max_seq_len), _ptr(dense_out),
+                               _stream_ptr(stream))
+    _check(st, "pa_debug_gather")
+
+
+# ---------------------------------------------------------------------------
+# conveniences over the batches of paged_kv_attention_16_gb300.inputs
+# ---------------------------------------------------------------------------
+
+def to_device(batch, device="cuda"):
+    """Copy every tensor field of a PagedBatch / MlaBatch to `device`."""
+    import dataclasses
+    fields = {}
+    for f in dataclasses.fields(batch):
+        v = getattr(batch, f.name)
+        fields[f.name] = v.to(device) if isinstance(v, torch.Tensor) else v
+    return type(batch)(**fields)
+
+
+def forward(b, out=None, stream=None, kv_split_tokens=None):
+    """pa_forward on a device-resident PagedBatch; returns `out`."""
+    if out is None:
+        out = torch.empty_like(b.q)
+    pa_forward(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc,
+               b.num_heads, b.num_kv_heads, b.head_dim, b.block_size, b.scale, out, stream,
+               max_seq_len=b.max_seq_len,
+               kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens)
+    return out
+
+
+def mla_decode(b, out=None, stream=None):
+    """pa_mla_decode on a device-resident MlaBatch; returns `out`."""
+    if out is None:
+        out = torch.empty((b.num_seqs, b.num_heads, b.kv_lora_rank), dtype=b.q.dtype,
+                          device=b.q.device)
+    pa_mla_decode(b.q, b.kv_cache, b.block_table, b.seq_lens, b.num_heads, b.kv_lora_rank,
+                  b.rope_dim, b.block_size, b.scale, out, stream, max_seq_len=b.max_seq_len,
+                  kv_split_tokens=b.kv_split_tokens)
+    return out

@@ -1,0 +1,71 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
+and the fp64 oracle on the same seeded inputs, compare element by element."""
+import numpy as np
+import torch
+
+from oracle import oracle as orc
+from paged_kv_attention_16_gb300 import inputs, pa
+
+# Tolerances fixed for this method: fp32 inputs within max-abs 1e-4; bf16
+# storage with fp32 accumulation within max-abs 2e-2 and mean-abs 2e-3.
+TOL = {"f32": dict(max_abs=1e-4, mean_abs=1e-4), "bf16": dict(max_abs=2e-2, mean_abs=2e-3)}
+
+
+def oracle_forward(b, rows=None):
+    return orc.paged_attention(
+        inputs.storage_array(b.q), inputs.storage_array(b.k_cache),
+        inputs.storage_array(b.v_cache), b.block_table.numpy(), b.seq_lens.numpy(),
+        b.query_start_loc.numpy(), b.num_heads, b.num_kv_heads, b.head_dim, b.block_size,
+        b.scale, rows=rows)
+
+
+def oracle_mla(b, rows=None):
+    return orc.mla_decode(inputs.storage_array(b.q), inputs.storage_array(b.kv_cache),
+                          b.block_table.numpy(), b.seq_lens.numpy(), b.kv_lora_rank, b.rope_dim,
+                          b.block_size, b.scale, rows=rows)
+
+
+def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0):
+    d = pa.to_device(b)
+    got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens)
+    status = pa.pa_get_device_status()
+    assert status == expect_status, f"device status {status:#x}, expected {expect_status:#x}"
+    return got.float().cpu().numpy().astype(np.float64)
+
+
+def compare(got, want, dtype, rows=None, what=""):
+    """Element-wise comparison on the listed flat (token*H + head) rows."""
+    g = got.reshape(-1, got.shape[-1])
+    w = want.reshape(-1, want.shape[-1])
+    if rows is not None:
+        g, w = g[rows], w[rows]
+    assert np.isfinite(w).all(), "oracle produced non-finite values"
+    assert np.isfinite(g).all(), f"{what}: GPU produced non-finite values"
+    err = np.abs(g - w)
+    tol = TOL[dtype]
+    max_abs, mean_abs = float(err.max()) if err.size else 0.0, float(err.mean()) if err.size else 0.0
+    assert max_abs <= tol["max_abs"], f"{what}: max-abs {max_abs:.3e} > {tol['max_abs']}"
+    assert mean_abs <= tol["mean_abs"], f"{what}: mean-abs {mean_abs:.3e} > {tol['mean_abs']}"
+    return max_abs, mean_abs
+
+
+def sample_rows(b, n_other, seed=0, all_decode=True):
+    """All rows of decode requests plus n_other random rows of the rest."""
+    H = b.num_heads
+    qsl = b.query_start_loc.numpy()
+    dec, other = [], []
+    for s in range(b.num_seqs):
+        toks = np.arange(qsl[s], qsl[s + 1])
+        rows = (toks[:, None] * H + np.arange(H)[None, :]).ravel()
+        (dec if qsl[s + 1] - qsl[s] == 1 else other).append(rows)
+    dec = np.concatenate(dec) if dec else np.zeros(0, np.int64)
+    other = np.concatenate(other) if other else np.zeros(0, np.int64)
+    rng = np.random.default_rng(seed)
+    if len(other) > n_other:
+        other = rng.choice(other, n_other, replace=False)
+    rows = np.concatenate([dec if all_decode else dec[:0], other]).astype(np.int64)
+    return np.sort(rows)
+
+
+def cuda_ok():
+    return torch.cuda.is_available()

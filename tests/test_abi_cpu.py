@@ -1,0 +1,80 @@
+"""libpa.so loads and exports every entry point include/pa.h declares, and
+its host-side argument checks answer without touching a GPU (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_kv_attention_16_gb300 import build as pbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "pa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return ctypes.CDLL(pbuild.build())
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("pa_forward", "pa_mla_decode", "pa_reserve", "pa_get_device_status",
+                 "pa_status_string", "pa_debug_gather"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_lists_every_export():
+    from paged_kv_attention_16_gb300 import pa
+    assert sorted(pa.EXPORTS) == declared_functions()
+
+
+def test_status_strings(lib):
+    lib.pa_status_string.restype = ctypes.c_char_p
+    assert lib.pa_status_string(0) == b"ok"
+    assert b"unsupported" in lib.pa_status_string(2)
+
+
+def _forward(lib, **kw):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, bt=1 << 20, sl=1 << 20, qsl=1 << 20, H=8, Hk=2,
+                D=128, bs=16, scale=0.1, out=1 << 20, stream=None, dtype=1, S=1, T=1, mbps=4,
+                nb=4, msl=64, kvs=0)
+    args.update(kw)
+    f = lib.pa_forward
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_float, vp, vp] + [ctypes.c_int] * 7
+    a = args
+    return f(a["q"], a["k"], a["v"], a["bt"], a["sl"], a["qsl"], a["H"], a["Hk"], a["D"], a["bs"],
+             a["scale"], a["out"], a["stream"], a["dtype"], a["S"], a["T"], a["mbps"], a["nb"],
+             a["msl"], a["kvs"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(H=0), 1), (dict(Hk=3), 1), (dict(S=-1), 1), (dict(dtype=7), 1),
+    (dict(D=96), 2), (dict(bs=8), 2), (dict(bs=512), 2), (dict(H=96, Hk=3), 2),
+    (dict(kvs=100), 2), (dict(T=0), 0), (dict(q=0), 1), (dict(out=(1 << 20) + 4), 1),
+])
+def test_host_argument_checks(lib, kw, want):
+    assert _forward(lib, **kw) == want
+
+
+def test_workspace_bytes_grow_with_splits(lib):
+    f = lib.pa_forward_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 8
+    small = f(1, 64, 64, 32, 8, 128, 8192, 0)
+    big = f(1, 64, 64, 32, 8, 128, 131072, 0)
+    assert 0 < small < big
