@@ -204,36 +204,50 @@ def secondary_workloads(pa, flush, peaks):
     hbm = peaks["hbm_gbs"]
     tfl = peaks["bf16_tflops"]
 
-    b = pa.to_device(inputs.llama_decode(1, poison=False))
+    hb = inputs.llama_decode(1, poison=False)
+    b = pa.to_device(hb)
     out = torch.empty_like(b.q)
     for _ in range(5):
         pa.forward(b, out=out)
     ms = time_per_step(lambda: pa.forward(b, out=out), 50, flush)
-    gbs = kv_bytes(b) / ms / 1e6
+    gbs = kv_bytes(hb) / ms / 1e6
     res["llama_decode_b1"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm,
                               "note": "2 MB of KV: launch-latency bound"}
     del b, out
 
-    b = pa.to_device(inputs.mixed_qwen3(poison=False))
+    hb = inputs.mixed_qwen3(poison=False)
+    b = pa.to_device(hb)
     out = torch.empty_like(b.q)
     pa.forward(b, out=out)
+    pa.pa_profile_enable(True)
+    pa.pa_profile_read()
     ms = time_per_step(lambda: pa.forward(b, out=out), 5, flush)
-    tf = attn_flops(b) / ms / 1e9
+    prof = pa.pa_profile_read()
+    pa.pa_profile_enable(False)
+    tf = attn_flops(hb) / ms / 1e9
     res["mixed_qwen3"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
-                          "kv_gbs": kv_bytes(b) / ms / 1e6,
-                          "tokens": b.num_tokens, "requests": b.num_seqs}
+                          "kv_gbs": kv_bytes(hb) / ms / 1e6,
+                          "tokens": hb.num_tokens, "requests": hb.num_seqs,
+                          "kernel_ms": {k: v[0] / v[1] for k, v in prof.items()}}
     del b, out
 
-    b = pa.to_device(inputs.long_chunked(poison=False))
+    hb = inputs.long_chunked(poison=False)
+    b = pa.to_device(hb)
     out = torch.empty_like(b.q)
     pa.forward(b, out=out)
+    pa.pa_profile_enable(True)
+    pa.pa_profile_read()
     ms = time_per_step(lambda: pa.forward(b, out=out), 5, flush)
-    tf = attn_flops(b) / ms / 1e9
+    prof = pa.pa_profile_read()
+    pa.pa_profile_enable(False)
+    tf = attn_flops(hb) / ms / 1e9
     res["long_chunked"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
-                           "kv_split_tokens": 32768}
+                           "kv_split_tokens": 32768,
+                           "kernel_ms": {k: v[0] / v[1] for k, v in prof.items()}}
     del b, out
 
-    m = pa.to_device(inputs.mla_decode_batch(poison=False))
+    hm = inputs.mla_decode_batch(poison=False)
+    m = pa.to_device(hm)
     out = torch.empty((m.num_seqs, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16,
                       device="cuda")
     st = pa.pa_mla_decode(m.q, m.kv_cache, m.block_table, m.seq_lens, m.num_heads,
@@ -241,8 +255,8 @@ def secondary_workloads(pa, flush, peaks):
                           max_seq_len=m.max_seq_len, check=False)
     if st == pa.PA_OK:
         ms = time_per_step(lambda: pa.mla_decode(m, out=out), 10, flush)
-        gbs = mla_bytes(m) / ms / 1e6
-        tf = mla_flops(m) / ms / 1e9
+        gbs = mla_bytes(hm) / ms / 1e6
+        tf = mla_flops(hm) / ms / 1e9
         res["mla_decode"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm, "tflops": tf,
                              "tensor_frac": tf / tfl}
     else:

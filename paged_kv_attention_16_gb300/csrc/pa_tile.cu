@@ -1,14 +1,438 @@
-// pa_tile.cu -- tensor-core (tcgen05) tile kernel for bf16 extend/prefill.
-// Until it lands, extend/prefill rows take the row-streaming kernel.
+// pa_tile.cu -- tensor-core tile kernel for bf16 extend / prefill rows.
+//
+// "vLLM Triton attention backend deep dive", section "Q-block optimisation":
+// several query tokens and heads are packed into one work item so the matrix
+// unit is fed and, under GQA, every KV page is read once for the whole group.
+// "vLLM AMD ROCm attention backend optimisation", section "Mixed inference
+// workload challenge": prefill is compute-bound, extend is hybrid; section
+// "Chunked context processing": long KV is walked in fixed chunks whose
+// partial results are merged by log-sum-exp.
+//
+// GB300 design.  One work item = 128 query rows (128/G tokens x the G heads of
+// one KV head, GQA-packed so the M = 128 MMA is full and the causal diagonal of
+// a tile is only 128/G positions wide) x one KV split.  Per CTA (2 per SM):
+//   warp 4   TMA producer: Q tile (128-byte swizzled boxes of G heads x 128/G
+//            tokens), then per 64-position KV tile the K and V page boxes
+//            {64 dims x 16 slots} named by the block table (K double-buffered,
+//            V one tile behind K);
+//   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
+//            K=head_dim, bf16 in, fp32 in TMEM), then O += P V (N=head_dim,
+//            K=64, V read MN-major straight from its page layout);
+//   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its S row,
+//            masks by select (causal bound, split bound), keeps a base-2
+//            online softmax with lazy rescaling of O in TMEM (only when the
+//            running max grows by more than 8), writes P as bf16 into the
+//            swizzled operand layout, and finally normalises O and stores the
+//            row (or a split partial with its log-sum-exp).
+// Tiles of a split that lie past every row's causal bound are never loaded.
 #include "pa_internal.h"
 
 namespace pa {
+namespace {
 
-bool tile_kernel_supported(int, int, int) { return false; }
+constexpr int kBN = 64;            // KV positions per tile
+constexpr int kBox = 16;           // slots per TMA box
+constexpr int kTileThreads = 192;  // 4 softmax warps, 1 producer warp, 1 MMA warp
+constexpr int kKStages = 2;
+constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemS = 0;     // S: columns [0, 64)
+constexpr uint32_t kTmemO = 64;    // O: columns [64, 64 + head_dim)
 
-cudaError_t launch_tile_kernel(const FwdParams &, const CUtensorMap &, const CUtensorMap &,
-                               const CUtensorMap &, int, cudaStream_t) {
-  return cudaErrorNotSupported;
+enum Bar {
+  kQFull = 0, kQFree, kKFull0, kKFull1, kKFree0, kKFree1, kVFull, kVFree,
+  kSFull, kSFree, kPFull, kODone, kOFree, kNumBars
+};
+
+template <int D>
+struct TileCfg {
+  static constexpr int NH = D / 64;                 // 128-byte halves of a row
+  static constexpr int Q_BYTES = NH * 128 * 128;    // 128 rows x 128 B per half
+  static constexpr int KV_HALF = kBN * 128;         // one half of a K or V tile
+  static constexpr int KV_BYTES = NH * KV_HALF;
+  static constexpr int P_BYTES = 128 * kBN * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
+  static constexpr int OFF_P = OFF_V + KV_BYTES;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
+  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, D, 1);
+};
+
+struct TileItem {
+  int s, kvh, split, t0;
+  int q_start, q_len, prefix, nsplit, split_len;
+  long long partial_base;
+  int kv_lo, kv_hi, nt;
+};
+
+__device__ inline bool decode_tile_item(const FwdParams &p, long long item, int G, TileItem &it) {
+  const int S = p.num_seqs;
+  const long long *end = p.list_end + (size_t)kListTile * S;
+  const int k = list_find(end, S, item);
+  const long long local = item - (k ? end[k - 1] : 0);
+  it.s = p.ord[k];
+  const ReqInfo r = p.req[it.s];
+  const int TQ = kTileRows / G;
+  const int ntiles = (r.q_len + TQ - 1) / TQ;
+  const long long per_kvh = (long long)ntiles * r.nsplit;
+  it.kvh = (int)(local / per_kvh);
+  const int rem = (int)(local % per_kvh);
+  const int qt = ntiles - 1 - rem / r.nsplit;  // tiles nearer the end see more KV: first
+  it.split = rem % r.nsplit;
+  it.t0 = qt * TQ;
+  it.q_start = r.q_start;
+  it.q_len = r.q_len;
+  it.prefix = r.ctx - r.q_len;
+  it.nsplit = r.nsplit;
+  it.split_len = r.split_len;
+  it.partial_base = r.partial_base;
+  const int t_last = min(it.t0 + TQ, r.q_len) - 1;
+  it.kv_lo = it.split * r.split_len;
+  it.kv_hi = min(it.kv_lo + r.split_len, it.prefix + t_last + 1);
+  it.nt = it.kv_hi > it.kv_lo ? (it.kv_hi - it.kv_lo + kBN - 1) / kBN : 0;
+  return it.nt > 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kTileThreads, 2)
+    tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+  using C = TileCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzled operand tiles need 1024-byte alignment.
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t *sQ = smem + C::OFF_Q;
+  uint8_t *sK = smem + C::OFF_K;
+  uint8_t *sV = smem + C::OFF_V;
+  uint8_t *sP = smem + C::OFF_P;
+  uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
+  int *s_bad = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = p.num_heads / p.num_kv_heads;
+  const int H = p.num_heads, bs = p.block_size;
+  const long long n_items = p.plan->n[kListTile];
+
+  if (tid == 0) {
+    prefetch_tensor_map(&tm_q);
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+    const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4};
+    for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], counts[b]);
+    fence_mbar_init();
+  }
+  if (warp == 5) tc_alloc(s_tmem, kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  bool dead = false;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------- producer
+    uint32_t tiles = 0, items = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      TileItem it;
+      if (!decode_tile_item(p, item, G, it)) continue;
+      const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
+      if (lane == 0) {
+        if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
+        mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
+        for (int h = 0; h < C::NH; ++h)
+          tma_load_3d(sQ + h * 128 * 128, &tm_q, h * 64, it.kvh * G, it.q_start + it.t0,
+                      &bar[kQFull]);
+      }
+      // K of tile j, then V of tile j - 1 (V is consumed a softmax later).
+      for (int j = 0; j <= it.nt; ++j) {
+        for (int which = 0; which < 2; ++which) {
+          const int jj = which == 0 ? j : j - 1;
+          if (jj < 0 || jj >= it.nt) continue;
+          const uint32_t g = tiles + jj;
+          const int pos = it.kv_lo + jj * kBN + lane * kBox;
+          const bool need = lane < kBN / kBox && pos < it.kv_hi;
+          int page = -1;
+          if (need) {
+            const int lp = pos / bs;
+            page = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
+          }
+          const bool ok = need && page >= 0 && page < p.num_blocks;
+          if (need && !ok) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+          const unsigned mask = __ballot_sync(0xffffffffu, ok);
+          uint64_t *full;
+          uint8_t *dst;
+          const CUtensorMap *map;
+          if (which == 0) {
+            const int st = g % kKStages;
+            full = &bar[kKFull0 + st];
+            dst = sK + st * C::KV_BYTES;
+            map = &tm_k;
+            if (lane == 0 && g >= kKStages)
+              mbar_wait(&bar[kKFree0 + st], ((g / kKStages) - 1) & 1, dead, p.status);
+          } else {
+            full = &bar[kVFull];
+            dst = sV;
+            map = &tm_v;
+            if (lane == 0 && g >= 1) mbar_wait(&bar[kVFree], (g - 1) & 1, dead, p.status);
+          }
+          if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * C::NH * kBox * 128);
+          __syncwarp();
+          if (ok)
+            for (int h = 0; h < C::NH; ++h)
+              tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh, pos % bs,
+                          page, full);
+        }
+      }
+      tiles += it.nt;
+      ++items;
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t tiles = 0, items = 0;
+      const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV), sp = smem_u32(sP);
+      auto issue_s = [&](uint32_t g) {
+        const int st = g % kKStages;
+        mbar_wait(&bar[kKFull0 + st], (g / kKStages) & 1, dead, p.status);
+        if (g > 0) mbar_wait(&bar[kSFree], (g - 1) & 1, dead, p.status);
+        tc_fence_after();
+        const uint32_t kb = sk + st * C::KV_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int h = kk / 4, sub = kk % 4;
+          const uint64_t a = umma_desc_sw128(sq + h * 128 * 128 + sub * 32, 16, 1024);
+          const uint64_t b = umma_desc_sw128(kb + h * C::KV_HALF + sub * 32, 16, 1024);
+          tc_mma_bf16(tmem + kTmemS, a, b, C::IDESC_S, kk > 0);
+        }
+        tc_commit(&bar[kKFree0 + st]);
+        tc_commit(&bar[kSFull]);
+      };
+      for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        TileItem it;
+        if (!decode_tile_item(p, item, G, it)) continue;
+        mbar_wait(&bar[kQFull], items & 1, dead, p.status);
+        issue_s(tiles);
+        for (int j = 0; j < it.nt; ++j) {
+          const uint32_t g = tiles + j;
+          if (j + 1 < it.nt) issue_s(g + 1);
+          mbar_wait(&bar[kPFull], g & 1, dead, p.status);
+          mbar_wait(&bar[kVFull], g & 1, dead, p.status);
+          if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint64_t a = umma_desc_sw128(sp + kk * 32, 16, 1024);
+            const uint64_t b = umma_desc_sw128(sv + kk * 16 * 128, C::KV_HALF, 1024);
+            tc_mma_bf16(tmem + kTmemO, a, b, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          tc_commit(&bar[kVFree]);
+          tc_commit(&bar[kODone]);
+        }
+        tc_commit(&bar[kQFree]);
+        tiles += it.nt;
+        ++items;
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int r = tid;  // row of the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    uint32_t tiles = 0, items = 0;
+    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      TileItem it;
+      if (!decode_tile_item(p, item, G, it)) continue;
+      // Any invalid page in the item's KV range zeroes the item's rows.
+      {
+        const int pfirst = it.kv_lo / bs, plast = (it.kv_hi - 1) / bs;
+        const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
+        int bad = 0;
+        for (int lp = pfirst + r; lp <= plast; lp += 128) {
+          const int pg = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
+          if (pg < 0 || pg >= p.num_blocks) bad = 1;
+        }
+        bad = __any_sync(0xffffffffu, bad);
+        if (r == 0) s_bad[items & 1] = 0;
+        named_sync(1, 128);
+        if (bad && lane == 0) atomicOr(&s_bad[items & 1], 1);
+        named_sync(1, 128);
+      }
+      const bool item_bad = s_bad[items & 1] != 0;
+      const int i = it.t0 + r / G;
+      const int head = it.kvh * G + r % G;
+      const bool row_valid = i < it.q_len;
+      const int row_hi_full = it.prefix + i + 1;
+      const int row_hi = row_valid ? min(row_hi_full, it.kv_lo + it.split_len) : it.kv_lo;
+      float m = -INFINITY, l = 0.f;
+      for (int j = 0; j < it.nt; ++j) {
+        const uint32_t g = tiles + j;
+        const int base = it.kv_lo + j * kBN;
+        mbar_wait(&bar[kSFull], g & 1, dead, p.status);
+        tc_fence_after();
+        float s[kBN];
+#pragma unroll
+        for (int c0 = 0; c0 < kBN; c0 += 32) {
+          uint32_t raw[32];
+          tc_ld32(tmem + lane_off + kTmemS + c0, raw);
+          tc_wait_ld();
+#pragma unroll
+          for (int x = 0; x < 32; ++x) s[c0 + x] = __uint_as_float(raw[x]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kSFree]);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          s[c] = (base + c < row_hi) ? s[c] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, s[c]);
+        }
+        // P and O may be touched only after the previous PV product is done.
+        if (j > 0) mbar_wait(&bar[kODone], (g - 1) & 1, dead, p.status);
+        tc_fence_after();
+        float alpha = 1.f;
+        bool rescale = false;
+        if (mx > m + kTau) {
+          alpha = fast_exp2(m - mx);
+          l *= alpha;
+          m = mx;
+          rescale = j > 0;
+        }
+        if (__any_sync(0xffffffffu, rescale)) {
+          const float a = rescale ? alpha : 1.f;
+#pragma unroll
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t raw[32];
+            tc_ld32(tmem + lane_off + kTmemO + c0, raw);
+            tc_wait_ld();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * a);
+            tc_st32(tmem + lane_off + kTmemO + c0, raw);
+          }
+          tc_wait_st();
+        }
+        const float mu = m == -INFINITY ? 0.f : m;
+        float sum = 0.f;
+        uint8_t *prow = sP + r * 128;
+#pragma unroll
+        for (int ch = 0; ch < kBN / 8; ++ch) {
+          uint32_t w[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float p0 = fast_exp2(s[ch * 8 + 2 * x] - mu);
+            const float p1 = fast_exp2(s[ch * 8 + 2 * x + 1] - mu);
+            sum += p0 + p1;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            w[x] = *reinterpret_cast<const uint32_t *>(&h2);
+          }
+          *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+        l += sum;
+        if (j == it.nt - 1 && it.kv_hi - base < kBN) {
+          // Rows past the tile's KV end may hold anything (NaN tails, stale
+          // data); P is 0 there but 0 * NaN is NaN, so zero those V rows.
+          mbar_wait(&bar[kVFull], g & 1, dead, p.status);
+          const int first = it.kv_hi - base;
+          const int nchunks = (kBN - first) * 8 * C::NH;
+          for (int e = r; e < nchunks; e += 128) {
+            const int h = e / ((kBN - first) * 8);
+            const int rem = e % ((kBN - first) * 8);
+            *reinterpret_cast<uint4 *>(sV + h * C::KV_HALF + (first + rem / 8) * 128 + (rem % 8) * 16) =
+                make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kPFull]);
+      }
+      // ---- epilogue: O / l -> output row or split partial
+      const uint32_t glast = tiles + it.nt - 1;
+      mbar_wait(&bar[kODone], glast & 1, dead, p.status);
+      tc_fence_after();
+      const bool write = row_valid && row_hi > it.kv_lo;
+      const bool direct = ceil_div_ll(row_hi_full, it.split_len) == 1;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      const uint32_t keep = item_bad ? 0u : 0xffffffffu;  // bad items write exact zeros
+      const size_t tok = (size_t)it.q_start + i;
+      const long long prow = it.partial_base + ((long long)i * H + head) * it.nsplit + it.split;
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t raw[32];
+        tc_ld32(tmem + lane_off + kTmemO + c0, raw);
+        tc_wait_ld();
+#pragma unroll
+        for (int x = 0; x < 32; ++x) raw[x] &= keep;
+        if (write) {
+          if (direct) {
+            uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
+                                                   (tok * H + head) * D + c0);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint32_t w[4];
+#pragma unroll
+              for (int x = 0; x < 4; ++x) {
+                const __nv_bfloat162 h2 =
+                    __floats2bfloat162_rn(__uint_as_float(raw[v * 8 + 2 * x]) * inv,
+                                          __uint_as_float(raw[v * 8 + 2 * x + 1]) * inv);
+                w[x] = *reinterpret_cast<const uint32_t *>(&h2);
+              }
+              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + c0);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[v] = make_float4(__uint_as_float(raw[4 * v]) * inv,
+                                   __uint_as_float(raw[4 * v + 1]) * inv,
+                                   __uint_as_float(raw[4 * v + 2]) * inv,
+                                   __uint_as_float(raw[4 * v + 3]) * inv);
+          }
+        }
+      }
+      if (write && !direct)
+        p.part_lse[prow] = item_bad ? __int_as_float(0x7fc00000) : (l > 0.f ? m + log2f(l) : -INFINITY);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kOFree]);
+      tiles += it.nt;
+      ++items;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 5) tc_dealloc(tmem, kTmemCols);
+}
+
+template <int D>
+cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                     const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
+  using C = TileCfg<D>;
+  cudaError_t e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       C::SMEM);
+  if (e != cudaSuccess) return e;
+  tile_kernel<D><<<num_sms * 2, kTileThreads, C::SMEM, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool tile_kernel_supported(int dtype, int head_dim, int group) {
+  return dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
+                               const CUtensorMap &tm_k, const CUtensorMap &tm_v, int num_sms,
+                               cudaStream_t stream) {
+  if (p.head_dim == 128) return launch_d<128>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  if (p.head_dim == 64) return launch_d<64>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace pa

@@ -241,3 +241,34 @@ def test_capture_without_workspace_is_refused():
         finally:
             g.capture_end()
     assert st == pa.PA_ERR_WORKSPACE
+
+
+# --------------------------------------------------------------------------
+# tensor-core tile path (bf16 extend / prefill)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("group", [1, 4, 16])
+def test_tile_prefill_and_extend_full(group):
+    Hk = 2
+    b = inputs.paged_batch([600, 1, 300, 77], [600, 1500, 1300, 77], Hk * group, Hk, 128, 16,
+                           dtype="bf16", seed=100 + group)
+    got = parity.gpu_forward(b)
+    parity.compare(got, parity.oracle_forward(b), "bf16", what=f"tile G{group}")
+
+
+def test_tile_chunked_extend_matches_unchunked():
+    b = inputs.paged_batch([200, 1], [3000, 2500], 16, 2, 128, 64, dtype="bf16", seed=7)
+    want = parity.oracle_forward(b)
+    for kvs in (0, 1024, 2048):
+        got = parity.gpu_forward(b, kv_split_tokens=kvs)
+        parity.compare(got, want, "bf16", what=f"chunk {kvs}")
+
+
+def test_bad_block_in_extend_zeroes_its_rows():
+    b = inputs.paged_batch([1, 40, 30], [100, 540, 30], 16, 2, 128, 16, dtype="bf16", seed=21)
+    want = parity.oracle_forward(b)
+    b.block_table[1, 3] = -7  # positions 48..63 of the extend request (prefix 500)
+    got = parity.gpu_forward(b, expect_status=pa.PA_DEV_BAD_BLOCK)
+    assert np.all(got[1:41] == 0.0)
+    parity.compare(got[[0] + list(range(41, 71))], want[[0] + list(range(41, 71))], "bf16",
+                   what="healthy rows")
