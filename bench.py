@@ -462,6 +462,38 @@ def run_reference(args):
                 "d2h_bytes_per_step": 0}}))
 
 
+def run_only(args):
+    """A plain loop over one workload (for profiler captures): W warm-up
+    calls then K timed calls; prints one JSON line with the mean time."""
+    torch.cuda.set_device(0)
+    from paged_kv_attention_16_gb300 import build as pbuild
+    pbuild.build()
+    from paged_kv_attention_16_gb300 import pa
+    name = args.only
+    if name == "mla_decode":
+        host = inputs.mla_decode_batch(poison=False)
+        m = pa.to_device(host)
+        out = torch.empty((m.num_seqs, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16,
+                          device="cuda")
+        fn = lambda: pa.mla_decode(m, out=out)  # noqa: E731
+    else:
+        host = inputs.WORKLOADS[name](poison=False)
+        b = pa.to_device(host)
+        out = torch.empty_like(b.q)
+        fn = lambda: pa.forward(b, out=out)  # noqa: E731
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(args.steps):
+        fn()
+    ev1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"only": name, "steps": args.steps,
+                      "ms_per_step": ev0.elapsed_time(ev1) / max(args.steps, 1)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,8 +502,13 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-secondary", action="store_true")
     ap.add_argument("--skip-cpu", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=sorted(list(inputs.WORKLOADS) + ["mla_decode"]),
+                    help="profile helper: loop over a single workload, no JSON contract")
     args = ap.parse_args()
-    if args.impl == "reference":
+    if args.only:
+        run_only(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_ours(args)

@@ -513,6 +513,40 @@ bool tile_path_ok(int dtype, int head_dim, int group) {
 }
 
 }  // namespace
+
+pa_status device_resources(cudaStream_t stream, size_t ws_bytes, void **ws,
+                           unsigned int **status, int *num_sms) {
+  DeviceState *d = nullptr;
+  pa_status s = device_state(stream, &d);
+  if (s != PA_OK) return s;
+  s = ensure_workspace(d, ws_bytes, stream);
+  if (s != PA_OK) return s;
+  *ws = d->ws;
+  *status = d->status;
+  *num_sms = d->num_sms;
+  return PA_OK;
+}
+
+bool encode_tiled(CUtensorMap *map, const void *base, int dtype, int rank,
+                  const unsigned long long *dims, const unsigned long long *strides,
+                  const unsigned int *box, bool swizzle128) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || rank < 1 || rank > 5) return false;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], e[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    e[i] = 1;
+  }
+  for (int i = 0; i + 1 < rank; ++i) st[i] = strides[i];
+  const CUtensorMapDataType t =
+      dtype == PA_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return fn(map, t, rank, const_cast<void *>(base), d, st, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace pa
 
 using namespace pa;

@@ -25,23 +25,15 @@ cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_k, const CUtensorMap &tm_v, int grid,
                                cudaStream_t stream);
 
-// Absorbed-MLA decode.
-struct MlaParams {
-  const void *q;
-  void *out;
-  const int32_t *block_table;
-  const int32_t *seq_lens;
-  int num_seqs, num_heads, kv_lora_rank, rope_dim, block_size;
-  int max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
-  float scale_log2;
-  int split_len;          // KV positions per split
-  int max_splits;         // splits per sequence the workspace holds
-  unsigned int *counter;  // work counter (reset by a memset node)
-  float *part_o;          // [num_seqs * num_heads * max_splits][kv_lora_rank]
-  float *part_lse;        // [num_seqs * num_heads * max_splits]
-  unsigned int *status;
-};
-cudaError_t launch_mla_decode(const MlaParams &p, const CUtensorMap &tm_q,
-                              const CUtensorMap &tm_kv, int num_sms, cudaStream_t stream);
+// Library-owned per-device resources for an entry point: workspace of at
+// least ws_bytes (grown outside capture), the device status word, SM count.
+pa_status device_resources(cudaStream_t stream, size_t ws_bytes, void **ws,
+                           unsigned int **status, int *num_sms);
+
+// cuTensorMapEncodeTiled over a bf16/fp32 tensor of `rank` dims (innermost
+// first), strides in bytes for dims 1..rank-1, optional 128-byte swizzle.
+bool encode_tiled(CUtensorMap *map, const void *base, int dtype, int rank,
+                  const unsigned long long *dims, const unsigned long long *strides,
+                  const unsigned int *box, bool swizzle128);
 
 }  // namespace pa
