@@ -131,9 +131,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     if (k < S) {
       s = p.ord[k];
       const ReqScalars r = read_req(p, s, qsl_bad);
-      const bool row_path = r.cls == kDecode || !p.tile_ok;
-      int len = r.cls == kDecode ? L : (row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens
-                                                                               : (r.ctx > 0 ? r.ctx : 1)));
+      // Decode rows stream on CUDA cores while G < 8; from G = 8 the FFMA
+      // issue rate, not HBM, would bound them, so they join the tensor-core
+      // tile path (one token x G heads per 128-row tile).
+      const bool row_path = !p.tile_ok || (r.cls == kDecode && G < 8);
+      int len;
+      if (r.cls == kDecode) {
+        len = row_path ? L : max(L, kTileDecodeMinSplit);
+        if (p.kv_split_tokens > 0 && p.kv_split_tokens < len) len = p.kv_split_tokens;
+      } else {
+        len = row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens : (r.ctx > 0 ? r.ctx : 1));
+      }
       int nsplit = (int)ceil_div_ll(r.ctx > 0 ? r.ctx : 1, len);
       if (nsplit < 1) nsplit = 1;
       info.q_start = r.q_start;
@@ -190,6 +198,29 @@ __device__ inline void store_out<__nv_bfloat16>(__nv_bfloat16 *dst, float v) {
   *dst = __float2bfloat16_rn(v);
 }
 
+// Rows with at most kWarpMergeSplits non-empty splits are merged by one warp
+// (lanes over head_dim); longer rows by a whole block (warps over splits).
+constexpr int kWarpMergeSplits = 8;
+
+struct MergeRow {
+  long long tok, base;
+  int h, nn;
+};
+
+__device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, long long row) {
+  const int S = p.num_seqs, H = p.num_heads;
+  const int k = list_find(mend, S, row);
+  const long long local = row - (k ? mend[k - 1] : 0);
+  const ReqInfo r = p.req[p.ord[k]];
+  const int i = (int)(local / H);
+  MergeRow m;
+  m.h = (int)(local % H);
+  m.tok = r.q_start + i;
+  m.nn = (int)ceil_div_ll(r.ctx - r.q_len + i + 1, r.split_len);  // non-empty splits
+  m.base = r.partial_base + ((long long)i * H + m.h) * r.nsplit;
+  return m;
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p) {
   __shared__ float s_red[kMergeThreads / 32][128];
@@ -200,6 +231,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = kMergeThreads / 32;
   T *out = reinterpret_cast<T *>(p.out);
+  const long long gw = ((long long)blockIdx.x * blockDim.x + tid) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
 
   if (p.plan->qsl_bad) {
     const size_t n = (size_t)p.num_tokens * H * D;
@@ -212,8 +245,6 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   {
     const long long *zend = p.list_end + (size_t)kListZero * S;
     const long long nz = p.plan->n[kListZero];
-    const long long gw = ((long long)blockIdx.x * blockDim.x + tid) >> 5;
-    const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
     for (long long row = gw; row < nz; row += nw) {
       const int k = list_find(zend, S, row);
       const long long local = row - (k ? zend[k - 1] : 0);
@@ -227,21 +258,52 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   const long long *mend = p.list_end + (size_t)kListMerge * S;
   const long long nm = p.plan->n[kListMerge];
   const int dpl = D / 32;  // dims per lane: 2 or 4
+
+  // ---- short rows: one warp each ---------------------------------------------
+  for (long long row = gw; row < nm; row += nw) {
+    const MergeRow mr = merge_row(p, mend, row);
+    if (mr.nn <= 1 || mr.nn > kWarpMergeSplits) continue;
+    const float lse = lane < mr.nn ? p.part_lse[mr.base + lane] : -INFINITY;
+    int bad = isnan(lse) ? 1 : 0;
+    float M = bad ? -INFINITY : lse;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    const float w_own = (lane < mr.nn && !bad) ? fast_exp2(lse - M) : 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
+#pragma unroll
+    for (int q = 0; q < kWarpMergeSplits; ++q) {
+      if (q >= mr.nn) break;
+      const float w = __shfl_sync(0xffffffffu, w_own, q);
+      L += w;
+      const float *src = p.part_o + (size_t)(mr.base + q) * D + lane * dpl;
+      if (dpl == 4) {
+        const float4 v = *reinterpret_cast<const float4 *>(src);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+        acc[2] = fmaf(w, v.z, acc[2]);
+        acc[3] = fmaf(w, v.w, acc[3]);
+      } else {
+        const float2 v = *reinterpret_cast<const float2 *>(src);
+        acc[0] = fmaf(w, v.x, acc[0]);
+        acc[1] = fmaf(w, v.y, acc[1]);
+      }
+    }
+    const float inv = (bad || !(L > 0.f)) ? 0.f : 1.f / L;
+    T *dst = out + ((size_t)mr.tok * H + mr.h) * D + lane * dpl;
+    for (int x = 0; x < dpl; ++x) store_out<T>(dst + x, acc[x] * inv);
+  }
+
+  // ---- long rows: one block each, warps over splits ---------------------------
   for (long long row = blockIdx.x; row < nm; row += gridDim.x) {
-    const int k = list_find(mend, S, row);
-    const long long local = row - (k ? mend[k - 1] : 0);
-    const ReqInfo r = p.req[p.ord[k]];
-    const int i = (int)(local / H), h = (int)(local % H);
-    const long long tok = r.q_start + i;
-    const int kv_row_hi = r.ctx - r.q_len + i + 1;
-    const int nn = (int)ceil_div_ll(kv_row_hi, r.split_len);  // non-empty splits of this row
-    if (nn <= 1) continue;  // the attention kernel wrote this row directly (uniform per CTA)
-    const long long base = r.partial_base + ((long long)i * H + h) * r.nsplit;
-    // max lse and bad-split check
+    const MergeRow mr = merge_row(p, mend, row);
+    if (mr.nn <= kWarpMergeSplits) continue;  // uniform per block
     float M = -INFINITY;
     int bad = 0;
-    for (int q = tid; q < nn; q += kMergeThreads) {
-      const float v = p.part_lse[base + q];
+    for (int q = tid; q < mr.nn; q += kMergeThreads) {
+      const float v = p.part_lse[mr.base + q];
       if (isnan(v)) bad = 1; else M = fmaxf(M, v);
     }
 #pragma unroll
@@ -263,10 +325,11 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wl = 0.f;
     if (!bad && M != -INFINITY) {
-      for (int q = warp; q < nn; q += NW) {
-        const float w = fast_exp2(p.part_lse[base + q] - M);
+#pragma unroll 8
+      for (int q = warp; q < mr.nn; q += NW) {
+        const float w = fast_exp2(p.part_lse[mr.base + q] - M);
         wl += w;
-        const float *src = p.part_o + (size_t)(base + q) * D + lane * dpl;
+        const float *src = p.part_o + (size_t)(mr.base + q) * D + lane * dpl;
         if (dpl == 4) {
           const float4 v = *reinterpret_cast<const float4 *>(src);
           acc[0] = fmaf(w, v.x, acc[0]);
@@ -290,7 +353,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
         L += s_wl[w];
       }
       const float v = (bad || !(L > 0.f)) ? 0.f : a / L;
-      store_out<T>(out + ((size_t)tok * H + h) * D + tid, v);
+      store_out<T>(out + ((size_t)mr.tok * H + mr.h) * D + tid, v);
     }
     __syncthreads();
   }

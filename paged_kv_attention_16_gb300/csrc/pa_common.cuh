@@ -78,6 +78,9 @@ constexpr int kRowMaxSplit = 8192;
 constexpr int kRowMinSplit = 256;
 // Rows per tensor-core tile of the extend/prefill kernel.
 constexpr int kTileRows = 128;
+// Smallest KV split of a decode row on the tile path (keeps items long
+// enough to amortise the tile pipeline's start-up).
+constexpr int kTileDecodeMinSplit = 1024;
 
 __host__ __device__ inline long long ceil_div_ll(long long a, long long b) {
   return (a + b - 1) / b;

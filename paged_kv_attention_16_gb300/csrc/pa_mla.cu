@@ -558,7 +558,9 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
   if (dev < 0 || dev >= 64) return PA_ERR_CUDA;
   if (!attr_done[dev]) {
     if (cudaFuncSetAttribute(mla_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, MLA_SMEM) !=
-        cudaSuccess)
+            cudaSuccess ||
+        cudaFuncSetAttribute(mla_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared) != cudaSuccess)
       return PA_ERR_CUDA;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * (num_sms / 2));

@@ -66,32 +66,47 @@ struct RowCfg {
   static constexpr int LPT = D / DPT;                          // lanes per (token, head group)
   static constexpr int LANES_TOK = LPT * HG;                   // lanes per token
   static constexpr int TPW = 32 / LANES_TOK;                   // tokens per warp
-  static constexpr int NWARP = 4;
-  static constexpr int NTHREADS = 32 * NWARP;
-  static constexpr int TPS = TPW * NWARP;                      // tokens per step
+  static constexpr int NWARP = 4;                              // compute warps
+  static constexpr int NTHREADS = 32 * (NWARP + 1);            // + one producer warp
+  static constexpr int TPS = TPW * NWARP;                      // tokens per sub-step
   static constexpr int BOX = 16;                               // slots per TMA box
-  static constexpr int ST = TPS > BOX ? TPS : BOX;             // tokens per stage
+  static constexpr int ST = TPS > 32 ? TPS : 32;               // tokens per stage
+  static constexpr int SUB = ST / TPS;                         // sub-steps per stage
+  static constexpr int NB0 = HPT >= 8 ? 1 : 8 / HPT;
+  static constexpr int NB = SUB < NB0 ? SUB : NB0;             // tokens batched per thread
   static constexpr int NBOX = ST / BOX;
   static constexpr int ROWB = D * static_cast<int>(sizeof(T));
   static constexpr int HALF_STAGE = ST * ROWB;
   static constexpr int STAGE_BYTES = 2 * HALF_STAGE;
-  static constexpr int NSTAGE = (48 * 1024 / STAGE_BYTES) < 3 ? 3 : (48 * 1024 / STAGE_BYTES);
-  static constexpr int SCRATCH_O = TPS * G * D * 4;
-  static constexpr int RING_BYTES = NSTAGE * STAGE_BYTES;
-  static constexpr int ALIAS_BYTES = RING_BYTES > SCRATCH_O ? RING_BYTES : SCRATCH_O;
+  static constexpr int NSTAGE = (64 * 1024 / STAGE_BYTES) < 3 ? 3 : (64 * 1024 / STAGE_BYTES);
   static constexpr int MAX_PAGES = kRowMaxSplit / BOX + 2;
-  static constexpr int OFF_ML = ALIAS_BYTES;
-  static constexpr int OFF_PAGES = OFF_ML + 2 * TPS * G * 4;
-  static constexpr int OFF_BAR = (OFF_PAGES + MAX_PAGES * 4 + 15) / 16 * 16;
-  static constexpr int OFF_MISC = OFF_BAR + 2 * NSTAGE * 8;
-  static constexpr int SMEM = OFF_MISC + 64;
-  static constexpr int OPT = (G * D + NTHREADS - 1) / NTHREADS;  // outputs per thread
+  // shared memory layout
+  static constexpr int OFF_RING = 0;
+  static constexpr int OFF_SCR = OFF_RING + NSTAGE * STAGE_BYTES;  // per-warp partials
+  static constexpr int SCR_BYTES = NWARP * G * D * 4;
+  static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;               // per-warp m, l
+  static constexpr int OFF_PAGES = OFF_ML + 2 * NWARP * G * 4;
+  static constexpr int OFF_DESC = OFF_PAGES + MAX_PAGES * 4;       // two item descriptors
+  static constexpr int OFF_BAR = (OFF_DESC + 2 * 64 + 15) / 16 * 16;
+  static constexpr int NBAR = 2 * NSTAGE + 4;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8;
+  static constexpr int OPT = (G * D + 127) / 128;  // outputs per compute thread
   static constexpr int LOG2_HPT = HPT == 1 ? 0 : HPT == 2 ? 1 : HPT == 4 ? 2 : 3;
   static_assert(LPT >= HPT, "transpose-reduce needs at least HPT lanes per token");
   static_assert(32 % LANES_TOK == 0, "token groups must tile a warp");
   static_assert(DPT % E == 0 && D % DPT == 0, "dims must split into 16-byte vectors");
   static_assert(HPT * DPT <= 64, "register budget");
-  static_assert(D % OPT == 0 || G * D <= NTHREADS, "outputs per thread must not straddle heads");
+  static_assert(SUB % NB == 0, "batches tile a stage");
+  static_assert(D % OPT == 0 || G * D <= 128, "outputs per thread must not straddle heads");
+};
+
+// Work item handed from the producer warp to the compute warps.
+struct RowDesc {
+  int done;       // 1: no more work
+  int bad;        // a page of the split is outside the pool
+  int tok, kvh, i, split, kv_lo, kv_hi, direct;
+  int nsplit;
+  long long prow0;  // partial row of head 0 of the group (split partials)
 };
 
 // Sum the HPT partial dot products of the LPT lanes of one (token, head
@@ -124,23 +139,24 @@ __device__ inline void reduce_scores(const float (&part)[HPT], float (&score)[HP
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(128) row_kernel(const __grid_constant__ CUtensorMap tm_k,
-                                                  const __grid_constant__ CUtensorMap tm_v,
-                                                  const FwdParams p) {
+__global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                     const __grid_constant__ CUtensorMap tm_v,
+                                                     const FwdParams p) {
   using C = RowCfg<T, D, G>;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t *ring = smem;
+  uint8_t *ring = smem + C::OFF_RING;
+  float *s_o = reinterpret_cast<float *>(smem + C::OFF_SCR);
   float *s_m = reinterpret_cast<float *>(smem + C::OFF_ML);
-  float *s_l = s_m + C::TPS * G;
+  float *s_l = s_m + C::NWARP * G;
   int *s_pages = reinterpret_cast<int *>(smem + C::OFF_PAGES);
+  RowDesc *s_desc = reinterpret_cast<RowDesc *>(smem + C::OFF_DESC);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint64_t *empty = full + C::NSTAGE;
-  long long *s_item = reinterpret_cast<long long *>(smem + C::OFF_MISC);
+  uint64_t *item_full = empty + C::NSTAGE;  // [2]
+  uint64_t *item_free = item_full + 2;      // [2]
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int slot = warp * C::TPW + lane / C::LANES_TOK;
-  const int hg = (lane % C::LANES_TOK) / C::LPT;
-  const int c = lane % C::LPT;
+  const int S = p.num_seqs, H = p.num_heads, bs = p.block_size;
 
   if (tid == 0) {
     prefetch_tensor_map(&tm_k);
@@ -149,73 +165,130 @@ __global__ void __launch_bounds__(128) row_kernel(const __grid_constant__ CUtens
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], C::NWARP);
     }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_free[i], C::NWARP);
+    }
     fence_mbar_init();
   }
   __syncthreads();
-
   bool dead = false;
-  uint32_t g0 = 0;  // global index of the current item's first stage
-  const long long n_items = p.plan->n[kListRow];
-  const int S = p.num_seqs, H = p.num_heads, bs = p.block_size;
-  const long long *row_end = p.list_end + (size_t)kListRow * S;
 
-  for (uint32_t iter = 0;; ++iter) {
-    // Double-buffered broadcast: a slot is rewritten only two iterations
-    // later, after every thread has passed the barrier in between.
-    if (tid == 0) s_item[iter & 1] = (long long)atomicAdd(&p.plan->counter[kListRow], 1ull);
-    __syncthreads();
-    const long long item = s_item[iter & 1];
-    if (item >= n_items) break;
-
-    // ---- decode the work item -------------------------------------------
-    const int k = list_find(row_end, S, item);
-    const long long start = k ? row_end[k - 1] : 0;
-    const int s = p.ord[k];
-    const ReqInfo r = p.req[s];
-    const long long local = item - start;
-    const long long per_kvh = (long long)r.nsplit * r.q_len;
-    const int kvh = (int)(local / per_kvh);
-    const int rem = (int)(local % per_kvh);
-    const int split = rem / r.q_len;
-    const int i = rem % r.q_len;
-    const int tok = r.q_start + i;
-    const int kv_row_hi = r.ctx - r.q_len + i + 1;  // causal: positions 0 .. prefix + i
-    const int kv_lo = split * r.split_len;
-    const int kv_hi = min(kv_row_hi, kv_lo + r.split_len);
-    if (kv_lo >= kv_hi) continue;  // this split lies past the row's causal bound
-    const bool direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
-    const long long prow0 = r.partial_base + ((long long)i * H + kvh * G) * r.nsplit + split;
-
-    // ---- page list of the split ------------------------------------------
-    const int pfirst = kv_lo / bs;
-    const int npages = (kv_hi - 1) / bs - pfirst + 1;
-    const int32_t *bt = p.block_table + (size_t)s * p.max_blocks_per_seq;
-    int bad = 0;
-    for (int j = tid; j < npages; j += C::NTHREADS) {
-      const int lp = pfirst + j;
-      const int pid = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
-      if (pid < 0 || pid >= p.num_blocks) bad = 1;
-      s_pages[j] = pid;
+  if (warp == C::NWARP) {
+    // ===================================================== producer warp
+    const long long n_items = p.plan->n[kListRow];
+    const long long *row_end = p.list_end + (size_t)kListRow * S;
+    uint32_t g = 0, seq = 0;  // stages issued, descriptors written
+    for (;;) {
+      long long item = 0;
+      if (lane == 0) item = (long long)atomicAdd(&p.plan->counter[kListRow], 1ull);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      RowDesc d{};
+      int kvh = 0, npages = 0, pfirst = 0, s = 0;
+      if (item >= n_items) {
+        d.done = 1;
+      } else {
+        const int k = list_find(row_end, S, item);
+        const long long start = k ? row_end[k - 1] : 0;
+        s = p.ord[k];
+        const ReqInfo r = p.req[s];
+        const long long local = item - start;
+        const long long per_kvh = (long long)r.nsplit * r.q_len;
+        kvh = (int)(local / per_kvh);
+        const int rem = (int)(local % per_kvh);
+        d.split = rem / r.q_len;
+        d.i = rem % r.q_len;
+        d.tok = r.q_start + d.i;
+        d.kvh = kvh;
+        const int kv_row_hi = r.ctx - r.q_len + d.i + 1;  // causal: 0 .. prefix + i
+        d.kv_lo = d.split * r.split_len;
+        d.kv_hi = min(kv_row_hi, d.kv_lo + r.split_len);
+        if (d.kv_lo >= d.kv_hi) continue;  // split past this row's causal bound
+        d.direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
+        d.nsplit = r.nsplit;
+        d.prow0 = r.partial_base + ((long long)d.i * H + kvh * G) * r.nsplit + d.split;
+        pfirst = d.kv_lo / bs;
+        npages = (d.kv_hi - 1) / bs - pfirst + 1;
+      }
+      // the page list is private to this warp; reuse it once our earlier TMA
+      // issues (which read it) are done -- they are: issue is synchronous
+      const int32_t *bt = p.block_table + (size_t)s * p.max_blocks_per_seq;
+      int bad = 0;
+      for (int j = lane; j < npages; j += 32) {
+        const int lp = pfirst + j;
+        const int pid = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
+        if (pid < 0 || pid >= p.num_blocks) bad = 1;
+        s_pages[j] = pid;
+      }
+      d.bad = __any_sync(0xffffffffu, bad);
+      if (d.bad && lane == 0) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+      __syncwarp();
+      // hand the descriptor over
+      const int slot = seq & 1;
+      if (lane == 0) {
+        if (seq >= 2) mbar_wait(&item_free[slot], ((seq >> 1) - 1) & 1, dead, p.status);
+        s_desc[slot] = d;
+        mbar_arrive(&item_full[slot]);
+      }
+      ++seq;
+      if (d.done) break;
+      if (d.bad) continue;
+      // stream the split's K/V stages
+      const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
+      for (int j = 0; j < nst; ++j, ++g) {
+        const int b = g % C::NSTAGE;
+        const int pos0 = d.kv_lo + j * C::ST;
+        const int pos = pos0 + lane * C::BOX;
+        const bool issue = lane < C::NBOX && pos < d.kv_hi;
+        const int nbox = __popc(__ballot_sync(0xffffffffu, issue));
+        if (lane == 0) {
+          if (g >= C::NSTAGE) mbar_wait(&empty[b], ((g / C::NSTAGE) - 1) & 1, dead, p.status);
+          mbar_arrive_expect_tx(&full[b], nbox * 2 * C::BOX * C::ROWB);
+        }
+        __syncwarp();
+        if (issue) {
+          const int page = s_pages[pos / bs - pfirst];
+          uint8_t *kb = ring + b * C::STAGE_BYTES + lane * C::BOX * C::ROWB;
+          tma_load_4d(kb, &tm_k, 0, kvh, pos % bs, page, &full[b]);
+          tma_load_4d(kb + C::HALF_STAGE, &tm_v, 0, kvh, pos % bs, page, &full[b]);
+        }
+      }
     }
-    bad = __syncthreads_or(bad);
-    if (bad) {
-      if (tid == 0) atomicOr(p.status, PA_DEV_BAD_BLOCK);
-      for (int e = tid; e < G * D; e += C::NTHREADS) {
-        const int h = e / D, d = e % D;
-        if (direct) {
-          store_elem(reinterpret_cast<T *>(p.out) + ((size_t)tok * H + kvh * G + h) * D + d, 0.f);
+    return;
+  }
+
+  // ======================================================= compute warps
+  const int slot_tok = warp * C::TPW + lane / C::LANES_TOK;  // token slot in a sub-step
+  const int hg = (lane % C::LANES_TOK) / C::LPT;
+  const int c = lane % C::LPT;
+  const int tgrp = lane / C::LANES_TOK;  // token group inside the warp
+  uint32_t g = 0;
+  for (uint32_t seq = 0;; ++seq) {
+    const int islot = seq & 1;
+    mbar_wait(&item_full[islot], (seq >> 1) & 1, dead, p.status);
+    const RowDesc d = s_desc[islot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_free[islot]);
+    if (d.done) break;
+    const int kvh = d.kvh;
+    if (d.bad) {
+      for (int e = tid; e < G * D; e += 128) {
+        const int h = e / D, dd = e % D;
+        if (d.direct) {
+          store_elem(reinterpret_cast<T *>(p.out) + ((size_t)d.tok * H + kvh * G + h) * D + dd, 0.f);
         } else {
-          const long long prow = prow0 + (long long)h * r.nsplit;
-          p.part_o[prow * D + d] = 0.f;
-          if (d == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
+          const long long prow = d.prow0 + (long long)h * d.nsplit;
+          p.part_o[prow * D + dd] = 0.f;
+          if (dd == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
         }
       }
       continue;
     }
 
-    // ---- q of this thread's heads and dims, pre-scaled to base 2 -----------
+    // q of this thread's heads and dims, pre-scaled to base 2
     float qv[C::HPT][C::DPT];
-    const T *qrow = reinterpret_cast<const T *>(p.q) + ((size_t)tok * H + kvh * G + hg * C::HPT) * D;
+    const T *qrow =
+        reinterpret_cast<const T *>(p.q) + ((size_t)d.tok * H + kvh * G + hg * C::HPT) * D;
 #pragma unroll
     for (int h = 0; h < C::HPT; ++h)
 #pragma unroll
@@ -230,134 +303,141 @@ __global__ void __launch_bounds__(128) row_kernel(const __grid_constant__ CUtens
       m[h] = -INFINITY;
       l[h] = 0.f;
 #pragma unroll
-      for (int d = 0; d < C::DPT; ++d) o[h][d] = 0.f;
+      for (int x = 0; x < C::DPT; ++x) o[h][x] = 0.f;
     }
 
-    // ---- TMA pipeline over the split's stages ------------------------------
-    const int nst = (kv_hi - kv_lo + C::ST - 1) / C::ST;
-    auto issue = [&](int j) {
-      const uint32_t g = g0 + j;
-      const int b = g % C::NSTAGE;
-      if (g >= C::NSTAGE) mbar_wait(&empty[b], ((g / C::NSTAGE) - 1) & 1, dead, p.status);
-      const int pos0 = kv_lo + j * C::ST;
-      int nbox = 0;
-#pragma unroll
-      for (int x = 0; x < C::NBOX; ++x) nbox += (pos0 + x * C::BOX < kv_hi) ? 1 : 0;
-      mbar_arrive_expect_tx(&full[b], nbox * 2 * C::BOX * C::ROWB);
-      uint8_t *kb = ring + b * C::STAGE_BYTES;
-      uint8_t *vb = kb + C::HALF_STAGE;
-      for (int x = 0; x < nbox; ++x) {
-        const int pos = pos0 + x * C::BOX;
-        const int page = s_pages[pos / bs - pfirst];
-        const int slot0 = pos % bs;
-        tma_load_4d(kb + x * C::BOX * C::ROWB, &tm_k, 0, kvh, slot0, page, &full[b]);
-        tma_load_4d(vb + x * C::BOX * C::ROWB, &tm_v, 0, kvh, slot0, page, &full[b]);
-      }
-    };
-    if (tid == 0) {
-      fence_proxy_async();
-      const int pre = nst < C::NSTAGE - 1 ? nst : C::NSTAGE - 1;
-      for (int j = 0; j < pre; ++j) issue(j);
-    }
-
-    for (int j = 0; j < nst; ++j) {
-      if (tid == 0 && j + C::NSTAGE - 1 < nst) issue(j + C::NSTAGE - 1);
-      const uint32_t g = g0 + j;
+    const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
+    for (int j = 0; j < nst; ++j, ++g) {
       const int b = g % C::NSTAGE;
       mbar_wait(&full[b], (g / C::NSTAGE) & 1, dead, p.status);
       const T *kb = reinterpret_cast<const T *>(ring + b * C::STAGE_BYTES);
       const T *vb = kb + C::ST * D;
 #pragma unroll
-      for (int sub = 0; sub < C::ST / C::TPS; ++sub) {
-        const int tl = sub * C::TPS + slot;
-        const bool valid = kv_lo + j * C::ST + tl < kv_hi;
-        float kf[C::DPT];
+      for (int sb = 0; sb < C::SUB; sb += C::NB) {
+        float sc[C::NB][C::HPT];
+        bool valid[C::NB];
+        // scores of NB tokens (independent chains)
 #pragma unroll
-        for (int v = 0; v < C::VPT; ++v)
-          load_vec(kb + tl * D + (c + v * C::LPT) * C::E, &kf[v * C::E]);
-        float part[C::HPT];
+        for (int nb = 0; nb < C::NB; ++nb) {
+          const int tl = (sb + nb) * C::TPS + slot_tok;
+          valid[nb] = d.kv_lo + j * C::ST + tl < d.kv_hi;
+          float kf[C::DPT];
+#pragma unroll
+          for (int v = 0; v < C::VPT; ++v)
+            load_vec(kb + tl * D + (c + v * C::LPT) * C::E, &kf[v * C::E]);
+          float part[C::HPT];
+#pragma unroll
+          for (int h = 0; h < C::HPT; ++h) {
+            float acc = 0.f;
+#pragma unroll
+            for (int x = 0; x < C::DPT; ++x) acc = fmaf(qv[h][x], kf[x], acc);
+            part[h] = acc;
+          }
+          reduce_scores<C::HPT, C::LPT, C::LOG2_HPT>(part, sc[nb], lane, c);
+        }
+        // one max update for the batch (lazy: only when it grows by > 8)
 #pragma unroll
         for (int h = 0; h < C::HPT; ++h) {
-          float acc = 0.f;
+          float mx = -INFINITY;
 #pragma unroll
-          for (int d = 0; d < C::DPT; ++d) acc = fmaf(qv[h][d], kf[d], acc);
-          part[h] = acc;
+          for (int nb = 0; nb < C::NB; ++nb)
+            if (valid[nb]) mx = fmaxf(mx, sc[nb][h]);
+          if (mx > m[h] + kLazyRescale) {
+            const float a = fast_exp2(m[h] - mx);
+            l[h] *= a;
+#pragma unroll
+            for (int x = 0; x < C::DPT; ++x) o[h][x] *= a;
+            m[h] = mx;
+          }
         }
-        float sc[C::HPT];
-        reduce_scores<C::HPT, C::LPT, C::LOG2_HPT>(part, sc, lane, c);
-        if (valid) {
+#pragma unroll
+        for (int nb = 0; nb < C::NB; ++nb) {
+          if (!valid[nb]) continue;
+          const int tl = (sb + nb) * C::TPS + slot_tok;
           float vf[C::DPT];
 #pragma unroll
           for (int v = 0; v < C::VPT; ++v)
             load_vec(vb + tl * D + (c + v * C::LPT) * C::E, &vf[v * C::E]);
 #pragma unroll
           for (int h = 0; h < C::HPT; ++h) {
-            if (sc[h] > m[h] + kLazyRescale) {
-              const float a = fast_exp2(m[h] - sc[h]);
-              l[h] *= a;
-#pragma unroll
-              for (int d = 0; d < C::DPT; ++d) o[h][d] *= a;
-              m[h] = sc[h];
-            }
-            const float pr = fast_exp2(sc[h] - m[h]);
+            const float pr = fast_exp2(sc[nb][h] - m[h]);
             l[h] += pr;
 #pragma unroll
-            for (int d = 0; d < C::DPT; ++d) o[h][d] = fmaf(pr, vf[d], o[h][d]);
+            for (int x = 0; x < C::DPT; ++x) o[h][x] = fmaf(pr, vf[x], o[h][x]);
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[b]);
     }
-    g0 += nst;
 
-    // ---- merge the token slots and write ------------------------------------
-    __syncthreads();  // the ring is free; it becomes merge scratch
-    float *s_o = reinterpret_cast<float *>(ring);
+    // ---- merge the token groups of this warp (log-sum-exp via shuffles)
 #pragma unroll
-    for (int h = 0; h < C::HPT; ++h) {
-      const int head = hg * C::HPT + h;
+    for (int off = C::LANES_TOK; off < 32; off <<= 1) {
 #pragma unroll
-      for (int v = 0; v < C::VPT; ++v)
+      for (int h = 0; h < C::HPT; ++h) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m[h], off);
+        const float l2 = __shfl_xor_sync(0xffffffffu, l[h], off);
+        const float M = fmaxf(m[h], m2);
+        const float a1 = m[h] == -INFINITY ? 0.f : fast_exp2(m[h] - M);
+        const float a2 = m2 == -INFINITY ? 0.f : fast_exp2(m2 - M);
+        l[h] = l[h] * a1 + l2 * a2;
 #pragma unroll
-        for (int e = 0; e < C::E; ++e)
-          s_o[(slot * G + head) * D + (c + v * C::LPT) * C::E + e] = o[h][v * C::E + e];
-      if (c == 0) {
-        s_m[slot * G + head] = m[h];
-        s_l[slot * G + head] = l[h];
+        for (int x = 0; x < C::DPT; ++x) {
+          const float o2 = __shfl_xor_sync(0xffffffffu, o[h][x], off);
+          o[h][x] = o[h][x] * a1 + o2 * a2;
+        }
+        m[h] = M;
       }
     }
-    __syncthreads();
+    // ---- across the four warps through shared memory
+    named_sync(1, 128);  // the scratch of the previous item has been read
+    if (tgrp == 0) {
+#pragma unroll
+      for (int h = 0; h < C::HPT; ++h) {
+        const int head = hg * C::HPT + h;
+#pragma unroll
+        for (int v = 0; v < C::VPT; ++v)
+#pragma unroll
+          for (int e = 0; e < C::E; ++e)
+            s_o[(warp * G + head) * D + (c + v * C::LPT) * C::E + e] = o[h][v * C::E + e];
+        if (c == 0) {
+          s_m[warp * G + head] = m[h];
+          s_l[warp * G + head] = l[h];
+        }
+      }
+    }
+    named_sync(1, 128);
     const int e0 = tid * C::OPT;
     if (e0 < G * D) {
       const int h = e0 / D, d0 = e0 % D;
       float M = -INFINITY;
-      for (int sl = 0; sl < C::TPS; ++sl) M = fmaxf(M, s_m[sl * G + h]);
+#pragma unroll
+      for (int w = 0; w < C::NWARP; ++w) M = fmaxf(M, s_m[w * G + h]);
       float L = 0.f, acc[C::OPT];
 #pragma unroll
       for (int x = 0; x < C::OPT; ++x) acc[x] = 0.f;
-      for (int sl = 0; sl < C::TPS; ++sl) {
-        const float ms = s_m[sl * G + h];
-        if (ms == -INFINITY) continue;
-        const float w = fast_exp2(ms - M);
-        L = fmaf(s_l[sl * G + h], w, L);
 #pragma unroll
-        for (int x = 0; x < C::OPT; ++x) acc[x] = fmaf(s_o[(sl * G + h) * D + d0 + x], w, acc[x]);
+      for (int w = 0; w < C::NWARP; ++w) {
+        const float ms = s_m[w * G + h];
+        if (ms == -INFINITY) continue;
+        const float wt = fast_exp2(ms - M);
+        L = fmaf(s_l[w * G + h], wt, L);
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) acc[x] = fmaf(s_o[(w * G + h) * D + d0 + x], wt, acc[x]);
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
-      if (direct) {
-        T *dst = reinterpret_cast<T *>(p.out) + ((size_t)tok * H + kvh * G + h) * D + d0;
+      if (d.direct) {
+        T *dst = reinterpret_cast<T *>(p.out) + ((size_t)d.tok * H + kvh * G + h) * D + d0;
 #pragma unroll
         for (int x = 0; x < C::OPT; ++x) store_elem(dst + x, acc[x] * inv);
       } else {
-        const long long prow = prow0 + (long long)h * r.nsplit;
+        const long long prow = d.prow0 + (long long)h * d.nsplit;
 #pragma unroll
         for (int x = 0; x < C::OPT; ++x) p.part_o[prow * D + d0 + x] = acc[x] * inv;
         if (d0 == 0) p.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
       }
     }
-    fence_proxy_async();  // generic use of the ring ends before TMA refills it
-    __syncthreads();
   }
 }
 
@@ -368,6 +448,9 @@ cudaError_t launch_one(const FwdParams &p, const CUtensorMap &tk, const CUtensor
   cudaError_t err = cudaFuncSetAttribute(row_kernel<T, D, G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (err != cudaSuccess) return err;
+  err = cudaFuncSetAttribute(row_kernel<T, D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (err != cudaSuccess) return err;
   row_kernel<T, D, G><<<grid, C::NTHREADS, C::SMEM, stream>>>(tk, tv, p);
   return cudaGetLastError();
 }
@@ -376,7 +459,9 @@ template <typename T, int D, int G>
 int occupancy_one() {
   using C = RowCfg<T, D, G>;
   if (cudaFuncSetAttribute(row_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           C::SMEM) != cudaSuccess)
+                           C::SMEM) != cudaSuccess ||
+      cudaFuncSetAttribute(row_kernel<T, D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return 0;
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_kernel<T, D, G>, C::NTHREADS,

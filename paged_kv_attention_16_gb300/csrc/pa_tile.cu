@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   const int G = p.num_heads / p.num_kv_heads;
   const int H = p.num_heads, bs = p.block_size;
   const long long n_items = p.plan->n[kListTile];
+  if (n_items == 0) return;  // no extend / prefill rows in this batch
 
   if (tid == 0) {
     prefetch_tensor_map(&tm_q);
@@ -267,6 +268,12 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       const bool row_valid = i < it.q_len;
       const int row_hi_full = it.prefix + i + 1;
       const int row_hi = row_valid ? min(row_hi_full, it.kv_lo + it.split_len) : it.kv_lo;
+      // Warps whose 32 rows are all padding (a decode tile holds G rows) keep
+      // the barrier protocol but skip the TMEM traffic and the exponentials.
+      const bool warp_active = __any_sync(0xffffffffu, row_hi > it.kv_lo);
+      // exp2(s * c - m) as one FFMA needs c > 0; otherwise scale first.
+      const float c2 = p.scale_log2;
+      const bool fold = c2 > 0.f;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.nt; ++j) {
         const uint32_t g = tiles + j;
@@ -274,64 +281,76 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         mbar_wait(&bar[kSFull], g & 1, dead, p.status);
         tc_fence_after();
         float s[kBN];
+        if (warp_active) {
 #pragma unroll
-        for (int c0 = 0; c0 < kBN; c0 += 32) {
-          uint32_t raw[32];
-          tc_ld32(tmem + lane_off + kTmemS + c0, raw);
-          tc_wait_ld();
+          for (int c0 = 0; c0 < kBN; c0 += 32) {
+            uint32_t raw[32];
+            tc_ld32(tmem + lane_off + kTmemS + c0, raw);
+            tc_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) s[c0 + x] = __uint_as_float(raw[x]);
+            for (int x = 0; x < 32; ++x) s[c0 + x] = __uint_as_float(raw[x]);
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kSFree]);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          s[c] = (base + c < row_hi) ? s[c] * p.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, s[c]);
-        }
         // P and O may be touched only after the previous PV product is done.
         if (j > 0) mbar_wait(&bar[kODone], (g - 1) & 1, dead, p.status);
         tc_fence_after();
-        float alpha = 1.f;
-        bool rescale = false;
-        if (mx > m + kTau) {
-          alpha = fast_exp2(m - mx);
-          l *= alpha;
-          m = mx;
-          rescale = j > 0;
-        }
-        if (__any_sync(0xffffffffu, rescale)) {
-          const float a = rescale ? alpha : 1.f;
+        if (warp_active) {
+          // Only tiles that cross a row's bound need the select.
+          if (__any_sync(0xffffffffu, base + kBN > row_hi)) {
 #pragma unroll
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t raw[32];
-            tc_ld32(tmem + lane_off + kTmemO + c0, raw);
-            tc_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * a);
-            tc_st32(tmem + lane_off + kTmemO + c0, raw);
+            for (int c = 0; c < kBN; ++c) s[c] = (base + c < row_hi) ? s[c] : -INFINITY;
           }
-          tc_wait_st();
-        }
-        const float mu = m == -INFINITY ? 0.f : m;
-        float sum = 0.f;
-        uint8_t *prow = sP + r * 128;
+          if (!fold) {
 #pragma unroll
-        for (int ch = 0; ch < kBN / 8; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float p0 = fast_exp2(s[ch * 8 + 2 * x] - mu);
-            const float p1 = fast_exp2(s[ch * 8 + 2 * x + 1] - mu);
-            sum += p0 + p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            w[x] = *reinterpret_cast<const uint32_t *>(&h2);
+            for (int c = 0; c < kBN; ++c) s[c] *= c2;
           }
-          *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+          if (fold && mx != -INFINITY) mx *= c2;
+          float alpha = 1.f;
+          bool rescale = false;
+          if (mx > m + kTau) {
+            alpha = fast_exp2(m - mx);
+            l *= alpha;
+            m = mx;
+            rescale = j > 0;
+          }
+          if (__any_sync(0xffffffffu, rescale)) {
+            const float a = rescale ? alpha : 1.f;
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+              uint32_t raw[32];
+              tc_ld32(tmem + lane_off + kTmemO + c0, raw);
+              tc_wait_ld();
+#pragma unroll
+              for (int x = 0; x < 32; ++x) raw[x] = __float_as_uint(__uint_as_float(raw[x]) * a);
+              tc_st32(tmem + lane_off + kTmemO + c0, raw);
+            }
+            tc_wait_st();
+          }
+          const float mu = m == -INFINITY ? 0.f : m;
+          const float cs = fold ? c2 : 1.f;
+          float sum = 0.f;
+          uint8_t *prow = sP + r * 128;
+#pragma unroll
+          for (int ch = 0; ch < kBN / 8; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const float p0 = fast_exp2(fmaf(s[ch * 8 + 2 * x], cs, -mu));
+              const float p1 = fast_exp2(fmaf(s[ch * 8 + 2 * x + 1], cs, -mu));
+              sum += p0 + p1;
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+              w[x] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+            *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          l += sum;
         }
-        l += sum;
         if (j == it.nt - 1 && it.kv_hi - base < kBN) {
           // Rows past the tile's KV end may hold anything (NaN tails, stale
           // data); P is 0 there but 0 * NaN is NaN, so zero those V rows.
@@ -362,6 +381,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       const long long prow = it.partial_base + ((long long)i * H + head) * it.nsplit + it.split;
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
+        if (!warp_active) break;
         uint32_t raw[32];
         tc_ld32(tmem + lane_off + kTmemO + c0, raw);
         tc_wait_ld();
@@ -415,6 +435,9 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
   using C = TileCfg<D>;
   cudaError_t e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        C::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   tile_kernel<D><<<num_sms * 2, kTileThreads, C::SMEM, stream>>>(tq, tk, tv, p);
   return cudaGetLastError();
