@@ -55,7 +55,8 @@ typedef enum {
   PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment ...   */
   PA_ERR_UNSUPPORTED = 2, /* a shape or dtype this build has no kernel for     */
   PA_ERR_WORKSPACE = 3,   /* workspace too small while the stream is capturing */
-  PA_ERR_CUDA = 4         /* a CUDA runtime / driver call failed               */
+  PA_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed               */
+  PA_ERR_SCRATCH_LIMIT = 5 /* the call needs more than the static scratch region */
 } pa_status;
 
 /* Device status bits (see above). */
@@ -117,6 +118,55 @@ size_t pa_forward_workspace_bytes(pa_dtype dtype, int num_seqs, int num_tokens,
                                   int num_heads, int num_kv_heads,
                                   int head_dim, int max_seq_len,
                                   int kv_split_tokens);
+
+/*
+ * pa_forward_static_scratch -- pa_forward without any device allocation.
+ *
+ * The pages describe no counterpart of this entry point.  It serves callers
+ * that must not allocate device memory while attention runs:
+ *   - code running while a CUDA graph is captured in global or thread-local
+ *     capture mode, where cudaMalloc / cudaFree are illegal and pa_forward
+ *     would otherwise need a pa_reserve call made beforehand;
+ *   - serving runtimes that hand all device memory to their own pool up
+ *     front and account for every byte, so a library that allocates or grows
+ *     its own workspace breaks their budget;
+ *   - latency-critical loops that cannot afford pa_forward's on-demand
+ *     workspace growth (freeing the old buffer synchronises the device).
+ * It computes exactly what pa_forward computes, with the same kernels.  Its
+ * scratch (planner tables, work counters, split partials) is one fixed region
+ * of PA_STATIC_SCRATCH_BYTES that libpa.so declares as a file-scope
+ * __device__ array: every GPU that loads the library holds that region until
+ * the process exits.
+ *
+ * Arguments: those of pa_forward, plus
+ *   device_status  optional device pointer to one uint32 owned by the caller;
+ *                  the PA_DEV_* bits of this call are OR-ed into it (clearing
+ *                  it is the caller's job).  NULL: the bits land in a word
+ *                  inside the static region and are not reported.
+ * Returns PA_ERR_SCRATCH_LIMIT and launches nothing when the call needs more
+ * scratch than the region holds, i.e. when pa_forward_workspace_bytes() for
+ * the same extents exceeds PA_STATIC_SCRATCH_BYTES - 256 (a decode batch of 64
+ * sequences, 32 heads, head_dim 128 and max_seq_len 8192 needs about 34 MB).
+ * Otherwise the status codes of pa_forward (never PA_ERR_WORKSPACE).
+ *
+ * The first call on each device looks up the region's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call outside any stream capture.  All calls share the one region,
+ * which keeps the last call's contents (each call's planner rewrites, in
+ * stream order, every table and counter the call reads): calls that overlap
+ * on the GPU -- on different streams, or from host threads without ordering --
+ * race on it and must be serialised by the caller.  Kernel timing
+ * (pa_profile_*) is not recorded for this entry point.
+ */
+#define PA_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+pa_status pa_forward_static_scratch(
+    const void *q, const void *k_cache, const void *v_cache,
+    const int32_t *block_table, const int32_t *seq_lens,
+    const int32_t *query_start_loc, int num_heads, int num_kv_heads,
+    int head_dim, int block_size, float scale, void *out, void *stream,
+    pa_dtype dtype, int num_seqs, int num_tokens, int max_blocks_per_seq,
+    int num_blocks, int max_seq_len, int kv_split_tokens,
+    uint32_t *device_status);
 
 /*
  * pa_mla_decode -- absorbed multi-head latent attention decode ("vLLM AMD ROCm

@@ -577,6 +577,125 @@ bool tile_path_ok(int dtype, int head_dim, int group) {
 
 }  // namespace
 
+pa_status fwd_check(const FwdCall &c) {
+  if (c.num_seqs < 0 || c.num_tokens < 0 || c.max_seq_len < 0 || c.kv_split_tokens < 0 ||
+      c.num_heads <= 0 || c.num_kv_heads <= 0 || c.head_dim <= 0 || c.block_size <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (c.dtype != PA_F32 && c.dtype != PA_BF16) return PA_ERR_INVALID_ARG;
+  if (c.num_heads % c.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+  const int group = c.num_heads / c.num_kv_heads;
+  if (!group_ok(group) || (c.head_dim != 64 && c.head_dim != 128) || c.block_size % 16 != 0 ||
+      c.block_size > 256 || c.kv_split_tokens % 16 != 0)
+    return PA_ERR_UNSUPPORTED;
+  if (c.num_tokens == 0) return PA_OK;  // no output rows
+  if (!c.q || !c.out || !c.qsl || (c.num_seqs > 0 && (!c.seq_lens || !c.block_table)))
+    return PA_ERR_INVALID_ARG;
+  if (c.num_seqs > 0 &&
+      (!c.k_cache || !c.v_cache || c.num_blocks <= 0 || c.max_blocks_per_seq <= 0))
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(c.q) || !aligned16(c.out) ||
+      (c.num_seqs > 0 && (!aligned16(c.k_cache) || !aligned16(c.v_cache))))
+    return PA_ERR_INVALID_ARG;
+  if ((long long)c.num_tokens * c.num_heads * c.head_dim > (1ll << 40)) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+size_t fwd_workspace_bytes(const FwdCall &c) {
+  const bool tile_ok = tile_path_ok(c.dtype, c.head_dim, c.num_heads / c.num_kv_heads);
+  return fwd_layout(c.num_seqs, c.num_tokens, c.num_heads, c.head_dim, c.max_seq_len,
+                    c.kv_split_tokens, tile_ok)
+      .total;
+}
+
+pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, int num_sms,
+                     cudaStream_t st, bool timed) {
+  const int group = c.num_heads / c.num_kv_heads;
+  const bool tile_ok = tile_path_ok(c.dtype, c.head_dim, group);
+  const FwdLayout lay = fwd_layout(c.num_seqs, c.num_tokens, c.num_heads, c.head_dim,
+                                   c.max_seq_len, c.kv_split_tokens, tile_ok);
+  const int row_ctas = row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * num_sms;
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  FwdParams p{};
+  p.q = c.q;
+  p.out = c.out;
+  p.block_table = c.block_table;
+  p.seq_lens = c.seq_lens;
+  p.qsl = c.qsl;
+  p.num_seqs = c.num_seqs;
+  p.num_tokens = c.num_tokens;
+  p.num_heads = c.num_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = c.block_size;
+  p.max_blocks_per_seq = c.max_blocks_per_seq;
+  p.num_blocks = c.num_blocks;
+  p.max_seq_len = c.max_seq_len;
+  p.kv_split_tokens = c.kv_split_tokens;
+  p.scale = c.scale;
+  p.scale_log2 = c.scale * kLog2e;
+  p.tile_ok = tile_ok ? 1 : 0;
+  p.row_ctas = row_ctas;
+  p.dtype = c.dtype;
+  p.plan = reinterpret_cast<PlanHeader *>(ws + lay.plan);
+  p.req = reinterpret_cast<ReqInfo *>(ws + lay.req);
+  p.ord = reinterpret_cast<int *>(ws + lay.ord);
+  p.list_end = reinterpret_cast<long long *>(ws + lay.list_end);
+  p.part_o = reinterpret_cast<float *>(ws + lay.part_o);
+  p.part_lse = reinterpret_cast<float *>(ws + lay.part_lse);
+  p.part_cap = lay.part_cap;
+  p.status = status;
+
+  int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
+  plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+  prof_end(slot, st);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+  if (c.num_seqs > 0) {
+    CUtensorMap tm_k, tm_v;
+    if (!encode_cache_map(&tm_k, c.k_cache, c.dtype, c.num_blocks, c.block_size, c.num_kv_heads,
+                          c.head_dim, c.head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_cache_map(&tm_v, c.v_cache, c.dtype, c.num_blocks, c.block_size, c.num_kv_heads,
+                          c.head_dim, c.head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return PA_ERR_CUDA;
+    slot = timed ? prof_begin(PA_K_ROW, st) : -1;
+    const cudaError_t row_err = launch_row_kernel(p, tm_k, tm_v, row_ctas, st);
+    prof_end(slot, st);
+    if (row_err != cudaSuccess) return PA_ERR_CUDA;
+    if (tile_ok) {
+      CUtensorMap tm_q, tm_kt, tm_vt;
+      // Q as [tokens, heads, dim] with 64-element (128-byte) swizzled boxes of
+      // G heads x (128 / G) tokens; K/V pages as 64-element swizzled boxes.
+      EncodeTiledFn fn = encode_fn();
+      cuuint64_t qd[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_heads,
+                          (cuuint64_t)c.num_tokens};
+      cuuint64_t qs[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)c.num_heads * c.head_dim * 2};
+      cuuint32_t qb[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileRows / group)};
+      cuuint32_t qe[3] = {1, 1, 1};
+      if (!fn ||
+          fn(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(c.q), qd, qs, qb, qe,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+          !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
+                            c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+          !encode_cache_map(&tm_vt, c.v_cache, c.dtype, c.num_blocks, c.block_size,
+                            c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+        return PA_ERR_CUDA;
+      slot = timed ? prof_begin(PA_K_TILE, st) : -1;
+      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vt, num_sms, st);
+      prof_end(slot, st);
+      if (tile_err != cudaSuccess) return PA_ERR_CUDA;
+    }
+  }
+  slot = timed ? prof_begin(PA_K_MERGE, st) : -1;
+  if (c.dtype == PA_BF16)
+    merge_kernel<__nv_bfloat16><<<num_sms * 4, kMergeThreads, 0, st>>>(p);
+  else
+    merge_kernel<float><<<num_sms * 4, kMergeThreads, 0, st>>>(p);
+  prof_end(slot, st);
+  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
 pa_status device_resources(cudaStream_t stream, size_t ws_bytes, void **ws,
                            unsigned int **status, int *num_sms) {
   DeviceState *d = nullptr;
@@ -623,6 +742,7 @@ const char *pa_status_string(pa_status status) {
     case PA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
     case PA_ERR_WORKSPACE: return "workspace too small during stream capture";
     case PA_ERR_CUDA: return "CUDA error";
+    case PA_ERR_SCRATCH_LIMIT: return "call exceeds the static scratch region";
   }
   return "unknown status";
 }
@@ -671,115 +791,18 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
                      int head_dim, int block_size, float scale, void *out, void *stream,
                      pa_dtype dtype, int num_seqs, int num_tokens, int max_blocks_per_seq,
                      int num_blocks, int max_seq_len, int kv_split_tokens) {
-  // ---- host argument checks ---------------------------------------------------
-  if (num_seqs < 0 || num_tokens < 0 || max_seq_len < 0 || kv_split_tokens < 0 ||
-      num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0)
-    return PA_ERR_INVALID_ARG;
-  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_INVALID_ARG;
-  if (num_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-  const int group = num_heads / num_kv_heads;
-  if (!group_ok(group) || (head_dim != 64 && head_dim != 128) || block_size % 16 != 0 ||
-      block_size > 256 || kv_split_tokens % 16 != 0)
-    return PA_ERR_UNSUPPORTED;
-  if (num_tokens == 0) return PA_OK;  // no output rows
-  if (!q || !out || !query_start_loc || (num_seqs > 0 && (!seq_lens || !block_table)))
-    return PA_ERR_INVALID_ARG;
-  if (num_seqs > 0 && (!k_cache || !v_cache || num_blocks <= 0 || max_blocks_per_seq <= 0))
-    return PA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(out) || (num_seqs > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
-    return PA_ERR_INVALID_ARG;
-  if ((long long)num_tokens * num_heads * head_dim > (1ll << 40)) return PA_ERR_UNSUPPORTED;
-
+  const FwdCall c{q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
+                  num_kv_heads, head_dim, block_size, scale, out, dtype, num_seqs, num_tokens,
+                  max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens};
+  pa_status s = fwd_check(c);
+  if (s != PA_OK || num_tokens == 0) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   DeviceState *d = nullptr;
-  pa_status s = device_state(st, &d);
+  s = device_state(st, &d);
   if (s != PA_OK) return s;
-  const bool tile_ok = tile_path_ok(dtype, head_dim, group);
-  const FwdLayout lay = fwd_layout(num_seqs, num_tokens, num_heads, head_dim, max_seq_len,
-                                   kv_split_tokens, tile_ok);
-  s = ensure_workspace(d, lay.total, st);
+  s = ensure_workspace(d, fwd_workspace_bytes(c), st);
   if (s != PA_OK) return s;
-
-  const int row_ctas = row_ctas_per_sm_cached(dtype, head_dim, group) * d->num_sms;
-  uint8_t *ws = reinterpret_cast<uint8_t *>(d->ws);
-  FwdParams p{};
-  p.q = q;
-  p.out = out;
-  p.block_table = block_table;
-  p.seq_lens = seq_lens;
-  p.qsl = query_start_loc;
-  p.num_seqs = num_seqs;
-  p.num_tokens = num_tokens;
-  p.num_heads = num_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.head_dim = head_dim;
-  p.block_size = block_size;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_blocks = num_blocks;
-  p.max_seq_len = max_seq_len;
-  p.kv_split_tokens = kv_split_tokens;
-  p.scale = scale;
-  p.scale_log2 = scale * kLog2e;
-  p.tile_ok = tile_ok ? 1 : 0;
-  p.row_ctas = row_ctas;
-  p.dtype = dtype;
-  p.plan = reinterpret_cast<PlanHeader *>(ws + lay.plan);
-  p.req = reinterpret_cast<ReqInfo *>(ws + lay.req);
-  p.ord = reinterpret_cast<int *>(ws + lay.ord);
-  p.list_end = reinterpret_cast<long long *>(ws + lay.list_end);
-  p.part_o = reinterpret_cast<float *>(ws + lay.part_o);
-  p.part_lse = reinterpret_cast<float *>(ws + lay.part_lse);
-  p.part_cap = lay.part_cap;
-  p.status = d->status;
-
-  int slot = prof_begin(PA_K_PLAN, st);
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
-  prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-
-  if (num_seqs > 0) {
-    CUtensorMap tm_k, tm_v;
-    if (!encode_cache_map(&tm_k, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
-                          head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_cache_map(&tm_v, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
-                          head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
-      return PA_ERR_CUDA;
-    slot = prof_begin(PA_K_ROW, st);
-    const cudaError_t row_err = launch_row_kernel(p, tm_k, tm_v, row_ctas, st);
-    prof_end(slot, st);
-    if (row_err != cudaSuccess) return PA_ERR_CUDA;
-    if (tile_ok) {
-      CUtensorMap tm_q, tm_kt, tm_vt;
-      // Q as [tokens, heads, dim] with 64-element (128-byte) swizzled boxes of
-      // G heads x (128 / G) tokens; K/V pages as 64-element swizzled boxes.
-      EncodeTiledFn fn = encode_fn();
-      cuuint64_t qd[3] = {(cuuint64_t)head_dim, (cuuint64_t)num_heads, (cuuint64_t)num_tokens};
-      cuuint64_t qs[2] = {(cuuint64_t)head_dim * 2, (cuuint64_t)num_heads * head_dim * 2};
-      cuuint32_t qb[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileRows / group)};
-      cuuint32_t qe[3] = {1, 1, 1};
-      if (!fn ||
-          fn(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), qd, qs, qb, qe,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-          !encode_cache_map(&tm_kt, k_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
-                            64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_cache_map(&tm_vt, v_cache, dtype, num_blocks, block_size, num_kv_heads, head_dim,
-                            64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
-        return PA_ERR_CUDA;
-      slot = prof_begin(PA_K_TILE, st);
-      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vt, d->num_sms, st);
-      prof_end(slot, st);
-      if (tile_err != cudaSuccess) return PA_ERR_CUDA;
-    }
-  }
-  slot = prof_begin(PA_K_MERGE, st);
-  if (dtype == PA_BF16)
-    merge_kernel<__nv_bfloat16><<<d->num_sms * 4, kMergeThreads, 0, st>>>(p);
-  else
-    merge_kernel<float><<<d->num_sms * 4, kMergeThreads, 0, st>>>(p);
-  prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-  return PA_OK;
+  return fwd_launch(c, d->ws, d->status, d->num_sms, st, true);
 }
 
 pa_status pa_debug_gather(const void *k_cache, const int32_t *block_table,

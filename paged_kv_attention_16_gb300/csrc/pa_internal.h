@@ -25,6 +25,25 @@ cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_k, const CUtensorMap &tm_v, int grid,
                                cudaStream_t stream);
 
+// One pa_forward call's host-side arguments.
+struct FwdCall {
+  const void *q, *k_cache, *v_cache;
+  const int32_t *block_table, *seq_lens, *qsl;
+  int num_heads, num_kv_heads, head_dim, block_size;
+  float scale;
+  void *out;
+  pa_dtype dtype;
+  int num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
+};
+// Host-side argument checks of pa_forward (PA_OK also when num_tokens == 0).
+pa_status fwd_check(const FwdCall &c);
+// Workspace bytes the call needs.
+size_t fwd_workspace_bytes(const FwdCall &c);
+// The launch sequence (planner, row kernel, tile kernel, merge) on a given
+// workspace and device status word; records kernel timing when `timed`.
+pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, int num_sms,
+                     cudaStream_t stream, bool timed);
+
 // Library-owned per-device resources for an entry point: workspace of at
 // least ws_bytes (grown outside capture), the device status word, SM count.
 pa_status device_resources(cudaStream_t stream, size_t ws_bytes, void **ws,

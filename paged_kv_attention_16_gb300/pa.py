@@ -15,6 +15,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libpa.so")
 
 PA_F32, PA_BF16 = 0, 1
 PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+PA_ERR_SCRATCH_LIMIT = 5
+PA_STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
 PA_DEV_BAD_BLOCK = 0x1
 PA_DEV_BAD_QLEN = 0x2
 PA_DEV_BAD_SEQLEN = 0x4
@@ -26,7 +28,7 @@ PA_DEV_TIMEOUT = 0x20
 EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode",
            "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
-           "pa_profile_read", "pa_kernel_name")
+           "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch")
 PA_K_COUNT = 8
 
 
@@ -73,6 +75,8 @@ def lib():
         L.pa_profile_enable.restype = c_int
         L.pa_profile_read.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(c_int)]
         L.pa_profile_read.restype = c_int
+        L.pa_forward_static_scratch.argtypes = L.pa_forward.argtypes + [vp]
+        L.pa_forward_static_scratch.restype = c_int
         L.pa_kernel_name.argtypes = [c_int]
         L.pa_kernel_name.restype = ctypes.c_char_p
         _lib = L
@@ -126,6 +130,25 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
         int(kv_split_tokens))
     if check:
         _check(st, "pa_forward")
+    return st
+
+
+def pa_forward_static_scratch(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                              num_heads, num_kv_heads, head_dim, block_size, scale, out,
+                              stream=None, *, max_seq_len, kv_split_tokens=0, num_blocks=None,
+                              device_status=None, check=True):
+    """pa_forward with no device allocation (scratch in the library's fixed
+    static region); device_status: optional int32 device tensor of one
+    element that receives the PA_DEV_* bits."""
+    st = lib().pa_forward_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(query_start_loc), int(num_heads), int(num_kv_heads), int(head_dim),
+        int(block_size), float(scale), _ptr(out), _stream_ptr(stream), _dtype_code(q),
+        int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
+        int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
+        int(kv_split_tokens), _ptr(device_status))
+    if check:
+        _check(st, "pa_forward_static_scratch")
     return st
 
 
