@@ -38,11 +38,12 @@ struct ReqScalars {
   bool valid;
 };
 
-__device__ inline ReqScalars read_req(const FwdParams &p, int s, bool qsl_bad) {
+__device__ inline ReqScalars classify(const FwdParams &p, int q_start, int q_end, int ctx,
+                                      bool qsl_bad) {
   ReqScalars r;
-  r.q_start = p.qsl[s];
-  r.q_len = p.qsl[s + 1] - r.q_start;
-  r.ctx = p.seq_lens[s];
+  r.q_start = q_start;
+  r.q_len = q_end - q_start;
+  r.ctx = ctx;
   r.valid = !qsl_bad && r.q_len >= 0 && r.ctx >= 0 && r.q_len <= r.ctx &&
             r.ctx <= p.max_seq_len &&
             ceil_div_ll(r.ctx, p.block_size) <= (long long)p.max_blocks_per_seq;
@@ -53,25 +54,38 @@ __device__ inline ReqScalars read_req(const FwdParams &p, int s, bool qsl_bad) {
   return r;
 }
 
+// Requests handled from shared memory in one pass per step; larger batches
+// loop over chunks of kPlanThreads and re-read the metadata.
+constexpr int kPlanCache = kPlanThreads;
+
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
-  __shared__ long long scratch[33];
+  __shared__ long long scratch[5 * 33];
+  __shared__ int4 s_req[kPlanCache];  // q_start, q_end, ctx, -
+  __shared__ int s_ord[kPlanCache];
   const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x;
   const int Hk = p.num_kv_heads, G = p.num_heads / p.num_kv_heads, H = p.num_heads;
+  const bool cached = S <= kPlanCache;
+  auto raw = [&](int s) -> int4 {
+    if (cached) return s_req[s];
+    return make_int4(p.qsl[s], p.qsl[s + 1], p.seq_lens[s], 0);
+  };
 
-  // -- global query_start_loc checks -------------------------------------------
+  // -- one read of the metadata, and the global query_start_loc checks -------
   int bad = 0;
+  if (cached && tid < S) s_req[tid] = make_int4(p.qsl[tid], p.qsl[tid + 1], p.seq_lens[tid], 0);
   if (tid == 0 && (p.qsl[0] != 0 || p.qsl[S] != T)) bad = 1;
   for (int s = tid; s < S; s += kPlanThreads)
     if (p.qsl[s + 1] < p.qsl[s]) bad = 1;
   const bool qsl_bad = __syncthreads_or(bad) != 0;
 
-  // -- pass 1: class counts and the decode KV work (split sizing) --------------
-  long long packed = 0, dec_work = 0;
+  // -- pass 1: class counts and the decode KV work (split sizing) ------------
+  long long v1[2] = {0, 0};  // packed class counts (21 bits each), decode work
   int metabad = 0;
   for (int s = tid; s < S; s += kPlanThreads) {
-    const ReqScalars r = read_req(p, s, qsl_bad);
-    packed += 1ll << (21 * r.cls);
-    if (r.valid && r.q_len == 1) dec_work += r.ctx;
+    const int4 q = raw(s);
+    const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
+    v1[0] += 1ll << (21 * r.cls);
+    if (r.valid && r.q_len == 1) v1[1] += r.ctx;
     if (!qsl_bad && !r.valid) {
       if (r.q_len < 0 || r.q_len > r.ctx) metabad |= PA_DEV_BAD_QLEN;
       if (r.ctx < 0 || r.ctx > p.max_seq_len ||
@@ -81,9 +95,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   }
   if (metabad) atomicOr(p.status, (unsigned)metabad);
   if (tid == 0 && qsl_bad) atomicOr(p.status, PA_DEV_BAD_QSL);
-  long long class_tot, work_tot;
-  block_inclusive_scan(packed, scratch, &class_tot);
-  block_inclusive_scan(dec_work, scratch, &work_tot);
+  long long t1[2];
+  block_scan_multi<2>(v1, scratch, t1);
+  const long long class_tot = t1[0], work_tot = t1[1];
   const long long mask21 = (1ll << 21) - 1;
   const long long n_dec = class_tot & mask21, n_ext = (class_tot >> 21) & mask21;
 
@@ -100,37 +114,41 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   if (Lr > kRowMaxSplit) Lr = kRowMaxSplit;
   if (p.kv_split_tokens > 0 && p.kv_split_tokens < Lr) Lr = p.kv_split_tokens;
 
-  // -- pass 2: stable partition into [decode : extend : prefill] ---------------
+  // -- pass 2: stable partition into [decode : extend : prefill] -------------
   long long carry = 0;
   for (int base = 0; base < S; base += kPlanThreads) {
     const int s = base + tid;
-    long long v = 0;
+    long long v[1] = {0};
     int cls = 0;
     if (s < S) {
-      cls = read_req(p, s, qsl_bad).cls;
-      v = 1ll << (21 * cls);
+      const int4 q = raw(s);
+      cls = classify(p, q.x, q.y, q.z, qsl_bad).cls;
+      v[0] = 1ll << (21 * cls);
     }
-    long long chunk_tot;
-    const long long incl = block_inclusive_scan(v, scratch, &chunk_tot) + carry;
+    long long ct[1];
+    block_scan_multi<1>(v, scratch, ct);
+    const long long incl = v[0] + carry;
     if (s < S) {
       const long long before = ((incl >> (21 * cls)) & mask21) - 1;
       const long long off = cls == kDecode ? 0 : cls == kExtend ? n_dec : n_dec + n_ext;
       p.ord[off + before] = s;
+      if (cached) s_ord[off + before] = s;
     }
-    carry += chunk_tot;
+    carry += ct[0];
   }
   __syncthreads();
 
-  // -- pass 3: per-request plan and list prefix sums in reordered order --------
-  long long run[kNumLists] = {0, 0, 0, 0}, run_part = 0;
+  // -- pass 3: per-request plan and list prefix sums in reordered order ------
+  long long run[kNumLists + 1] = {0, 0, 0, 0, 0};  // lists, then partial rows
   for (int base = 0; base < S; base += kPlanThreads) {
     const int k = base + tid;
-    long long cnt[kNumLists] = {0, 0, 0, 0}, part = 0;
+    long long cnt[kNumLists + 1] = {0, 0, 0, 0, 0};
     int s = -1;
     ReqInfo info{};
     if (k < S) {
-      s = p.ord[k];
-      const ReqScalars r = read_req(p, s, qsl_bad);
+      s = cached ? s_ord[k] : p.ord[k];
+      const int4 q = raw(s);
+      const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
       // Decode rows stream on CUDA cores while G < 8; from G = 8 the FFMA
       // issue rate, not HBM, would bound them, so they join the tensor-core
       // tile path (one token x G heads per 128-row tile).
@@ -155,25 +173,25 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
         else cnt[kListTile] = (long long)Hk * ceil_div_ll((long long)r.q_len * G, kTileRows) * nsplit;
         if (nsplit > 1) {
           cnt[kListMerge] = (long long)r.q_len * H;
-          part = (long long)r.q_len * H * nsplit;
+          cnt[kNumLists] = (long long)r.q_len * H * nsplit;
         }
       } else if (!qsl_bad && r.q_len > 0) {
         cnt[kListZero] = (long long)r.q_len * H;
       }
     }
-    long long tot;
-    const long long part_incl = block_inclusive_scan(part, scratch, &tot) + run_part;
-    info.partial_base = part_incl - part;
-    run_part += tot;
+    const long long part = cnt[kNumLists];
+    long long tot[kNumLists + 1];
+    block_scan_multi<kNumLists + 1>(cnt, scratch, tot);
+    info.partial_base = cnt[kNumLists] + run[kNumLists] - part;
 #pragma unroll
-    for (int x = 0; x < kNumLists; ++x) {
-      const long long incl = block_inclusive_scan(cnt[x], scratch, &tot) + run[x];
-      if (k < S) p.list_end[(size_t)x * S + k] = incl;
-      run[x] += tot;
-    }
+    for (int x = 0; x < kNumLists; ++x)
+      if (k < S) p.list_end[(size_t)x * S + k] = cnt[x] + run[x];
+#pragma unroll
+    for (int x = 0; x <= kNumLists; ++x) run[x] += tot[x];
     if (k < S) p.req[s] = info;
   }
   if (tid == 0) {
+    const long long run_part = run[kNumLists];
     const bool overflow = run_part > p.part_cap;
     if (overflow) atomicOr(p.status, PA_DEV_OVERFLOW);
     const bool zero_all = qsl_bad || overflow;

@@ -235,6 +235,46 @@ __device__ inline long long block_inclusive_scan(long long v, long long *scratch
   return x;
 }
 
+// Block-wide inclusive scan of N 64-bit counts at once (one pair of
+// barriers for all N).  `scratch` holds N * 33 long longs; tot[i] receives
+// the block total of v[i].  All threads must call.
+template <int N>
+__device__ inline void block_scan_multi(long long (&v)[N], long long *scratch,
+                                        long long (&tot)[N]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int nwarps = blockDim.x >> 5;
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, v[i], o);
+      if (lane >= o) v[i] += y;
+    }
+    if (lane == 31) scratch[i * 33 + warp] = v[i];
+  }
+  __syncthreads();
+  if (warp == 0) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+      long long w = lane < nwarps ? scratch[i * 33 + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nwarps) scratch[i * 33 + lane] = w;
+      if (lane == nwarps - 1) scratch[i * 33 + 32] = w;
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    if (warp > 0) v[i] += scratch[i * 33 + warp - 1];
+    tot[i] = scratch[i * 33 + 32];
+  }
+  __syncthreads();
+}
+
 }  // namespace pa
 
 namespace pa {
@@ -275,6 +315,18 @@ __device__ inline void tc_mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bde
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Same MMA with the A operand (M x K, K-major, bf16 pairs packed in 32-bit
+// columns, row i in lane i) read from tensor memory at `tmem_a`.
+__device__ inline void tc_mma_bf16_ts(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                      uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 

@@ -16,13 +16,15 @@
 //            {64 dims x 16 slots} named by the block table (K double-buffered,
 //            V one tile behind K);
 //   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
-//            K=head_dim, bf16 in, fp32 in TMEM), then O += P V (N=head_dim,
-//            K=64, V read MN-major straight from its page layout);
+//            K=head_dim, bf16 in, fp32 in TMEM), then O += P V with P read
+//            from TMEM (N=head_dim, K=64, V read MN-major straight from its
+//            page layout);
 //   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its S row,
 //            masks by select (causal bound, split bound), keeps a base-2
 //            online softmax with lazy rescaling of O in TMEM (only when the
-//            running max grows by more than 8), writes P as bf16 into the
-//            swizzled operand layout, and finally normalises O and stores the
+//            running max grows by more than 8), stores P as packed bf16 into
+//            one of two TMEM buffers (so the softmax of tile j+1 overlaps the
+//            PV product of tile j), and finally normalises O and stores the
 //            row (or a split partial with its log-sum-exp).
 // Tiles of a split that lie past every row's causal bound are never loaded.
 #include "pa_internal.h"
@@ -38,10 +40,11 @@ constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
 constexpr uint32_t kTmemCols = 256;
 constexpr uint32_t kTmemS = 0;     // S: columns [0, 64)
 constexpr uint32_t kTmemO = 64;    // O: columns [64, 64 + head_dim)
+constexpr uint32_t kTmemP = 192;   // P: two buffers of 32 columns (64 bf16 per row)
 
 enum Bar {
-  kQFull = 0, kQFree, kKFull0, kKFull1, kKFree0, kKFree1, kVFull, kVFree,
-  kSFull, kSFree, kPFull, kODone, kOFree, kNumBars
+  kQFull = 0, kQFree, kKFull0, kKFull1, kKFree0, kKFree1, kVFull0, kVFull1, kVFree0, kVFree1,
+  kSFull, kSFree, kPFull0, kPFull1, kODone0, kODone1, kOFree, kNumBars
 };
 
 template <int D>
@@ -50,12 +53,10 @@ struct TileCfg {
   static constexpr int Q_BYTES = NH * 128 * 128;    // 128 rows x 128 B per half
   static constexpr int KV_HALF = kBN * 128;         // one half of a K or V tile
   static constexpr int KV_BYTES = NH * KV_HALF;
-  static constexpr int P_BYTES = 128 * kBN * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
@@ -108,7 +109,6 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   uint8_t *sQ = smem + C::OFF_Q;
   uint8_t *sK = smem + C::OFF_K;
   uint8_t *sV = smem + C::OFF_V;
-  uint8_t *sP = smem + C::OFF_P;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *s_bad = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
@@ -123,8 +123,10 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     prefetch_tensor_map(&tm_q);
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
-    const int counts[kNumBars] = {1, 1, 1, 1, 1, 1, 1, 1, 1, 4, 4, 1, 4};
-    for (int b = 0; b < kNumBars; ++b) mbar_init(&bar[b], counts[b]);
+    for (int b = 0; b < kNumBars; ++b) {
+      const bool per_warp = b == kSFree || b == kPFull0 || b == kPFull1 || b == kOFree;
+      mbar_init(&bar[b], per_warp ? 4 : 1);
+    }
     fence_mbar_init();
   }
   if (warp == 5) tc_alloc(s_tmem, kTmemCols);
@@ -175,10 +177,11 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             if (lane == 0 && g >= kKStages)
               mbar_wait(&bar[kKFree0 + st], ((g / kKStages) - 1) & 1, dead, p.status);
           } else {
-            full = &bar[kVFull];
-            dst = sV;
+            const int st = g & 1;
+            full = &bar[kVFull0 + st];
+            dst = sV + st * C::KV_BYTES;
             map = &tm_v;
-            if (lane == 0 && g >= 1) mbar_wait(&bar[kVFree], (g - 1) & 1, dead, p.status);
+            if (lane == 0 && g >= 2) mbar_wait(&bar[kVFree0 + st], ((g >> 1) - 1) & 1, dead, p.status);
           }
           if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * C::NH * kBox * 128);
           __syncwarp();
@@ -195,7 +198,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t tiles = 0, items = 0;
-      const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV), sp = smem_u32(sP);
+      const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
       auto issue_s = [&](uint32_t g) {
         const int st = g % kKStages;
         mbar_wait(&bar[kKFull0 + st], (g / kKStages) & 1, dead, p.status);
@@ -220,18 +223,20 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         for (int j = 0; j < it.nt; ++j) {
           const uint32_t g = tiles + j;
           if (j + 1 < it.nt) issue_s(g + 1);
-          mbar_wait(&bar[kPFull], g & 1, dead, p.status);
-          mbar_wait(&bar[kVFull], g & 1, dead, p.status);
+          const int pb = g & 1;
+          mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, p.status);
+          mbar_wait(&bar[kVFull0 + pb], (g >> 1) & 1, dead, p.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
           tc_fence_after();
+          const uint32_t vb = sv + pb * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t a = umma_desc_sw128(sp + kk * 32, 16, 1024);
-            const uint64_t b = umma_desc_sw128(sv + kk * 16 * 128, C::KV_HALF, 1024);
-            tc_mma_bf16(tmem + kTmemO, a, b, C::IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            const uint64_t b = umma_desc_sw128(vb + kk * 16 * 128, C::KV_HALF, 1024);
+            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 32 + kk * 8, b, C::IDESC_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&bar[kVFree]);
-          tc_commit(&bar[kODone]);
+          tc_commit(&bar[kVFree0 + pb]);
+          tc_commit(&bar[kODone0 + pb]);
         }
         tc_commit(&bar[kQFree]);
         tiles += it.nt;
@@ -294,8 +299,9 @@ __global__ void __launch_bounds__(kTileThreads, 2)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kSFree]);
-        // P and O may be touched only after the previous PV product is done.
-        if (j > 0) mbar_wait(&bar[kODone], (g - 1) & 1, dead, p.status);
+        // P buffer g & 1 was last read by the PV product of tile g - 2.
+        const int pb = g & 1;
+        if (g >= 2) mbar_wait(&bar[kODone0 + pb], ((g >> 1) - 1) & 1, dead, p.status);
         tc_fence_after();
         if (warp_active) {
           // Only tiles that cross a row's bound need the select.
@@ -320,6 +326,9 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             rescale = j > 0;
           }
           if (__any_sync(0xffffffffu, rescale)) {
+            // O must hold the product of tile g - 1 before it is rescaled.
+            mbar_wait(&bar[kODone0 + (pb ^ 1)], ((g - 1) >> 1) & 1, dead, p.status);
+            tc_fence_after();
             const float a = rescale ? alpha : 1.f;
 #pragma unroll
             for (int c0 = 0; c0 < D; c0 += 32) {
@@ -335,43 +344,41 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           const float mu = m == -INFINITY ? 0.f : m;
           const float cs = fold ? c2 : 1.f;
           float sum = 0.f;
-          uint8_t *prow = sP + r * 128;
+          uint32_t pw[kBN / 2];
 #pragma unroll
-          for (int ch = 0; ch < kBN / 8; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const float p0 = fast_exp2(fmaf(s[ch * 8 + 2 * x], cs, -mu));
-              const float p1 = fast_exp2(fmaf(s[ch * 8 + 2 * x + 1], cs, -mu));
-              sum += p0 + p1;
-              const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-              w[x] = *reinterpret_cast<const uint32_t *>(&h2);
-            }
-            *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int x = 0; x < kBN / 2; ++x) {
+            const float p0 = fast_exp2(fmaf(s[2 * x], cs, -mu));
+            const float p1 = fast_exp2(fmaf(s[2 * x + 1], cs, -mu));
+            sum += p0 + p1;
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
           }
+          tc_st32(tmem + lane_off + kTmemP + pb * 32, pw);
+          tc_wait_st();
           l += sum;
         }
         if (j == it.nt - 1 && it.kv_hi - base < kBN) {
           // Rows past the tile's KV end may hold anything (NaN tails, stale
           // data); P is 0 there but 0 * NaN is NaN, so zero those V rows.
-          mbar_wait(&bar[kVFull], g & 1, dead, p.status);
+          mbar_wait(&bar[kVFull0 + pb], (g >> 1) & 1, dead, p.status);
           const int first = it.kv_hi - base;
           const int nchunks = (kBN - first) * 8 * C::NH;
+          uint8_t *vs = sV + pb * C::KV_BYTES;
           for (int e = r; e < nchunks; e += 128) {
             const int h = e / ((kBN - first) * 8);
             const int rem = e % ((kBN - first) * 8);
-            *reinterpret_cast<uint4 *>(sV + h * C::KV_HALF + (first + rem / 8) * 128 + (rem % 8) * 16) =
+            *reinterpret_cast<uint4 *>(vs + h * C::KV_HALF + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async();
         }
-        fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kPFull]);
+        if (lane == 0) mbar_arrive(&bar[kPFull0 + pb]);
       }
       // ---- epilogue: O / l -> output row or split partial
       const uint32_t glast = tiles + it.nt - 1;
-      mbar_wait(&bar[kODone], glast & 1, dead, p.status);
+      mbar_wait(&bar[kODone0 + (glast & 1)], (glast >> 1) & 1, dead, p.status);
       tc_fence_after();
       const bool write = row_valid && row_hi > it.kv_lo;
       const bool direct = ceil_div_ll(row_hi_full, it.split_len) == 1;
