@@ -96,6 +96,43 @@ __device__ inline int list_find(const long long *end, int n, long long idx) {
   return lo;
 }
 
+// Rolling cache of block-table entries for a producer warp: lane i holds
+// entry base + i of the current chunk and base + 32 + i of the next, so a
+// stream of page look-ups that only moves forward costs one coalesced load
+// per 32 pages, issued a chunk ahead, instead of a dependent load per tile.
+struct PageCache {
+  const int32_t *bt;
+  int limit;  // entries at or beyond `limit` read as -1
+  int base, cur, nxt;
+
+  __device__ void start(const int32_t *table, int lim, int first, int lane) {
+    bt = table;
+    limit = lim;
+    base = first;
+    cur = first + lane < lim ? __ldg(table + first + lane) : -1;
+    nxt = first + 32 + lane < lim ? __ldg(table + first + 32 + lane) : -1;
+  }
+
+  // All 32 lanes call; lp < 0 means this lane needs no page.  Needed pages
+  // must not move backwards between calls.
+  __device__ int get(int lp, int lane) {
+    int lo = __reduce_min_sync(0xffffffffu, lp < 0 ? 0x7fffffff : lp);
+    while (lo != 0x7fffffff && lo >= base + 32) {
+      base += 32;
+      cur = nxt;
+      const int n = base + 32 + lane;
+      nxt = n < limit ? __ldg(bt + n) : -1;
+    }
+    const int off = lp - base;
+    const int a = __shfl_sync(0xffffffffu, cur, off & 31);
+    const int b = __shfl_sync(0xffffffffu, nxt, off & 31);
+    if (lp < 0) return -1;
+    if (off >= 0 && off < 32) return a;
+    if (off >= 32 && off < 64) return b;
+    return lp < limit ? __ldg(bt + lp) : -1;  // far jump: read directly
+  }
+};
+
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
@@ -184,6 +221,22 @@ __device__ inline void tma_load_3d(void *dst, const CUtensorMap *map, int c0, in
       " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Bring a 4-D / 3-D TMA box into L2 without touching shared memory (deepens
+// the load pipeline beyond what the shared-memory ring can hold).
+__device__ inline void tma_prefetch_4d(const CUtensorMap *map, int c0, int c1, int c2, int c3) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+               : "memory");
+}
+
+__device__ inline void tma_prefetch_3d(const CUtensorMap *map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 __device__ inline void prefetch_tensor_map(const CUtensorMap *map) {
@@ -387,6 +440,17 @@ __device__ inline void tc_st32(uint32_t taddr, const uint32_t (&r)[32]) {
       : "memory");
 }
 
+// 16 consecutive 32-bit TMEM columns of this thread's lane (warp-wide).
+__device__ inline void tc_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15])
+      : "memory");
+}
+
 __device__ inline void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ inline void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
@@ -455,6 +519,18 @@ __device__ inline void mbar_wait_cluster(uint64_t *bar, uint32_t parity, bool &d
       return;
     }
   }
+}
+
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
+// another CTA of the cluster; completion is counted as transaction bytes on
+// the destination CTA's mbarrier.
+__device__ inline void bulk_copy_to_peer(uint32_t dst_cluster, const void *src, uint32_t bytes,
+                                         uint32_t mbar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst_cluster),
+      "r"(smem_u32(src)), "r"(bytes), "r"(mbar_cluster)
+      : "memory");
 }
 
 __device__ inline void cluster_sync_all() {

@@ -16,10 +16,12 @@
 // Each CTA loads only its own columns of every cached row (TMA, 128-byte
 // swizzled boxes of 64 columns x 32 slots), so the cache is read from HBM
 // exactly once and no FLOP is duplicated.  Per 32-position tile each CTA
-// forms its partial scores S_c = Q[:, own] K[:, own]^T in TMEM, sends them to
-// its peer through distributed shared memory, adds the peer's partial, runs
-// the same online softmax (base 2, lazy rescaling) and accumulates
-// O[:, own] += P V[:, own] (N = 256, V read MN-major from the staged rows).
+// forms its partial scores S_c = Q[:, own] K[:, own]^T in TMEM, stages them in
+// its own shared memory and pushes them to its peer with one bulk DSMEM copy
+// (completion counted on the peer's mbarrier), adds the peer's partial, runs
+// the same online softmax (base 2, lazy rescaling), stores P as packed bf16
+// in TMEM and accumulates O[:, own] += P V[:, own] (N = 256, P read from TMEM,
+// V read MN-major from the staged rows).
 // Splits of a long context are merged by log-sum-exp in a second kernel.
 #include "pa_internal.h"
 
@@ -38,21 +40,21 @@ constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O: columns [0, 256)
 constexpr uint32_t kTmemS = 256;    // S: two buffers of 32 columns
+constexpr uint32_t kTmemP = 320;    // P: two buffers of 16 columns (32 bf16 per row)
 constexpr int kMinSplit = 512;
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + kMaxChunks * kChunkQ;
 constexpr int STAGE_BYTES = kMaxChunks * kChunkKV;
-constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;
-constexpr int X_BYTES = 128 * kMN * 4;
-constexpr int OFF_P = OFF_X + 2 * X_BYTES;
-constexpr int P_BYTES = 128 * 128;
-constexpr int OFF_BAR = OFF_P + P_BYTES;
+constexpr int X_BYTES = 128 * kMN * 4;               // one tile of partial scores
+constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;  // peer's partials, 2 buffers
+constexpr int OFF_XS = OFF_X + 2 * X_BYTES;               // own partials staged, 2 buffers
+constexpr int OFF_BAR = OFF_XS + 2 * X_BYTES;
 
 enum MBar {
   kQFull = 0, kQFree, kKVFull0, kKVFree0 = kKVFull0 + kMlaStages, kSFull0 = kKVFree0 + kMlaStages,
-  kSFree0 = kSFull0 + 2, kXFull0 = kSFree0 + 2, kXFree0 = kXFull0 + 2, kPFull = kXFree0 + 2,
-  kODone, kOFree, kNumMBars
+  kSFree0 = kSFull0 + 2, kXFull0 = kSFree0 + 2, kXFree0 = kXFull0 + 2, kPFull0 = kXFree0 + 2,
+  kODone0 = kPFull0 + 2, kOFree = kODone0 + 2, kNumMBars
 };
 constexpr int OFF_MISC = OFF_BAR + kNumMBars * 8;
 constexpr int MLA_SMEM = OFF_MISC + 64 + 1024;
@@ -141,7 +143,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   uint8_t *sQ = smem + OFF_Q;
   uint8_t *sKV = smem + OFF_KV;
   uint8_t *sX = smem + OFF_X;
-  uint8_t *sP = smem + OFF_P;
+  uint8_t *sXS = smem + OFF_XS;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   int *s_bad = reinterpret_cast<int *>(smem + OFF_MISC + 16);
@@ -158,10 +160,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     prefetch_tensor_map(&tm_q);
     prefetch_tensor_map(&tm_kv);
     for (int b = 0; b < kNumMBars; ++b) {
-      uint32_t cnt = 1;
-      if (b == kSFree0 || b == kSFree0 + 1 || b == kPFull || b == kOFree) cnt = 4;
-      if (b == kXFull0 || b == kXFull0 + 1 || b == kXFree0 || b == kXFree0 + 1) cnt = 128;
-      mbar_init(&bar[b], cnt);
+      const bool per_warp = b == kSFree0 || b == kSFree0 + 1 || b == kPFull0 ||
+                            b == kPFull0 + 1 || b == kOFree;
+      mbar_init(&bar[b], per_warp ? 4u : 1u);
     }
     fence_mbar_init();
   }
@@ -182,43 +183,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------- producer
-    if (lane == 0) {
-      uint32_t tiles = 0, items = 0;
-      for (long long item = cluster; item < n_items; item += nclusters) {
-        int s, split, kv_lo, kv_hi;
-        decode(item, s, split, kv_lo, kv_hi);
-        const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
+    // The whole warp walks the items (the page cache is warp-wide); lane 0
+    // waits on the barriers and issues the copies.
+    uint32_t tiles = 0, items = 0;
+    for (long long item = cluster; item < n_items; item += nclusters) {
+      int s, split, kv_lo, kv_hi;
+      decode(item, s, split, kv_lo, kv_hi);
+      const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
+      if (lane == 0) {
         if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, a.status);
         mbar_arrive_expect_tx(&bar[kQFull], nch * kChunkQ);
         for (int i = 0; i < nch; ++i)
           tma_load_3d(sQ + i * kChunkQ, &tm_q, chunk_of(rank, i) * 64, 0, s, &bar[kQFull]);
-        const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
-        for (int j = 0; j < nt; ++j) {
-          const uint32_t g = tiles + j;
-          const int st = g % kMlaStages;
+      }
+      const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
+      PageCache pc;
+      pc.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
+      for (int j = 0; j < nt; ++j) {
+        const uint32_t g = tiles + j;
+        const int st = g % kMlaStages;
+        const int pos = kv_lo + j * kMN;
+        const int page = pc.get(pos / bs, lane);
+        const bool ok = page >= 0 && page < a.num_blocks;
+        if (lane == 0) {
+          if (!ok) atomicOr(a.status, PA_DEV_BAD_BLOCK);
           if (g >= kMlaStages)
             mbar_wait(&bar[kKVFree0 + st], ((g / kMlaStages) - 1) & 1, dead, a.status);
-          const int pos = kv_lo + j * kMN;
-          const int lp = pos / bs;
-          const int page = lp < a.max_blocks_per_seq ? __ldg(bt + lp) : -1;
-          const bool ok = page >= 0 && page < a.num_blocks;
-          if (!ok) atomicOr(a.status, PA_DEV_BAD_BLOCK);
           mbar_arrive_expect_tx(&bar[kKVFull0 + st], ok ? nch * kChunkKV : 0);
           if (ok)
             for (int i = 0; i < nch; ++i)
               tma_load_3d(sKV + st * STAGE_BYTES + i * kChunkKV, &tm_kv, chunk_of(rank, i) * 64,
                           pos % bs, page, &bar[kKVFull0 + st]);
         }
-        tiles += nt;
-        ++items;
+        __syncwarp();
       }
+      tiles += nt;
+      ++items;
     }
-    __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t tiles = 0, items = 0;
-      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV), sp = smem_u32(sP);
+      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
       auto issue_s = [&](uint32_t g) {
         const int st = g % kMlaStages, b = g & 1;
         mbar_wait(&bar[kKVFull0 + st], (g / kMlaStages) & 1, dead, a.status);
@@ -243,18 +249,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         for (int j = 0; j < nt; ++j) {
           const uint32_t g = tiles + j;
           if (j + 1 < nt) issue_s(g + 1);
-          mbar_wait(&bar[kPFull], g & 1, dead, a.status);
+          const int pb = g & 1;
+          mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, a.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, a.status);
           tc_fence_after();
           const uint32_t vb = skv + (g % kMlaStages) * STAGE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kMN / 16; ++kk) {
-            const uint64_t ad = umma_desc_sw128(sp + kk * 32, 16, 1024);
             const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, kChunkKV, 1024);
-            tc_mma_bf16(tmem + kTmemO, ad, bd, IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 16 + kk * 8, bd, IDESC_PV,
+                           (j > 0 || kk > 0) ? 1u : 0u);
           }
           tc_commit(&bar[kKVFree0 + g % kMlaStages]);
-          tc_commit(&bar[kODone]);
+          tc_commit(&bar[kODone0 + pb]);
         }
         tc_commit(&bar[kQFree]);
         tiles += nt;
@@ -268,7 +275,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint32_t x_peer[2], xfull_peer[2], xfree_peer[2];
     for (int b = 0; b < 2; ++b) {
-      x_peer[b] = cluster_map(smem_u32(sX + b * X_BYTES + r * kMN * 4), peer);
+      x_peer[b] = cluster_map(smem_u32(sX + b * X_BYTES), peer);
       xfull_peer[b] = cluster_map(smem_u32(&bar[kXFull0 + b]), peer);
       xfree_peer[b] = cluster_map(smem_u32(&bar[kXFree0 + b]), peer);
     }
@@ -305,14 +312,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&bar[kSFree0 + b]);
-        // partial scores to the peer, then the peer's partial from our buffer
+        // stage the partial scores, then one bulk copy to the peer: the staging
+        // and the peer's buffer b are free once the peer has consumed tile g - 2
         if (g >= 2) mbar_wait_cluster(&bar[kXFree0 + b], ((g >> 1) - 1) & 1, dead, a.status);
+        float4 *st4 = reinterpret_cast<float4 *>(sXS + b * X_BYTES + r * kMN * 4);
 #pragma unroll
         for (int v = 0; v < kMN / 4; ++v)
-          st_cluster_v4(x_peer[b] + 16 * v, __uint_as_float(raw[4 * v]),
-                        __uint_as_float(raw[4 * v + 1]), __uint_as_float(raw[4 * v + 2]),
-                        __uint_as_float(raw[4 * v + 3]));
-        mbar_arrive_remote(xfull_peer[b]);
+          st4[v] = make_float4(__uint_as_float(raw[4 * v]), __uint_as_float(raw[4 * v + 1]),
+                               __uint_as_float(raw[4 * v + 2]), __uint_as_float(raw[4 * v + 3]));
+        fence_proxy_async();
+        named_sync(1, 128);
+        if (r == 0) {
+          mbar_arrive_expect_tx(&bar[kXFull0 + b], X_BYTES);  // the peer's tile g lands here
+          bulk_copy_to_peer(x_peer[b], sXS + b * X_BYTES, X_BYTES, xfull_peer[b]);
+        }
         mbar_wait_cluster(&bar[kXFull0 + b], (g >> 1) & 1, dead, a.status);
         float sc[kMN];
         const float4 *xr = reinterpret_cast<const float4 *>(sX + b * X_BYTES + r * kMN * 4);
@@ -324,14 +337,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           sc[4 * v + 2] = __uint_as_float(raw[4 * v + 2]) + o4.z;
           sc[4 * v + 3] = __uint_as_float(raw[4 * v + 3]) + o4.w;
         }
-        mbar_arrive_remote(xfree_peer[b]);
-        float mx = -INFINITY;
+        named_sync(1, 128);
+        if (r == 0) mbar_arrive_remote(xfree_peer[b]);
+        float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kMN; ++c) {
           sc[c] = (base + c < kv_hi) ? sc[c] * a.scale_log2 : -INFINITY;
-          mx = fmaxf(mx, sc[c]);
+          mxa[c & 3] = fmaxf(mxa[c & 3], sc[c]);
         }
-        if (j > 0) mbar_wait(&bar[kODone], (g - 1) & 1, dead, a.status);
+        const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        // P buffer b was last read by the PV product of tile g - 2
+        if (g >= 2) mbar_wait(&bar[kODone0 + b], ((g >> 1) - 1) & 1, dead, a.status);
         tc_fence_after();
         float alpha = 1.f;
         bool rescale = false;
@@ -342,6 +358,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           rescale = j > 0;
         }
         if (__any_sync(0xffffffffu, rescale)) {
+          mbar_wait(&bar[kODone0 + (b ^ 1)], ((g - 1) >> 1) & 1, dead, a.status);
+          tc_fence_after();
           const float al = rescale ? alpha : 1.f;
           for (int c0 = 0; c0 < kVHalf; c0 += 32) {
             uint32_t o[32];
@@ -354,22 +372,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           tc_wait_st();
         }
         const float mu = m == -INFINITY ? 0.f : m;
-        float sum = 0.f;
-        uint8_t *prow = sP + r * 128;
+        float suma[4] = {0.f, 0.f, 0.f, 0.f};
+        uint32_t pw[kMN / 2];
 #pragma unroll
-        for (int ch = 0; ch < kMN / 8; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int x = 0; x < 4; ++x) {
-            const float p0 = fast_exp2(sc[ch * 8 + 2 * x] - mu);
-            const float p1 = fast_exp2(sc[ch * 8 + 2 * x + 1] - mu);
-            sum += p0 + p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            w[x] = *reinterpret_cast<const uint32_t *>(&h2);
-          }
-          *reinterpret_cast<uint4 *>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int x = 0; x < kMN / 2; ++x) {
+          const float p0 = fast_exp2(sc[2 * x] - mu);
+          const float p1 = fast_exp2(sc[2 * x + 1] - mu);
+          suma[x & 3] += p0 + p1;
+          const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+          pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
         }
-        l += sum;
+        tc_st16(tmem + lane_off + kTmemP + b * 16, pw);
+        tc_wait_st();
+        l += (suma[0] + suma[1]) + (suma[2] + suma[3]);
         if (j == nt - 1 && kv_hi - base < kMN) {
           // slots past the sequence end may hold anything; 0 * NaN is NaN
           mbar_wait(&bar[kKVFull0 + g % kMlaStages], (g / kMlaStages) & 1, dead, a.status);
@@ -381,15 +396,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
             *reinterpret_cast<uint4 *>(vb + ci * kChunkKV + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
           }
+          fence_proxy_async();
         }
-        fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kPFull]);
+        if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
       }
       // ---- epilogue
       const uint32_t glast = tiles + nt - 1;
-      mbar_wait(&bar[kODone], glast & 1, dead, a.status);
+      mbar_wait(&bar[kODone0 + (glast & 1)], (glast >> 1) & 1, dead, a.status);
       tc_fence_after();
       const int ns = a.nsplit[s];
       const bool direct = ns == 1;

@@ -252,6 +252,7 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
           tma_load_4d(kb, &tm_k, 0, kvh, pos % bs, page, &full[b]);
           tma_load_4d(kb + C::HALF_STAGE, &tm_v, 0, kvh, pos % bs, page, &full[b]);
         }
+
       }
     }
     return;

@@ -143,6 +143,9 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       TileItem it;
       if (!decode_tile_item(p, item, G, it)) continue;
       const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
+      PageCache kc, vc;  // one per stream: each only moves forward
+      kc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
+      vc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
       if (lane == 0) {
         if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
         mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
@@ -158,11 +161,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           const uint32_t g = tiles + jj;
           const int pos = it.kv_lo + jj * kBN + lane * kBox;
           const bool need = lane < kBN / kBox && pos < it.kv_hi;
-          int page = -1;
-          if (need) {
-            const int lp = pos / bs;
-            page = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
-          }
+          const int page = (which == 0 ? kc : vc).get(need ? pos / bs : -1, lane);
           const bool ok = need && page >= 0 && page < p.num_blocks;
           if (need && !ok) atomicOr(p.status, PA_DEV_BAD_BLOCK);
           const unsigned mask = __ballot_sync(0xffffffffu, ok);
@@ -189,6 +188,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             for (int h = 0; h < C::NH; ++h)
               tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh, pos % bs,
                           page, full);
+
         }
       }
       tiles += it.nt;
@@ -313,9 +313,14 @@ __global__ void __launch_bounds__(kTileThreads, 2)
 #pragma unroll
             for (int c = 0; c < kBN; ++c) s[c] *= c2;
           }
-          float mx = -INFINITY;
+          // row max with 8 independent chains (a single chain is 64 deep)
+          float mxa[8];
 #pragma unroll
-          for (int c = 0; c < kBN; ++c) mx = fmaxf(mx, s[c]);
+          for (int x = 0; x < 8; ++x) mxa[x] = s[x];
+#pragma unroll
+          for (int c = 8; c < kBN; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], s[c]);
+          float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
           if (fold && mx != -INFINITY) mx *= c2;
           float alpha = 1.f;
           bool rescale = false;
@@ -343,19 +348,19 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           }
           const float mu = m == -INFINITY ? 0.f : m;
           const float cs = fold ? c2 : 1.f;
-          float sum = 0.f;
+          float suma[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           uint32_t pw[kBN / 2];
 #pragma unroll
           for (int x = 0; x < kBN / 2; ++x) {
             const float p0 = fast_exp2(fmaf(s[2 * x], cs, -mu));
             const float p1 = fast_exp2(fmaf(s[2 * x + 1], cs, -mu));
-            sum += p0 + p1;
+            suma[x & 7] += p0 + p1;
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
           }
           tc_st32(tmem + lane_off + kTmemP + pb * 32, pw);
           tc_wait_st();
-          l += sum;
+          l += ((suma[0] + suma[1]) + (suma[2] + suma[3])) + ((suma[4] + suma[5]) + (suma[6] + suma[7]));
         }
         if (j == it.nt - 1 && it.kv_hi - base < kBN) {
           // Rows past the tile's KV end may hold anything (NaN tails, stale
