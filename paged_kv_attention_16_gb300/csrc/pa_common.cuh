@@ -250,6 +250,19 @@ __device__ inline float fast_exp2(float x) {
   return y;
 }
 
+// Packed two-lane fp32 FMA (one instruction, two IEEE fma results):
+// returns {a0 * b0 + c0, a1 * b1 + c1}.
+__device__ inline void ffma2(float &c0, float &c1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%0, %1};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // bf16x2 packed in a 32-bit word -> two floats (bf16 is the top half of fp32).
 __device__ inline float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ inline float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

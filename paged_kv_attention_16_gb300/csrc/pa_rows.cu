@@ -329,10 +329,11 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
           float part[C::HPT];
 #pragma unroll
           for (int h = 0; h < C::HPT; ++h) {
-            float acc = 0.f;
+            float a0 = 0.f, a1 = 0.f;  // even / odd dims, two-lane packed FMA
 #pragma unroll
-            for (int x = 0; x < C::DPT; ++x) acc = fmaf(qv[h][x], kf[x], acc);
-            part[h] = acc;
+            for (int x = 0; x < C::DPT; x += 2)
+              ffma2(a0, a1, qv[h][x], qv[h][x + 1], kf[x], kf[x + 1]);
+            part[h] = a0 + a1;
           }
           reduce_scores<C::HPT, C::LPT, C::LOG2_HPT>(part, sc[nb], lane, c);
         }
@@ -364,7 +365,7 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
             const float pr = fast_exp2(sc[nb][h] - m[h]);
             l[h] += pr;
 #pragma unroll
-            for (int x = 0; x < C::DPT; ++x) o[h][x] = fmaf(pr, vf[x], o[h][x]);
+            for (int x = 0; x < C::DPT; x += 2) ffma2(o[h][x], o[h][x + 1], pr, pr, vf[x], vf[x + 1]);
           }
         }
       }
