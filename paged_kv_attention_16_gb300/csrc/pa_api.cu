@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x;
   const int Hk = p.num_kv_heads, G = p.num_heads / p.num_kv_heads, H = p.num_heads;
   const bool cached = S <= kPlanCache;
+  pdl_trigger();  // the row kernel may start its prologue meanwhile
   auto raw = [&](int s) -> int4 {
     if (cached) return s_req[s];
     return make_int4(p.qsl[s], p.qsl[s + 1], p.seq_lens[s], 0);
@@ -248,6 +249,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   const int S = p.num_seqs, H = p.num_heads, D = p.head_dim;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = kMergeThreads / 32;
+  pdl_wait();
   T *out = reinterpret_cast<T *>(p.out);
   const long long gw = ((long long)blockIdx.x * blockDim.x + tid) >> 5;
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -705,12 +707,14 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     }
   }
   slot = timed ? prof_begin(PA_K_MERGE, st) : -1;
-  if (c.dtype == PA_BF16)
-    merge_kernel<__nv_bfloat16><<<num_sms * 4, kMergeThreads, 0, st>>>(p);
-  else
-    merge_kernel<float><<<num_sms * 4, kMergeThreads, 0, st>>>(p);
+  const cudaError_t merge_err =
+      c.dtype == PA_BF16
+          ? launch_dependent(merge_kernel<__nv_bfloat16>, dim3(num_sms * 4), dim3(kMergeThreads),
+                             0, st, p)
+          : launch_dependent(merge_kernel<float>, dim3(num_sms * 4), dim3(kMergeThreads), 0, st,
+                             p);
   prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (merge_err != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 

@@ -468,6 +468,15 @@ __device__ inline void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligne
 __device__ inline void tc_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // Named barrier over `count` threads (ids 1..15; 0 is __syncthreads).
+// Programmatic dependent launch.  A kernel launched with programmatic stream
+// serialization may start (and run its prologue) while the kernel before it
+// in the stream is still finishing; pdl_wait() blocks until that kernel has
+// completed and its writes are visible, so it must precede every access to
+// data the earlier kernels produce.  pdl_trigger() lets the next kernel start
+// launching early; the next kernel still waits for this one to complete.
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ inline void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ inline void named_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }

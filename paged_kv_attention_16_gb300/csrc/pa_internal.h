@@ -6,6 +6,25 @@
 
 namespace pa {
 
+// Launches `kernel` with programmatic stream serialization: its CTAs may be
+// scheduled while the previous kernel of the stream drains.  The kernel must
+// call pdl_wait() before it reads anything earlier kernels wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Kernel timing: prof_begin records a start event when timing is on and the
 // stream is not capturing (returns -1 otherwise); prof_end records the end.
 int prof_begin(int kernel_id, cudaStream_t stream);

@@ -89,6 +89,7 @@ __device__ inline int chunk_of(uint32_t rank, int i) {
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const MlaArgs a) {
   __shared__ long long scratch[33];
   const int S = a.num_seqs, tid = threadIdx.x;
+  pdl_trigger();  // the decode kernel may start its prologue meanwhile
   long long tot = 0;
   int bad = 0;
   for (int s = tid; s < S; s += 1024) {
@@ -152,6 +153,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t rank = cluster_ctarank(), peer = rank ^ 1u;
   const int nch = rank == 0 ? 5 : 4;
   const long long cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+  pdl_trigger();
+  pdl_wait();  // the plan
   const long long n_items = a.plan[0];
   const int L = (int)a.plan[1];
   const int S = a.num_seqs, bs = a.block_size;
@@ -464,6 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaArgs a) {
   const int tid = threadIdx.x;
   const long long rows = (long long)a.num_seqs * kMlaH;
+  pdl_wait();  // the split partials
   __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out);
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
     const int s = (int)(row / kMlaH);
@@ -628,13 +632,14 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
   prof_end(slot, st);
   if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA, st);
-  mla_kernel<<<2 * a.num_clusters, kMlaThreads, MLA_SMEM, st>>>(tm_q, tm_kv, a);
+  cudaError_t err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads),
+                                     MLA_SMEM, st, tm_q, tm_kv, a);
   prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA_MERGE, st);
-  mla_merge_kernel<<<num_sms * 4, 256, 0, st>>>(a);
+  err = launch_dependent(mla_merge_kernel, dim3(num_sms * 4), dim3(256), 0, st, a);
   prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (err != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;
 }
 

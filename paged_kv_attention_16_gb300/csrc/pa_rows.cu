@@ -172,6 +172,8 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
     fence_mbar_init();
   }
   __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the plan
   bool dead = false;
 
   if (warp == C::NWARP) {
@@ -453,8 +455,8 @@ cudaError_t launch_one(const FwdParams &p, const CUtensorMap &tk, const CUtensor
   err = cudaFuncSetAttribute(row_kernel<T, D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
   if (err != cudaSuccess) return err;
-  row_kernel<T, D, G><<<grid, C::NTHREADS, C::SMEM, stream>>>(tk, tv, p);
-  return cudaGetLastError();
+  return launch_dependent(row_kernel<T, D, G>, dim3(grid), dim3(C::NTHREADS), C::SMEM, stream,
+                          tk, tv, p);
 }
 
 template <typename T, int D, int G>

@@ -116,6 +116,8 @@ __global__ void __launch_bounds__(kTileThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.num_heads / p.num_kv_heads;
   const int H = p.num_heads, bs = p.block_size;
+  pdl_trigger();
+  pdl_wait();  // the plan, and the row kernel before us in the stream
   const long long n_items = p.plan->n[kListTile];
   if (n_items == 0) return;  // no extend / prefill rows in this batch
 
@@ -451,8 +453,8 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
   e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  tile_kernel<D><<<num_sms * 2, kTileThreads, C::SMEM, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  return launch_dependent(tile_kernel<D>, dim3(num_sms * 2), dim3(kTileThreads), C::SMEM,
+                          stream, tq, tk, tv, p);
 }
 
 }  // namespace
