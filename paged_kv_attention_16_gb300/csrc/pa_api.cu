@@ -60,12 +60,18 @@ constexpr int kPlanCache = kPlanThreads;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   __shared__ long long scratch[5 * 33];
+  __shared__ int s_max_merge_splits;
   __shared__ int4 s_req[kPlanCache];  // q_start, q_end, ctx, -
   __shared__ int s_ord[kPlanCache];
   const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x;
   const int Hk = p.num_kv_heads, G = p.num_heads / p.num_kv_heads, H = p.num_heads;
   const bool cached = S <= kPlanCache;
+  // Launched programmatically after whatever preceded this call in the
+  // stream: wait for it (it may have written the metadata, or still read
+  // this workspace) before touching memory.
+  pdl_wait();
   pdl_trigger();  // the row kernel may start its prologue meanwhile
+  if (tid == 0) s_max_merge_splits = 0;
   auto raw = [&](int s) -> int4 {
     if (cached) return s_req[s];
     return make_int4(p.qsl[s], p.qsl[s + 1], p.seq_lens[s], 0);
@@ -173,6 +179,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
         if (row_path) cnt[kListRow] = (long long)Hk * r.q_len * nsplit;
         else cnt[kListTile] = (long long)Hk * ceil_div_ll((long long)r.q_len * G, kTileRows) * nsplit;
         if (nsplit > 1) {
+          atomicMax(&s_max_merge_splits, nsplit);
           cnt[kListMerge] = (long long)r.q_len * H;
           cnt[kNumLists] = (long long)r.q_len * H * nsplit;
         }
@@ -200,6 +207,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     for (int x = 0; x < 8; ++x) p.plan->counter[x] = 0;
     p.plan->qsl_bad = zero_all ? 1 : 0;
     p.plan->split_len_decode = L;
+    p.plan->max_merge_splits = s_max_merge_splits;
     p.plan->partial_rows = run_part;
   }
 }
@@ -220,15 +228,20 @@ __device__ inline void store_out<__nv_bfloat16>(__nv_bfloat16 *dst, float v) {
 // Rows with at most kWarpMergeSplits non-empty splits are merged by one warp
 // (lanes over head_dim); longer rows by a whole block (warps over splits).
 constexpr int kWarpMergeSplits = 8;
+// Merge-list prefix sums kept in shared memory for batches up to this size.
+constexpr int kMergeCache = 1024;
 
 struct MergeRow {
   long long tok, base;
   int h, nn;
 };
 
-__device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, long long row) {
+// mend: the merge list's ends, in global memory or (shared = true) in a
+// shared-memory copy.
+__device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, bool shared,
+                                     long long row) {
   const int S = p.num_seqs, H = p.num_heads;
-  const int k = list_find(mend, S, row);
+  const int k = shared ? list_find_shared(mend, S, row) : list_find(mend, S, row);
   const long long local = row - (k ? mend[k - 1] : 0);
   const ReqInfo r = p.req[p.ord[k]];
   const int i = (int)(local / H);
@@ -249,6 +262,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   const int S = p.num_seqs, H = p.num_heads, D = p.head_dim;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int NW = kMergeThreads / 32;
+  pdl_trigger();  // the next call's planner may get its CTA in place
   pdl_wait();
   T *out = reinterpret_cast<T *>(p.out);
   const long long gw = ((long long)blockIdx.x * blockDim.x + tid) >> 5;
@@ -275,13 +289,22 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
     }
   }
 
-  const long long *mend = p.list_end + (size_t)kListMerge * S;
   const long long nm = p.plan->n[kListMerge];
+  if (nm == 0) return;
+  // the merge list's per-request ends, searched once per row
+  __shared__ long long s_mend[kMergeCache];
+  const long long *mend = p.list_end + (size_t)kListMerge * S;
+  const bool mend_shared = S <= kMergeCache;
+  if (mend_shared) {
+    for (int k = tid; k < S; k += kMergeThreads) s_mend[k] = mend[k];
+    __syncthreads();
+    mend = s_mend;
+  }
   const int dpl = D / 32;  // dims per lane: 2 or 4
 
   // ---- short rows: one warp each ---------------------------------------------
   for (long long row = gw; row < nm; row += nw) {
-    const MergeRow mr = merge_row(p, mend, row);
+    const MergeRow mr = merge_row(p, mend, mend_shared, row);
     if (mr.nn <= 1 || mr.nn > kWarpMergeSplits) continue;
     const float lse = lane < mr.nn ? p.part_lse[mr.base + lane] : -INFINITY;
     int bad = isnan(lse) ? 1 : 0;
@@ -317,8 +340,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   }
 
   // ---- long rows: one block each, warps over splits ---------------------------
+  if (p.plan->max_merge_splits <= kWarpMergeSplits) return;
   for (long long row = blockIdx.x; row < nm; row += gridDim.x) {
-    const MergeRow mr = merge_row(p, mend, row);
+    const MergeRow mr = merge_row(p, mend, mend_shared, row);
     if (mr.nn <= kWarpMergeSplits) continue;  // uniform per block
     float M = -INFINITY;
     int bad = 0;
@@ -666,9 +690,9 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.status = status;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
-  plan_kernel<<<1, kPlanThreads, 0, st>>>(p);
+  const cudaError_t plan_err = launch_dependent(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, p);
   prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (plan_err != cudaSuccess) return PA_ERR_CUDA;
 
   if (c.num_seqs > 0) {
     CUtensorMap tm_k, tm_v;

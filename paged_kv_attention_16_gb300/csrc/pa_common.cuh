@@ -45,6 +45,7 @@ struct PlanHeader {
   unsigned long long counter[8];  // dynamic work counters, reset by the planner
   int qsl_bad;                  // query_start_loc failed its checks
   int split_len_decode;         // chosen decode split length
+  int max_merge_splits;         // largest nsplit among requests with merge rows
   long long partial_rows;       // partial rows the plan uses
 };
 
@@ -92,6 +93,16 @@ __device__ inline int list_find(const long long *end, int n, long long idx) {
   while (lo < hi) {
     int mid = (lo + hi) >> 1;
     if (__ldg(end + mid) > idx) hi = mid; else lo = mid + 1;
+  }
+  return lo;
+}
+
+// list_find over a copy in shared memory (plain loads: __ldg is global-only).
+__device__ inline int list_find_shared(const long long *end, int n, long long idx) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (end[mid] > idx) hi = mid; else lo = mid + 1;
   }
   return lo;
 }

@@ -89,6 +89,7 @@ __device__ inline int chunk_of(uint32_t rank, int i) {
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const MlaArgs a) {
   __shared__ long long scratch[33];
   const int S = a.num_seqs, tid = threadIdx.x;
+  pdl_wait();     // whatever preceded this call in the stream
   pdl_trigger();  // the decode kernel may start its prologue meanwhile
   long long tot = 0;
   int bad = 0;
@@ -467,6 +468,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 __global__ void __launch_bounds__(256) mla_merge_kernel(const MlaArgs a) {
   const int tid = threadIdx.x;
   const long long rows = (long long)a.num_seqs * kMlaH;
+  pdl_trigger();
   pdl_wait();  // the split partials
   __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out);
   for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -628,11 +630,11 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
     return PA_ERR_CUDA;
 
   int slot = prof_begin(PA_K_PLAN, st);
-  mla_plan_kernel<<<1, 1024, 0, st>>>(a);
+  cudaError_t err = launch_dependent(mla_plan_kernel, dim3(1), dim3(1024), 0, st, a);
   prof_end(slot, st);
-  if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+  if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA, st);
-  cudaError_t err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads),
+  err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads),
                                      MLA_SMEM, st, tm_q, tm_kv, a);
   prof_end(slot, st);
   if (err != cudaSuccess) return PA_ERR_CUDA;
