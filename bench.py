@@ -36,6 +36,12 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_attention_16_gb300 import inputs  # noqa: E402
 
+# DRAM bytes (read + write) of one row_kernel<bf16,128,4> launch on this
+# workload, from the ncu capture summarised in
+# profiles/row_kernel_llama_decode_b64.md.  Set to None whenever the row
+# kernel changes until it is captured again.
+ROW_KERNEL_TRAFFIC = 1_194_445_000 + 15_643_648
+
 METRIC = "decode KV GB/s (% of HBM peak); mixed-batch attention TFLOPS (% of peak)"
 WORKLOAD = ("llama-3.1-8b-shaped GQA decode: batch 64, ctx uniform [500, 8192], 32 q heads, "
             "8 kv heads, head_dim 128, block_size 16, bf16, random page placement")
@@ -415,7 +421,8 @@ def run_ours(args):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "hbm_frac": value / hbm,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm, "traffic": ROW_KERNEL_TRAFFIC,
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "kernel": "row_kernel<bf16,128,4> (decode row streaming)",
                      "kernel_ms": row_avg, "bytes_per_launch": step_kv + step_io,
                      "kernel_timing": "CUDA events around each launch, second pass of the "
