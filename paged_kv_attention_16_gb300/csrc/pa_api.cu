@@ -609,7 +609,9 @@ int row_ctas_per_sm_cached(int dtype, int head_dim, int group) {
   std::lock_guard<std::mutex> lock(mu);
   if (dev < 0 || dev >= 64) return 1;
   if (!have[dev][a][b][c]) {
-    cache[dev][a][b][c] = row_kernel_ctas_per_sm(dtype, head_dim, group);
+    cache[dev][a][b][c] = row_mma_supported(dtype, head_dim, group)
+                              ? row_mma_ctas_per_sm(head_dim, group)
+                              : row_kernel_ctas_per_sm(dtype, head_dim, group);
     have[dev][a][b][c] = true;
   }
   return cache[dev][a][b][c] > 0 ? cache[dev][a][b][c] : 1;
@@ -695,20 +697,38 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   if (plan_err != cudaSuccess) return PA_ERR_CUDA;
 
   if (c.num_seqs > 0) {
-    CUtensorMap tm_k, tm_v;
-    if (!encode_cache_map(&tm_k, c.k_cache, c.dtype, c.num_blocks, c.block_size, c.num_kv_heads,
-                          c.head_dim, c.head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_cache_map(&tm_v, c.v_cache, c.dtype, c.num_blocks, c.block_size, c.num_kv_heads,
-                          c.head_dim, c.head_dim, 16, CU_TENSOR_MAP_SWIZZLE_NONE))
+    const bool mma_rows = row_mma_supported(c.dtype, c.head_dim, group);
+    // K/V pages as 64-element (128-byte) swizzled boxes of 16 slots: the
+    // bf16 row kernel and the tile kernel read them with ldmatrix / UMMA.
+    CUtensorMap tm_kt, tm_vt;
+    if ((mma_rows || tile_ok) &&
+        (!encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
+                           c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
+         !encode_cache_map(&tm_vt, c.v_cache, c.dtype, c.num_blocks, c.block_size,
+                           c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B)))
       return PA_ERR_CUDA;
+    cudaError_t row_err;
     slot = timed ? prof_begin(PA_K_ROW, st) : -1;
-    const cudaError_t row_err = launch_row_kernel(p, tm_k, tm_v, row_ctas, st);
+    if (mma_rows) {
+      row_err = launch_row_mma_kernel(p, tm_kt, tm_vt, row_ctas, st);
+    } else {
+      // fp32: whole rows of head_dim elements, no swizzle (CUDA-core kernel)
+      CUtensorMap tm_k, tm_v;
+      if (!encode_cache_map(&tm_k, c.k_cache, c.dtype, c.num_blocks, c.block_size,
+                            c.num_kv_heads, c.head_dim, c.head_dim, 16,
+                            CU_TENSOR_MAP_SWIZZLE_NONE) ||
+          !encode_cache_map(&tm_v, c.v_cache, c.dtype, c.num_blocks, c.block_size,
+                            c.num_kv_heads, c.head_dim, c.head_dim, 16,
+                            CU_TENSOR_MAP_SWIZZLE_NONE))
+        return PA_ERR_CUDA;
+      row_err = launch_row_kernel(p, tm_k, tm_v, row_ctas, st);
+    }
     prof_end(slot, st);
     if (row_err != cudaSuccess) return PA_ERR_CUDA;
     if (tile_ok) {
-      CUtensorMap tm_q, tm_kt, tm_vt;
       // Q as [tokens, heads, dim] with 64-element (128-byte) swizzled boxes of
-      // G heads x (128 / G) tokens; K/V pages as 64-element swizzled boxes.
+      // G heads x (128 / G) tokens.
+      CUtensorMap tm_q;
       EncodeTiledFn fn = encode_fn();
       cuuint64_t qd[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_heads,
                           (cuuint64_t)c.num_tokens};
@@ -718,11 +738,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
       if (!fn ||
           fn(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(c.q), qd, qs, qb, qe,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
-          !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
-                            c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-          !encode_cache_map(&tm_vt, c.v_cache, c.dtype, c.num_blocks, c.block_size,
-                            c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B))
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PA_ERR_CUDA;
       slot = timed ? prof_begin(PA_K_TILE, st) : -1;
       const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vt, num_sms, st);

@@ -38,6 +38,13 @@ int row_kernel_ctas_per_sm(int dtype, int head_dim, int group);
 cudaError_t launch_row_kernel(const FwdParams &p, const CUtensorMap &tm_k,
                               const CUtensorMap &tm_v, int grid, cudaStream_t stream);
 
+// bf16 decode rows on warp-level MMAs (mma.sync m16n8k16); K/V maps are the
+// 128-byte-swizzled 64-element boxes the tile kernel also uses.
+bool row_mma_supported(int dtype, int head_dim, int group);
+int row_mma_ctas_per_sm(int head_dim, int group);
+cudaError_t launch_row_mma_kernel(const FwdParams &p, const CUtensorMap &tm_k,
+                                  const CUtensorMap &tm_v, int grid, cudaStream_t stream);
+
 // Tensor-core (tcgen05) tile kernel for bf16 extend/prefill rows.
 bool tile_kernel_supported(int dtype, int head_dim, int group);
 cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,

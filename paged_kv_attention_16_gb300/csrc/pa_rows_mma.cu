@@ -1,0 +1,537 @@
+// pa_rows_mma.cu -- the bf16 decode row kernel on warp-level tensor-core MMAs.
+//
+// A decode row is one query token of one request against that request's KV
+// pages ("vLLM Triton attention backend deep dive", sections "Technical
+// implementation of paged attention" and "Parallel tiled softmax (3D
+// kernel)"); it is bound by HBM bandwidth ("vLLM AMD ROCm attention backend
+// optimisation", section "Mixed inference workload challenge").  One work
+// item is one token x one KV head (its G query heads) x one KV split, as in
+// the CUDA-core row kernel (pa_rows.cu), which keeps the fp32 path.
+//
+// Why warp MMAs here: on CUDA cores a bf16 decode row costs ~50 warp
+// instructions per KV position (conversions, 2*G*D FMAs, shuffle
+// reductions), which caps the kernel below HBM speed at two resident CTAs
+// per SM.  The row's contraction is a dense (G x D) . (D x N) product, so it
+// is run as mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the G heads
+// padded to 16 rows: ~6 instructions per KV position.  tcgen05 needs at
+// least 64 rows per MMA and a round trip through tensor memory for the
+// softmax; with G <= 16 real rows the warp-level form keeps S and P in
+// registers and needs no tensor-memory traffic.
+//
+// Layout and flow:
+//  * Producer warp: per item, the split's page ids; per stage (64 KV
+//    positions), TMA box copies {64 dims x 1 head x 16 slots x 1 page} of K
+//    and V with 128-byte swizzle straight from the pages into a ring of
+//    shared-memory stages.  Stage = [K | V], each [D/64 halves][64 rows][128 B].
+//  * Compute warp w owns rows 16w..16w+15 of every stage (one TMA box).
+//    S = Q K^T: Q fragments stay in registers for the item; K fragments by
+//    ldmatrix (conflict-free thanks to the swizzle).  Online softmax in base
+//    2 on the accumulator fragment (row max over the 4 lanes of a quad),
+//    lazy rescale (the max moves only when it grows by more than 8).  P is
+//    packed to bf16 in place as the A operand of O += P V (V by ldmatrix.trans).
+//  * KV positions past the split's end: their scores are masked by select;
+//    their V rows (which may hold anything, including NaN) are zeroed in
+//    shared memory before the PV product, since 0 * NaN is NaN.
+//  * End of item: the four warps' (m, l, O) are merged through shared memory
+//    and written to the output (single split) or as a split partial.
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+constexpr float kLazyRescale = 8.0f;
+
+template <int D, int G>
+struct MmaRowCfg {
+  static constexpr int NWARP = 4;                    // compute warps
+  static constexpr int NTHREADS = 32 * (NWARP + 1);  // + producer warp
+  static constexpr int ROWS_W = 16;                  // KV rows per warp per stage
+  static constexpr int ST = NWARP * ROWS_W;          // KV rows per stage (64)
+  static constexpr int BOX = 16;                     // slots per TMA box
+  static constexpr int HALVES = D / 64;              // 128-byte swizzle atoms per row
+  static constexpr int HALF_BYTES = ST * 128;        // one half of K (or V) in a stage
+  static constexpr int KV_BYTES = HALVES * HALF_BYTES;
+  static constexpr int STAGE_BYTES = 2 * KV_BYTES;
+  static constexpr int BOX_BYTES = BOX * 128;
+  static constexpr int KS = D / 16;                  // k-steps of S = Q K^T
+  static constexpr int NT = D / 8;                   // n-tiles of O
+  static constexpr int SCR_BYTES = NWARP * G * D * 4;
+  // two resident CTAs per SM: about 113 KB of shared memory each
+  static constexpr int NSTAGE0 = (112 * 1024 - SCR_BYTES - 4096) / STAGE_BYTES;
+  static constexpr int NSTAGE = NSTAGE0 < 2 ? 2 : (NSTAGE0 > 6 ? 6 : NSTAGE0);
+  static constexpr int MAX_PAGES = kRowMaxSplit / BOX + 2;
+  static constexpr int OFF_RING = 0;  // 1024-byte aligned (swizzle atoms)
+  static constexpr int OFF_SCR = OFF_RING + NSTAGE * STAGE_BYTES;
+  static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;
+  static constexpr int OFF_PAGES = OFF_ML + 2 * NWARP * G * 4;
+  static constexpr int OFF_DESC = OFF_PAGES + MAX_PAGES * 4;
+  static constexpr int OFF_BAR = (OFF_DESC + 2 * 64 + 15) / 16 * 16;
+  static constexpr int NBAR = 2 * NSTAGE + 4;
+  static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;  // + alignment slack
+  static constexpr int OPT = (G * D + 127) / 128;         // merge outputs per thread
+  static_assert(D == 64 || D == 128, "head_dim 64 or 128");
+  static_assert(G >= 1 && G <= 16, "at most 16 query heads per KV head");
+};
+
+struct MmaRowDesc {
+  int done, bad;
+  int tok, kvh, i, split, kv_lo, kv_hi, direct, nsplit;
+  long long prow0;  // partial row of head 0 of the group (split partials)
+};
+static_assert(sizeof(MmaRowDesc) <= 64, "descriptor slot is 64 bytes");
+
+__device__ inline void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ inline void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+// c += a (16x16, row) * b (16x8, col); bf16 inputs, fp32 accumulators.
+__device__ inline void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                 uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Two floats to a bf16 pair (round to nearest even): `lo` in bits 0..15.
+__device__ inline uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t *>(&v);
+}
+
+// Shared-memory address of 16-byte chunk `c` (0 .. D/8-1) of stage row `r`
+// under the 128-byte swizzle the TMA copies apply (chunk index XOR row % 8
+// inside each 1024-byte atom of 8 rows).
+template <int D>
+__device__ inline uint32_t swz_addr(uint32_t base, int r, int c) {
+  return base + (c >> 3) * (64 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+}
+
+
+template <int D, int G>
+__global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                                const __grid_constant__ CUtensorMap tm_v,
+                                                const FwdParams p) {
+  using C = MmaRowCfg<D, G>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t *ring = smem + C::OFF_RING;
+  float *s_o = reinterpret_cast<float *>(smem + C::OFF_SCR);
+  float *s_m = reinterpret_cast<float *>(smem + C::OFF_ML);
+  float *s_l = s_m + C::NWARP * G;
+  int *s_pages = reinterpret_cast<int *>(smem + C::OFF_PAGES);
+  MmaRowDesc *s_desc = reinterpret_cast<MmaRowDesc *>(smem + C::OFF_DESC);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+  uint64_t *empty = full + C::NSTAGE;
+  uint64_t *item_full = empty + C::NSTAGE;  // [2]
+  uint64_t *item_free = item_full + 2;      // [2]
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int S = p.num_seqs, H = p.num_heads, bs = p.block_size;
+
+  if (tid == 0) {
+    prefetch_tensor_map(&tm_k);
+    prefetch_tensor_map(&tm_v);
+    for (int i = 0; i < C::NSTAGE; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], C::NWARP);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&item_full[i], 1);
+      mbar_init(&item_free[i], C::NWARP);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  pdl_trigger();
+  pdl_wait();  // the plan
+  bool dead = false;
+
+  if (warp == C::NWARP) {
+    // ===================================================== producer warp
+    const long long n_items = p.plan->n[kListRow];
+    const long long *row_end = p.list_end + (size_t)kListRow * S;
+    uint32_t g = 0, seq = 0;  // stages issued, descriptors written
+    for (;;) {
+      long long item = 0;
+      if (lane == 0) item = (long long)atomicAdd(&p.plan->counter[kListRow], 1ull);
+      item = __shfl_sync(0xffffffffu, item, 0);
+      MmaRowDesc d{};
+      int npages = 0, pfirst = 0, s = 0;
+      if (item >= n_items) {
+        d.done = 1;
+      } else {
+        const int k = list_find(row_end, S, item);
+        const long long start = k ? row_end[k - 1] : 0;
+        s = p.ord[k];
+        const ReqInfo r = p.req[s];
+        const long long local = item - start;
+        const long long per_kvh = (long long)r.nsplit * r.q_len;
+        d.kvh = (int)(local / per_kvh);
+        const int rem = (int)(local % per_kvh);
+        d.split = rem / r.q_len;
+        d.i = rem % r.q_len;
+        d.tok = r.q_start + d.i;
+        const int kv_row_hi = r.ctx - r.q_len + d.i + 1;  // causal: 0 .. prefix + i
+        d.kv_lo = d.split * r.split_len;
+        d.kv_hi = min(kv_row_hi, d.kv_lo + r.split_len);
+        if (d.kv_lo >= d.kv_hi) continue;  // split past this row's causal bound
+        d.direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
+        d.nsplit = r.nsplit;
+        d.prow0 = r.partial_base + ((long long)d.i * H + d.kvh * G) * r.nsplit + d.split;
+        pfirst = d.kv_lo / bs;
+        npages = (d.kv_hi - 1) / bs - pfirst + 1;
+      }
+      // the page list is private to this warp; its earlier readers (TMA
+      // issues below) are synchronous, so it is free to overwrite
+      const int32_t *bt = p.block_table + (size_t)s * p.max_blocks_per_seq;
+      int bad = 0;
+      for (int j = lane; j < npages; j += 32) {
+        const int lp = pfirst + j;
+        const int pid = lp < p.max_blocks_per_seq ? __ldg(bt + lp) : -1;
+        if (pid < 0 || pid >= p.num_blocks) bad = 1;
+        s_pages[j] = pid;
+      }
+      d.bad = __any_sync(0xffffffffu, bad);
+      if (d.bad && lane == 0) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+      __syncwarp();
+      const int slot = seq & 1;
+      if (lane == 0) {
+        if (seq >= 2) mbar_wait(&item_free[slot], ((seq >> 1) - 1) & 1, dead, p.status);
+        s_desc[slot] = d;
+        mbar_arrive(&item_full[slot]);
+      }
+      ++seq;
+      if (d.done) break;
+      if (d.bad) continue;
+      // stream the split: per stage, lane -> (box, K|V, half)
+      const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
+      const int bx = lane / (2 * C::HALVES);
+      const int kv = (lane / C::HALVES) & 1;
+      const int hf = lane % C::HALVES;
+      for (int j = 0; j < nst; ++j, ++g) {
+        const int b = g % C::NSTAGE;
+        const int pos0 = d.kv_lo + j * C::ST;
+        const int pos = pos0 + bx * C::BOX;
+        const bool issue = bx < C::NWARP && pos < d.kv_hi;
+        const int nbox = min(C::NWARP, (d.kv_hi - pos0 + C::BOX - 1) / C::BOX);
+        if (lane == 0) {
+          if (g >= C::NSTAGE) mbar_wait(&empty[b], ((g / C::NSTAGE) - 1) & 1, dead, p.status);
+          mbar_arrive_expect_tx(&full[b], nbox * 2 * C::HALVES * C::BOX_BYTES);
+        }
+        __syncwarp();
+        if (issue) {
+          const int page = s_pages[pos / bs - pfirst];
+          uint8_t *dst = ring + b * C::STAGE_BYTES + kv * C::KV_BYTES + hf * C::HALF_BYTES +
+                         bx * C::BOX_BYTES;
+          tma_load_4d(dst, kv ? &tm_v : &tm_k, hf * 64, d.kvh, pos % bs, page, &full[b]);
+        }
+      }
+    }
+    return;
+  }
+
+  // ======================================================= compute warps
+  const int gq = lane >> 2, tq = lane & 3;  // fragment row group, column pair
+  const int r0 = warp * C::ROWS_W;          // this warp's rows in every stage
+  const uint32_t ring_s = smem_u32(ring);
+  uint32_t g = 0;
+  for (uint32_t seq = 0;; ++seq) {
+    const int islot = seq & 1;
+    mbar_wait(&item_full[islot], (seq >> 1) & 1, dead, p.status);
+    const MmaRowDesc d = s_desc[islot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&item_free[islot]);
+    if (d.done) break;
+    const int kvh = d.kvh;
+    if (d.bad) {
+      for (int e = tid; e < G * D; e += 128) {
+        const int h = e / D, dd = e % D;
+        if (d.direct) {
+          reinterpret_cast<__nv_bfloat16 *>(p.out)[((size_t)d.tok * H + kvh * G + h) * D + dd] =
+              __float2bfloat16_rn(0.f);
+        } else {
+          const long long prow = d.prow0 + (long long)h * d.nsplit;
+          p.part_o[prow * D + dd] = 0.f;
+          if (dd == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
+        }
+      }
+      continue;
+    }
+
+    // Q of the G heads as A fragments (rows >= G are zero): a0/a2 row gq,
+    // a1/a3 row gq + 8; columns 16 ks + 2 tq (+8 for a2/a3).
+    uint32_t qa[C::KS][4];
+    {
+      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+          reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((size_t)d.tok * H + kvh * G) * D);
+#pragma unroll
+      for (int ks = 0; ks < C::KS; ++ks) {
+        const int c = (ks * 16 + 2 * tq) >> 1;  // in bf16 pairs
+        qa[ks][0] = gq < G ? __ldg(qrow + gq * (D / 2) + c) : 0u;
+        qa[ks][1] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c) : 0u;
+        qa[ks][2] = gq < G ? __ldg(qrow + gq * (D / 2) + c + 4) : 0u;
+        qa[ks][3] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c + 4) : 0u;
+      }
+    }
+    float o[C::NT][4];
+#pragma unroll
+    for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+    const float sl2 = p.scale_log2;
+
+    const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
+    for (int j = 0; j < nst; ++j, ++g) {
+      const int b = g % C::NSTAGE;
+      mbar_wait(&full[b], (g / C::NSTAGE) & 1, dead, p.status);
+      const int nv = min(C::ROWS_W, d.kv_hi - (d.kv_lo + j * C::ST + r0));
+      const uint32_t kbase = ring_s + b * C::STAGE_BYTES;
+      const uint32_t vbase = kbase + C::KV_BYTES;
+      if (nv > 0) {
+        if (nv < C::ROWS_W) {
+          // zero the V rows past the split's end (this warp's box only)
+          uint8_t *vb = ring + b * C::STAGE_BYTES + C::KV_BYTES;
+          for (int e = lane; e < (C::ROWS_W - nv) * C::HALVES * 8; e += 32) {
+            const int r = r0 + nv + e / (C::HALVES * 8);
+            const int c = e % (C::HALVES * 8);
+            *reinterpret_cast<uint4 *>(vb + (c >> 3) * C::HALF_BYTES + r * 128 + (c & 7) * 16) =
+                make_uint4(0u, 0u, 0u, 0u);
+          }
+          __syncwarp();
+        }
+        // ---- S = Q K^T for this warp's 16 rows (two n-tiles of 8)
+        float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int kr = r0 + (mi >> 1) * 8 + rr;  // K row this lane addresses
+#pragma unroll
+          for (int ks = 0; ks < C::KS; ++ks) {
+            uint32_t kb[4];
+            ldsm_x4(swz_addr<D>(kbase, kr, ks * 2 + (mi & 1)), kb);
+            mma_16816(s[0], qa[ks], kb[0], kb[1]);
+            mma_16816(s[1], qa[ks], kb[2], kb[3]);
+          }
+        }
+        // ---- scale, mask, online softmax (rows gq and gq + 8)
+        float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+        for (int n = 0; n < 2; ++n)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int col = n * 8 + 2 * tq + (e & 1);
+            s[n][e] = col < nv ? s[n][e] * sl2 : -INFINITY;
+            if (e < 2) mx_lo = fmaxf(mx_lo, s[n][e]);
+            else mx_hi = fmaxf(mx_hi, s[n][e]);
+          }
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+        mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+        if (mx_lo > m_lo + kLazyRescale) {
+          const float a = fast_exp2(m_lo - mx_lo);
+          l_lo *= a;
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n) {
+            o[n][0] *= a;
+            o[n][1] *= a;
+          }
+          m_lo = mx_lo;
+        }
+        if constexpr (G > 8) {
+          mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+          mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+          if (mx_hi > m_hi + kLazyRescale) {
+            const float a = fast_exp2(m_hi - mx_hi);
+            l_hi *= a;
+#pragma unroll
+            for (int n = 0; n < C::NT; ++n) {
+              o[n][2] *= a;
+              o[n][3] *= a;
+            }
+            m_hi = mx_hi;
+          }
+        }
+        float pr[2][4];
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+          pr[n][0] = fast_exp2(s[n][0] - m_lo);
+          pr[n][1] = fast_exp2(s[n][1] - m_lo);
+          if constexpr (G > 8) {
+            pr[n][2] = fast_exp2(s[n][2] - m_hi);
+            pr[n][3] = fast_exp2(s[n][3] - m_hi);
+          } else {
+            pr[n][2] = pr[n][3] = 0.f;
+          }
+        }
+        l_lo += (pr[0][0] + pr[0][1]) + (pr[1][0] + pr[1][1]);
+        if constexpr (G > 8) l_hi += (pr[0][2] + pr[0][3]) + (pr[1][2] + pr[1][3]);
+        // P as the A operand (16 rows x 16 KV positions)
+        uint32_t pa[4];
+        pa[0] = pack_bf16(pr[0][0], pr[0][1]);
+        pa[1] = pack_bf16(pr[0][2], pr[0][3]);
+        pa[2] = pack_bf16(pr[1][0], pr[1][1]);
+        pa[3] = pack_bf16(pr[1][2], pr[1][3]);
+        // ---- O += P V (V fragments transposed out of the row-major stage)
+        {
+          const int mi = lane >> 3, rr = lane & 7;
+          const int vr = r0 + (mi & 1) * 8 + rr;  // V row this lane addresses
+#pragma unroll
+          for (int np = 0; np < C::NT / 2; ++np) {
+            uint32_t vb4[4];
+            ldsm_x4_trans(swz_addr<D>(vbase, vr, np * 2 + (mi >> 1)), vb4);
+            mma_16816(o[2 * np], pa, vb4[0], vb4[1]);
+            mma_16816(o[2 * np + 1], pa, vb4[2], vb4[3]);
+          }
+        }
+        if (nv < C::ROWS_W) fence_proxy_async();  // generic zeroing before the next TMA fill
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[b]);
+    }
+
+    // ---- this warp's (m, l, O) rows to shared memory
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    if constexpr (G > 8) {
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+      l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    }
+    named_sync(1, 128);  // the scratch of the previous item has been read
+    if (gq < G) {
+#pragma unroll
+      for (int n = 0; n < C::NT; ++n)
+        *reinterpret_cast<float2 *>(&s_o[(warp * G + gq) * D + n * 8 + 2 * tq]) =
+            make_float2(o[n][0], o[n][1]);
+      if (tq == 0) {
+        s_m[warp * G + gq] = m_lo;
+        s_l[warp * G + gq] = l_lo;
+      }
+    }
+    if constexpr (G > 8) {
+      if (gq + 8 < G) {
+#pragma unroll
+        for (int n = 0; n < C::NT; ++n)
+          *reinterpret_cast<float2 *>(&s_o[(warp * G + gq + 8) * D + n * 8 + 2 * tq]) =
+              make_float2(o[n][2], o[n][3]);
+        if (tq == 0) {
+          s_m[warp * G + gq + 8] = m_hi;
+          s_l[warp * G + gq + 8] = l_hi;
+        }
+      }
+    }
+    named_sync(1, 128);
+    // ---- log-sum-exp merge of the four warps, then output or partial
+    const int e0 = tid * C::OPT;
+    if (e0 < G * D) {
+      const int h = e0 / D, d0 = e0 % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < C::NWARP; ++w) M = fmaxf(M, s_m[w * G + h]);
+      float L = 0.f, acc[C::OPT];
+#pragma unroll
+      for (int x = 0; x < C::OPT; ++x) acc[x] = 0.f;
+#pragma unroll
+      for (int w = 0; w < C::NWARP; ++w) {
+        const float ms = s_m[w * G + h];
+        if (ms == -INFINITY) continue;
+        const float wt = fast_exp2(ms - M);
+        L = fmaf(s_l[w * G + h], wt, L);
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) acc[x] = fmaf(s_o[(w * G + h) * D + d0 + x], wt, acc[x]);
+      }
+      const float inv = L > 0.f ? 1.f / L : 0.f;
+      if (d.direct) {
+        __nv_bfloat16 *dst =
+            reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)d.tok * H + kvh * G + h) * D + d0;
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) dst[x] = __float2bfloat16_rn(acc[x] * inv);
+      } else {
+        const long long prow = d.prow0 + (long long)h * d.nsplit;
+#pragma unroll
+        for (int x = 0; x < C::OPT; ++x) p.part_o[prow * D + d0 + x] = acc[x] * inv;
+        if (d0 == 0) p.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
+      }
+    }
+  }
+}
+
+template <int D, int G>
+cudaError_t set_attrs() {
+  using C = MmaRowCfg<D, G>;
+  cudaError_t e = cudaFuncSetAttribute(row_mma_kernel<D, G>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(row_mma_kernel<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                              cudaSharedmemCarveoutMaxShared);
+}
+
+template <typename Fn>
+bool dispatch_mma(int head_dim, int group, Fn &&fn) {
+#define PA_MMA_CASE(D, G) \
+  if (head_dim == D && group == G) { fn.template operator()<D, G>(); return true; }
+#define PA_MMA_GROUPS(D) \
+  PA_MMA_CASE(D, 1) PA_MMA_CASE(D, 2) PA_MMA_CASE(D, 4) PA_MMA_CASE(D, 8) PA_MMA_CASE(D, 16)
+  PA_MMA_GROUPS(64)
+  PA_MMA_GROUPS(128)
+#undef PA_MMA_GROUPS
+#undef PA_MMA_CASE
+  return false;
+}
+
+struct MmaOccFn {
+  int n = 0;
+  template <int D, int G>
+  void operator()() {
+    using C = MmaRowCfg<D, G>;
+    if (set_attrs<D, G>() != cudaSuccess) return;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, row_mma_kernel<D, G>, C::NTHREADS,
+                                                      C::SMEM) != cudaSuccess)
+      n = 0;
+  }
+};
+
+struct MmaLaunchFn {
+  const FwdParams &p;
+  const CUtensorMap &tk, &tv;
+  int grid;
+  cudaStream_t stream;
+  cudaError_t err;
+  template <int D, int G>
+  void operator()() {
+    using C = MmaRowCfg<D, G>;
+    err = set_attrs<D, G>();
+    if (err != cudaSuccess) return;
+    err = launch_dependent(row_mma_kernel<D, G>, dim3(grid), dim3(C::NTHREADS), C::SMEM, stream,
+                           tk, tv, p);
+  }
+};
+
+}  // namespace
+
+bool row_mma_supported(int dtype, int head_dim, int group) {
+  return dtype == PA_BF16 && (head_dim == 64 || head_dim == 128) &&
+         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
+}
+
+int row_mma_ctas_per_sm(int head_dim, int group) {
+  MmaOccFn occ;
+  dispatch_mma(head_dim, group, occ);
+  return occ.n;
+}
+
+cudaError_t launch_row_mma_kernel(const FwdParams &p, const CUtensorMap &tm_k,
+                                  const CUtensorMap &tm_v, int grid, cudaStream_t stream) {
+  MmaLaunchFn l{p, tm_k, tm_v, grid, stream, cudaErrorInvalidValue};
+  dispatch_mma(p.head_dim, p.num_heads / p.num_kv_heads, l);
+  return l.err;
+}
+
+}  // namespace pa
