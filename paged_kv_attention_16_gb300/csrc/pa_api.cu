@@ -59,11 +59,10 @@ __device__ inline ReqScalars classify(const FwdParams &p, int q_start, int q_end
 constexpr int kPlanCache = kPlanThreads;
 
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
-  __shared__ long long scratch[5 * 33];
-  __shared__ int s_max_merge_splits;
+  __shared__ long long scratch[(kNumLists + 1) * 33];
   __shared__ int4 s_req[kPlanCache];  // q_start, q_end, ctx, -
   __shared__ int s_ord[kPlanCache];
-  const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x;
+  const int S = p.num_seqs, T = p.num_tokens, tid = threadIdx.x, nthr = blockDim.x;
   const int Hk = p.num_kv_heads, G = p.num_heads / p.num_kv_heads, H = p.num_heads;
   const bool cached = S <= kPlanCache;
   // Launched programmatically after whatever preceded this call in the
@@ -71,7 +70,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   // this workspace) before touching memory.
   pdl_wait();
   pdl_trigger();  // the row kernel may start its prologue meanwhile
-  if (tid == 0) s_max_merge_splits = 0;
   auto raw = [&](int s) -> int4 {
     if (cached) return s_req[s];
     return make_int4(p.qsl[s], p.qsl[s + 1], p.seq_lens[s], 0);
@@ -81,14 +79,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   int bad = 0;
   if (cached && tid < S) s_req[tid] = make_int4(p.qsl[tid], p.qsl[tid + 1], p.seq_lens[tid], 0);
   if (tid == 0 && (p.qsl[0] != 0 || p.qsl[S] != T)) bad = 1;
-  for (int s = tid; s < S; s += kPlanThreads)
+  for (int s = tid; s < S; s += nthr)
     if (p.qsl[s + 1] < p.qsl[s]) bad = 1;
   const bool qsl_bad = __syncthreads_or(bad) != 0;
 
   // -- pass 1: class counts and the decode KV work (split sizing) ------------
   long long v1[2] = {0, 0};  // packed class counts (21 bits each), decode work
   int metabad = 0;
-  for (int s = tid; s < S; s += kPlanThreads) {
+  for (int s = tid; s < S; s += nthr) {
     const int4 q = raw(s);
     const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
     v1[0] += 1ll << (21 * r.cls);
@@ -123,7 +121,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
 
   // -- pass 2: stable partition into [decode : extend : prefill] -------------
   long long carry = 0;
-  for (int base = 0; base < S; base += kPlanThreads) {
+  for (int base = 0; base < S; base += nthr) {
     const int s = base + tid;
     long long v[1] = {0};
     int cls = 0;
@@ -146,23 +144,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   __syncthreads();
 
   // -- pass 3: per-request plan and list prefix sums in reordered order ------
-  long long run[kNumLists + 1] = {0, 0, 0, 0, 0};  // lists, then partial rows
-  for (int base = 0; base < S; base += kPlanThreads) {
+  long long run[kNumLists + 1] = {};  // lists, then partial rows
+  for (int base = 0; base < S; base += nthr) {
     const int k = base + tid;
-    long long cnt[kNumLists + 1] = {0, 0, 0, 0, 0};
+    long long cnt[kNumLists + 1] = {};
     int s = -1;
     ReqInfo info{};
     if (k < S) {
       s = cached ? s_ord[k] : p.ord[k];
       const int4 q = raw(s);
       const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
-      // Decode rows stream on CUDA cores while G < 8; from G = 8 the FFMA
-      // issue rate, not HBM, would bound them, so they join the tensor-core
-      // tile path (one token x G heads per 128-row tile).
-      const bool row_path = !p.tile_ok || (r.cls == kDecode && G < 8);
+      // Decode rows stream through the row kernel (warp MMAs for bf16, at
+      // most 16 query rows per KV head); extend and prefill rows fill
+      // 128-row tiles of the tcgen05 tile kernel when it applies.
+      const bool row_path = !p.tile_ok || r.cls == kDecode;
       int len;
       if (r.cls == kDecode) {
-        len = row_path ? L : max(L, kTileDecodeMinSplit);
+        len = L;
         if (p.kv_split_tokens > 0 && p.kv_split_tokens < len) len = p.kv_split_tokens;
       } else {
         len = row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens : (r.ctx > 0 ? r.ctx : 1));
@@ -179,7 +177,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
         if (row_path) cnt[kListRow] = (long long)Hk * r.q_len * nsplit;
         else cnt[kListTile] = (long long)Hk * ceil_div_ll((long long)r.q_len * G, kTileRows) * nsplit;
         if (nsplit > 1) {
-          atomicMax(&s_max_merge_splits, nsplit);
+          // row i has ceil((ctx - q_len + i + 1) / len) non-empty splits:
+          // more than kWarpMergeSplits from i = W * len - (ctx - q_len) on
+          const long long i_long =
+              max(0ll, (long long)kWarpMergeSplits * len - (r.ctx - r.q_len));
+          if (i_long < r.q_len) cnt[kListMergeLong] = (r.q_len - i_long) * H;
           cnt[kListMerge] = (long long)r.q_len * H;
           cnt[kNumLists] = (long long)r.q_len * H * nsplit;
         }
@@ -207,7 +209,6 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     for (int x = 0; x < 8; ++x) p.plan->counter[x] = 0;
     p.plan->qsl_bad = zero_all ? 1 : 0;
     p.plan->split_len_decode = L;
-    p.plan->max_merge_splits = s_max_merge_splits;
     p.plan->partial_rows = run_part;
   }
 }
@@ -226,8 +227,8 @@ __device__ inline void store_out<__nv_bfloat16>(__nv_bfloat16 *dst, float v) {
 }
 
 // Rows with at most kWarpMergeSplits non-empty splits are merged by one warp
-// (lanes over head_dim); longer rows by a whole block (warps over splits).
-constexpr int kWarpMergeSplits = 8;
+// (lane q holds split q's log-sum-exp; lanes over head_dim for the sums);
+// longer rows (their own list) by a whole block (warps over splits).
 // Merge-list prefix sums kept in shared memory for batches up to this size.
 constexpr int kMergeCache = 1024;
 
@@ -236,19 +237,38 @@ struct MergeRow {
   int h, nn;
 };
 
-// mend: the merge list's ends, in global memory or (shared = true) in a
-// shared-memory copy.
-__device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, bool shared,
-                                     long long row) {
+// mend / ord: the merge list's ends and the request order, in global memory
+// or (shared = true) as shared-memory copies.
+__device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, const int *ord,
+                                     bool shared, long long row) {
   const int S = p.num_seqs, H = p.num_heads;
   const int k = shared ? list_find_shared(mend, S, row) : list_find(mend, S, row);
   const long long local = row - (k ? mend[k - 1] : 0);
-  const ReqInfo r = p.req[p.ord[k]];
+  const ReqInfo r = p.req[ord[k]];
   const int i = (int)(local / H);
   MergeRow m;
   m.h = (int)(local % H);
   m.tok = r.q_start + i;
   m.nn = (int)ceil_div_ll(r.ctx - r.q_len + i + 1, r.split_len);  // non-empty splits
+  m.base = r.partial_base + ((long long)i * H + m.h) * r.nsplit;
+  return m;
+}
+
+// Entry `row` of the long-row list: request k's rows i >= i_long (those with
+// more than kWarpMergeSplits non-empty splits), H heads each.
+__device__ inline MergeRow merge_row_long(const FwdParams &p, const long long *lend,
+                                          long long row) {
+  const int S = p.num_seqs, H = p.num_heads;
+  const int k = list_find(lend, S, row);
+  const long long local = row - (k ? lend[k - 1] : 0);
+  const ReqInfo r = p.req[p.ord[k]];
+  const long long i_long =
+      max(0ll, (long long)kWarpMergeSplits * r.split_len - (r.ctx - r.q_len));
+  const int i = (int)(i_long + local / H);
+  MergeRow m;
+  m.h = (int)(local % H);
+  m.tok = r.q_start + i;
+  m.nn = (int)ceil_div_ll(r.ctx - r.q_len + i + 1, r.split_len);
   m.base = r.partial_base + ((long long)i * H + m.h) * r.nsplit;
   return m;
 }
@@ -291,20 +311,27 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
 
   const long long nm = p.plan->n[kListMerge];
   if (nm == 0) return;
-  // the merge list's per-request ends, searched once per row
+  // the merge list's per-request ends (searched once per row) and the
+  // request order, copied to shared memory for batches up to kMergeCache
   __shared__ long long s_mend[kMergeCache];
+  __shared__ int s_ordc[kMergeCache];
   const long long *mend = p.list_end + (size_t)kListMerge * S;
+  const int *ord = p.ord;
   const bool mend_shared = S <= kMergeCache;
   if (mend_shared) {
-    for (int k = tid; k < S; k += kMergeThreads) s_mend[k] = mend[k];
+    for (int k = tid; k < S; k += kMergeThreads) {
+      s_mend[k] = mend[k];
+      s_ordc[k] = ord[k];
+    }
     __syncthreads();
     mend = s_mend;
+    ord = s_ordc;
   }
   const int dpl = D / 32;  // dims per lane: 2 or 4
 
   // ---- short rows: one warp each ---------------------------------------------
   for (long long row = gw; row < nm; row += nw) {
-    const MergeRow mr = merge_row(p, mend, mend_shared, row);
+    const MergeRow mr = merge_row(p, mend, ord, mend_shared, row);
     if (mr.nn <= 1 || mr.nn > kWarpMergeSplits) continue;
     const float lse = lane < mr.nn ? p.part_lse[mr.base + lane] : -INFINITY;
     int bad = isnan(lse) ? 1 : 0;
@@ -315,23 +342,39 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
       bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     }
     const float w_own = (lane < mr.nn && !bad) ? fast_exp2(lse - M) : 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f}, L = 0.f;
+    float L = w_own;
 #pragma unroll
-    for (int q = 0; q < kWarpMergeSplits; ++q) {
-      if (q >= mr.nn) break;
-      const float w = __shfl_sync(0xffffffffu, w_own, q);
-      L += w;
-      const float *src = p.part_o + (size_t)(mr.base + q) * D + lane * dpl;
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    // partial rows in groups of 8: the loads of a group are independent
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const float *src0 = p.part_o + (size_t)mr.base * D + lane * dpl;
+    for (int q0 = 0; q0 < mr.nn; q0 += 8) {
       if (dpl == 4) {
-        const float4 v = *reinterpret_cast<const float4 *>(src);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
-        acc[2] = fmaf(w, v.z, acc[2]);
-        acc[3] = fmaf(w, v.w, acc[3]);
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (q0 + u < mr.nn) v[u] = __ldg(reinterpret_cast<const float4 *>(src0 + (size_t)(q0 + u) * D));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (q0 + u >= mr.nn) break;
+          const float w = __shfl_sync(0xffffffffu, w_own, q0 + u);
+          acc[0] = fmaf(w, v[u].x, acc[0]);
+          acc[1] = fmaf(w, v[u].y, acc[1]);
+          acc[2] = fmaf(w, v[u].z, acc[2]);
+          acc[3] = fmaf(w, v[u].w, acc[3]);
+        }
       } else {
-        const float2 v = *reinterpret_cast<const float2 *>(src);
-        acc[0] = fmaf(w, v.x, acc[0]);
-        acc[1] = fmaf(w, v.y, acc[1]);
+        float2 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (q0 + u < mr.nn) v[u] = __ldg(reinterpret_cast<const float2 *>(src0 + (size_t)(q0 + u) * D));
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          if (q0 + u >= mr.nn) break;
+          const float w = __shfl_sync(0xffffffffu, w_own, q0 + u);
+          acc[0] = fmaf(w, v[u].x, acc[0]);
+          acc[1] = fmaf(w, v[u].y, acc[1]);
+        }
       }
     }
     const float inv = (bad || !(L > 0.f)) ? 0.f : 1.f / L;
@@ -340,10 +383,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   }
 
   // ---- long rows: one block each, warps over splits ---------------------------
-  if (p.plan->max_merge_splits <= kWarpMergeSplits) return;
-  for (long long row = blockIdx.x; row < nm; row += gridDim.x) {
-    const MergeRow mr = merge_row(p, mend, mend_shared, row);
-    if (mr.nn <= kWarpMergeSplits) continue;  // uniform per block
+  const long long nl = p.plan->n[kListMergeLong];
+  const long long *lend = p.list_end + (size_t)kListMergeLong * S;
+  for (long long row = blockIdx.x; row < nl; row += gridDim.x) {
+    const MergeRow mr = merge_row_long(p, lend, row);
     float M = -INFINITY;
     int bad = 0;
     for (int q = tid; q < mr.nn; q += kMergeThreads) {
@@ -692,7 +735,13 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.status = status;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
-  const cudaError_t plan_err = launch_dependent(plan_kernel, dim3(1), dim3(kPlanThreads), 0, st, p);
+  // One thread per request, whole warps, at most kPlanThreads: small batches
+  // get a small block and cheap barriers.  (The shared-memory copy of the
+  // metadata needs a thread per request whenever S <= kPlanCache.)
+  int plan_threads = ((c.num_seqs > 0 ? c.num_seqs : 1) + 31) / 32 * 32;
+  if (plan_threads > kPlanThreads) plan_threads = kPlanThreads;
+  const cudaError_t plan_err =
+      launch_dependent(plan_kernel, dim3(1), dim3(plan_threads), 0, st, p);
   prof_end(slot, st);
   if (plan_err != cudaSuccess) return PA_ERR_CUDA;
 

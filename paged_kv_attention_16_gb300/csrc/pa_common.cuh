@@ -38,14 +38,25 @@ struct ReqInfo {
 // [0, n) laid over the requests in [decode : extend : prefill] order, with
 // end[k] = inclusive prefix of the per-request counts.  A consumer maps an
 // index to its request with a binary search over end[].
-enum ListId : int { kListRow = 0, kListTile = 1, kListMerge = 2, kListZero = 3, kNumLists = 4 };
+// kListMergeLong: the merge rows with more than kWarpMergeSplits non-empty
+// splits (a suffix of each request's rows), merged by a whole block each.
+enum ListId : int {
+  kListRow = 0,
+  kListTile = 1,
+  kListMerge = 2,
+  kListZero = 3,
+  kListMergeLong = 4,
+  kNumLists = 5
+};
+
+// Rows with at most this many non-empty splits are merged by one warp.
+constexpr int kWarpMergeSplits = 32;
 
 struct PlanHeader {
   long long n[kNumLists];       // total entries per list
   unsigned long long counter[8];  // dynamic work counters, reset by the planner
   int qsl_bad;                  // query_start_loc failed its checks
   int split_len_decode;         // chosen decode split length
-  int max_merge_splits;         // largest nsplit among requests with merge rows
   long long partial_rows;       // partial rows the plan uses
 };
 
@@ -79,9 +90,6 @@ constexpr int kRowMaxSplit = 8192;
 constexpr int kRowMinSplit = 256;
 // Rows per tensor-core tile of the extend/prefill kernel.
 constexpr int kTileRows = 128;
-// Smallest KV split of a decode row on the tile path (keeps items long
-// enough to amortise the tile pipeline's start-up).
-constexpr int kTileDecodeMinSplit = 1024;
 
 __host__ __device__ inline long long ceil_div_ll(long long a, long long b) {
   return (a + b - 1) / b;

@@ -1,6 +1,8 @@
-// pa_rows.cu -- the row-streaming kernel: one work item is one query token of
+// pa_rows.cu -- the fp32 row-streaming kernel on CUDA cores (bf16 rows use
+// the warp-MMA kernel of pa_rows_mma.cu): one work item is one query token of
 // one request, all G query heads of one KV head (the GQA group), over one KV
-// split.  It carries the decode path, which is bound by HBM bandwidth
+// split.  It carries every fp32 row, decode, extend and prefill (fp32 has no
+// tensor-core path: no TF32).  Decode rows are bound by HBM bandwidth
 // ("vLLM AMD ROCm attention backend optimisation", section "Mixed inference
 // workload challenge": decode is memory-bound; "vLLM Triton attention backend
 // deep dive", section "Parallel tiled softmax (3D kernel)": the KV walk of a
@@ -482,10 +484,7 @@ bool dispatch(int dtype, int head_dim, int group, Fn &&fn) {
 #define PA_ROW_GROUPS(T, D) \
   PA_ROW_CASE(T, D, 1) PA_ROW_CASE(T, D, 2) PA_ROW_CASE(T, D, 4) PA_ROW_CASE(T, D, 8) \
   PA_ROW_CASE(T, D, 16)
-  if (dtype == PA_BF16) {
-    PA_ROW_GROUPS(__nv_bfloat16, 64)
-    PA_ROW_GROUPS(__nv_bfloat16, 128)
-  } else if (dtype == PA_F32) {
+  if (dtype == PA_F32) {
     PA_ROW_GROUPS(float, 64)
     PA_ROW_GROUPS(float, 128)
   }
