@@ -16,16 +16,19 @@
 //            {64 dims x 16 slots} named by the block table (K double-buffered,
 //            V one tile behind K);
 //   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
-//            K=head_dim, bf16 in, fp32 in TMEM), then O += P V with P read
+//            K=head_dim, bf16 in, fp32 in TMEM) into one of two S buffers,
+//            running a tile ahead of the softmax, then O += P V with P read
 //            from TMEM (N=head_dim, K=64, V read MN-major straight from its
 //            page layout);
 //   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its S row,
 //            masks by select (causal bound, split bound), keeps a base-2
 //            online softmax with lazy rescaling of O in TMEM (only when the
-//            running max grows by more than 8), stores P as packed bf16 into
-//            one of two TMEM buffers (so the softmax of tile j+1 overlaps the
-//            PV product of tile j), and finally normalises O and stores the
-//            row (or a split partial with its log-sum-exp).
+//            running max grows by more than 8), stores P as packed bf16 over
+//            the first half of the tile's own S buffer (so S of tile j+1 is
+//            computed while the softmax works on tile j, and the softmax of
+//            tile j+1 overlaps the PV product of tile j), and finally
+//            normalises O and stores the row (or a split partial with its
+//            log-sum-exp).
 // Tiles of a split that lie past every row's causal bound are never loaded.
 #include "pa_internal.h"
 
@@ -35,17 +38,25 @@ namespace {
 constexpr int kBN = 64;            // KV positions per tile
 constexpr int kBox = 16;           // slots per TMA box
 constexpr int kTileThreads = 192;  // 4 softmax warps, 1 producer warp, 1 MMA warp
-constexpr int kKStages = 2;
+constexpr int kKStages = 2;        // K tiles in flight per CTA
+constexpr int kVStages = 2;        // V tiles in flight per CTA
+constexpr int kTileCtasPerSm = 2;  // resident CTAs per SM (grid = SMs x this)
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;     // S: columns [0, 64)
-constexpr uint32_t kTmemO = 64;    // O: columns [64, 64 + head_dim)
-constexpr uint32_t kTmemP = 192;   // P: two buffers of 32 columns (64 bf16 per row)
+// Tensor memory (256 columns per CTA, two CTAs per SM): two S buffers of 64
+// fp32 columns; P (64 bf16 per row = 32 columns) is written over the first
+// half of its own S buffer; O after them.
+constexpr uint32_t kTmemS = 0;     // S buffer b: columns [64 b, 64 b + 64)
+constexpr uint32_t kTmemO = 128;   // O: columns [128, 128 + head_dim)
 
-enum Bar {
-  kQFull = 0, kQFree, kKFull0, kKFull1, kKFree0, kKFree1, kVFull0, kVFull1, kVFree0, kVFree1,
-  kSFull, kSFree, kPFull0, kPFull1, kODone0, kODone1, kOFree, kNumBars
-};
+// S buffer b = tile & 1: kSFull0 + b (S product done), kPFull0 + b (P
+// written over it), kODone0 + b (the PV product that read P is done: the
+// buffer is free for S of tile + 2).
+enum Bar { kQFull = 0, kQFree, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree, kKFull0 };
+constexpr int kKFree0 = kKFull0 + kKStages;
+constexpr int kVFull0 = kKFree0 + kKStages;
+constexpr int kVFree0 = kVFull0 + kVStages;
+constexpr int kNumBars = kVFree0 + kVStages;
 
 template <int D>
 struct TileCfg {
@@ -56,7 +67,7 @@ struct TileCfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + 2 * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
@@ -99,7 +110,7 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
 }
 
 template <int D>
-__global__ void __launch_bounds__(kTileThreads, 2)
+__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
   using C = TileCfg<D>;
@@ -126,7 +137,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
     for (int b = 0; b < kNumBars; ++b) {
-      const bool per_warp = b == kSFree || b == kPFull0 || b == kPFull1 || b == kOFree;
+      const bool per_warp = b == kPFull0 || b == kPFull1 || b == kOFree;
       mbar_init(&bar[b], per_warp ? 4 : 1);
     }
     fence_mbar_init();
@@ -178,11 +189,12 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             if (lane == 0 && g >= kKStages)
               mbar_wait(&bar[kKFree0 + st], ((g / kKStages) - 1) & 1, dead, p.status);
           } else {
-            const int st = g & 1;
+            const int st = g % kVStages;
             full = &bar[kVFull0 + st];
             dst = sV + st * C::KV_BYTES;
             map = &tm_v;
-            if (lane == 0 && g >= 2) mbar_wait(&bar[kVFree0 + st], ((g >> 1) - 1) & 1, dead, p.status);
+            if (lane == 0 && g >= kVStages)
+              mbar_wait(&bar[kVFree0 + st], ((g / kVStages) - 1) & 1, dead, p.status);
           }
           if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * C::NH * kBox * 128);
           __syncwarp();
@@ -201,10 +213,12 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     if (lane == 0) {
       uint32_t tiles = 0, items = 0;
       const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
+      // S of tile g into buffer g & 1, once the PV product of tile g - 2
+      // (which read P from that buffer) is done.
       auto issue_s = [&](uint32_t g) {
-        const int st = g % kKStages;
+        const int st = g % kKStages, sb = g & 1;
         mbar_wait(&bar[kKFull0 + st], (g / kKStages) & 1, dead, p.status);
-        if (g > 0) mbar_wait(&bar[kSFree], (g - 1) & 1, dead, p.status);
+        if (g >= 2) mbar_wait(&bar[kODone0 + sb], ((g - 2) >> 1) & 1, dead, p.status);
         tc_fence_after();
         const uint32_t kb = sk + st * C::KV_BYTES;
 #pragma unroll
@@ -212,33 +226,34 @@ __global__ void __launch_bounds__(kTileThreads, 2)
           const int h = kk / 4, sub = kk % 4;
           const uint64_t a = umma_desc_sw128(sq + h * 128 * 128 + sub * 32, 16, 1024);
           const uint64_t b = umma_desc_sw128(kb + h * C::KV_HALF + sub * 32, 16, 1024);
-          tc_mma_bf16(tmem + kTmemS, a, b, C::IDESC_S, kk > 0);
+          tc_mma_bf16(tmem + kTmemS + sb * kBN, a, b, C::IDESC_S, kk > 0);
         }
         tc_commit(&bar[kKFree0 + st]);
-        tc_commit(&bar[kSFull]);
+        tc_commit(&bar[kSFull0 + sb]);
       };
       for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
         TileItem it;
         if (!decode_tile_item(p, item, G, it)) continue;
         mbar_wait(&bar[kQFull], items & 1, dead, p.status);
         issue_s(tiles);
+        if (it.nt > 1) issue_s(tiles + 1);
         for (int j = 0; j < it.nt; ++j) {
           const uint32_t g = tiles + j;
-          if (j + 1 < it.nt) issue_s(g + 1);
-          const int pb = g & 1;
+          const int pb = g & 1, vs = g % kVStages;
           mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, p.status);
-          mbar_wait(&bar[kVFull0 + pb], (g >> 1) & 1, dead, p.status);
+          mbar_wait(&bar[kVFull0 + vs], (g / kVStages) & 1, dead, p.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
           tc_fence_after();
-          const uint32_t vb = sv + pb * C::KV_BYTES;
+          const uint32_t vb = sv + vs * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint64_t b = umma_desc_sw128(vb + kk * 16 * 128, C::KV_HALF, 1024);
-            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 32 + kk * 8, b, C::IDESC_PV,
+            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&bar[kVFree0 + pb]);
+          tc_commit(&bar[kVFree0 + vs]);
           tc_commit(&bar[kODone0 + pb]);
+          if (j + 2 < it.nt) issue_s(g + 2);
         }
         tc_commit(&bar[kQFree]);
         tiles += it.nt;
@@ -285,26 +300,21 @@ __global__ void __launch_bounds__(kTileThreads, 2)
       for (int j = 0; j < it.nt; ++j) {
         const uint32_t g = tiles + j;
         const int base = it.kv_lo + j * kBN;
-        mbar_wait(&bar[kSFull], g & 1, dead, p.status);
+        const int pb = g & 1;  // S buffer of this tile; P goes over its first half
+        mbar_wait(&bar[kSFull0 + pb], (g >> 1) & 1, dead, p.status);
         tc_fence_after();
         float s[kBN];
         if (warp_active) {
+          uint32_t raw0[32], raw1[32];
+          tc_ld32(tmem + lane_off + kTmemS + pb * kBN, raw0);
+          tc_ld32(tmem + lane_off + kTmemS + pb * kBN + 32, raw1);
+          tc_wait_ld();
 #pragma unroll
-          for (int c0 = 0; c0 < kBN; c0 += 32) {
-            uint32_t raw[32];
-            tc_ld32(tmem + lane_off + kTmemS + c0, raw);
-            tc_wait_ld();
-#pragma unroll
-            for (int x = 0; x < 32; ++x) s[c0 + x] = __uint_as_float(raw[x]);
+          for (int x = 0; x < 32; ++x) {
+            s[x] = __uint_as_float(raw0[x]);
+            s[32 + x] = __uint_as_float(raw1[x]);
           }
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kSFree]);
-        // P buffer g & 1 was last read by the PV product of tile g - 2.
-        const int pb = g & 1;
-        if (g >= 2) mbar_wait(&bar[kODone0 + pb], ((g >> 1) - 1) & 1, dead, p.status);
-        tc_fence_after();
         if (warp_active) {
           // Only tiles that cross a row's bound need the select.
           if (__any_sync(0xffffffffu, base + kBN > row_hi)) {
@@ -360,17 +370,18 @@ __global__ void __launch_bounds__(kTileThreads, 2)
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
           }
-          tc_st32(tmem + lane_off + kTmemP + pb * 32, pw);
+          tc_st32(tmem + lane_off + kTmemS + pb * kBN, pw);
           tc_wait_st();
           l += ((suma[0] + suma[1]) + (suma[2] + suma[3])) + ((suma[4] + suma[5]) + (suma[6] + suma[7]));
         }
         if (j == it.nt - 1 && it.kv_hi - base < kBN) {
           // Rows past the tile's KV end may hold anything (NaN tails, stale
           // data); P is 0 there but 0 * NaN is NaN, so zero those V rows.
-          mbar_wait(&bar[kVFull0 + pb], (g >> 1) & 1, dead, p.status);
+          const int vst = g % kVStages;
+          mbar_wait(&bar[kVFull0 + vst], (g / kVStages) & 1, dead, p.status);
           const int first = it.kv_hi - base;
           const int nchunks = (kBN - first) * 8 * C::NH;
-          uint8_t *vs = sV + pb * C::KV_BYTES;
+          uint8_t *vs = sV + vst * C::KV_BYTES;
           for (int e = r; e < nchunks; e += 128) {
             const int h = e / ((kBN - first) * 8);
             const int rem = e % ((kBN - first) * 8);
@@ -453,7 +464,7 @@ cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
   e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_dependent(tile_kernel<D>, dim3(num_sms * 2), dim3(kTileThreads), C::SMEM,
+  return launch_dependent(tile_kernel<D>, dim3(num_sms * kTileCtasPerSm), dim3(kTileThreads), C::SMEM,
                           stream, tq, tk, tv, p);
 }
 
