@@ -747,10 +747,10 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
 
   if (c.num_seqs > 0) {
     const bool mma_rows = row_mma_supported(c.dtype, c.head_dim, group);
-    // K/V pages as 64-element (128-byte) swizzled boxes of 16 slots: the
-    // bf16 row kernel and the tile kernel read them with ldmatrix / UMMA.
+    // K/V pages as 64-element (128-byte) swizzled boxes of 16 slots for the
+    // tile kernel's UMMA operands.
     CUtensorMap tm_kt, tm_vt;
-    if ((mma_rows || tile_ok) &&
+    if (tile_ok &&
         (!encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
                            c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
          !encode_cache_map(&tm_vt, c.v_cache, c.dtype, c.num_blocks, c.block_size,
@@ -759,7 +759,24 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     cudaError_t row_err;
     slot = timed ? prof_begin(PA_K_ROW, st) : -1;
     if (mma_rows) {
-      row_err = launch_row_mma_kernel(p, tm_kt, tm_vt, row_ctas, st);
+      // One box = 16 slots x both 64-dim halves of one KV head of a page:
+      // dims {64 dims, slots, halves, kv heads, pages} (the slot stride is
+      // larger than the half stride; TMA takes strides in any order).
+      const unsigned long long es = 2;
+      const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
+                                          (unsigned long long)(c.head_dim / 64),
+                                          (unsigned long long)c.num_kv_heads,
+                                          (unsigned long long)c.num_blocks};
+      const unsigned long long strides[4] = {
+          (unsigned long long)c.num_kv_heads * c.head_dim * es, 64 * es,
+          (unsigned long long)c.head_dim * es,
+          (unsigned long long)c.block_size * c.num_kv_heads * c.head_dim * es};
+      const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
+      CUtensorMap tm_kr, tm_vr;
+      if (!encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true) ||
+          !encode_tiled(&tm_vr, c.v_cache, c.dtype, 5, dims, strides, box, true))
+        return PA_ERR_CUDA;
+      row_err = launch_row_mma_kernel(p, tm_kr, tm_vr, row_ctas, st);
     } else {
       // fp32: whole rows of head_dim elements, no swizzle (CUDA-core kernel)
       CUtensorMap tm_k, tm_v;

@@ -233,6 +233,17 @@ __device__ inline void tma_load_4d(void *dst, const CUtensorMap *map, int c0, in
       : "memory");
 }
 
+// 5-D tiled TMA load global -> shared, completion counted on `bar`.
+__device__ inline void tma_load_5d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                   int c3, int c4, uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
+      "r"(smem_u32(bar))
+      : "memory");
+}
+
 __device__ inline void tma_load_3d(void *dst, const CUtensorMap *map, int c0, int c1, int c2,
                                    uint64_t *bar) {
   asm volatile(

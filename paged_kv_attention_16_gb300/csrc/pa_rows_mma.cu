@@ -20,9 +20,13 @@
 //
 // Layout and flow:
 //  * Producer warp: per item, the split's page ids; per stage (64 KV
-//    positions), TMA box copies {64 dims x 1 head x 16 slots x 1 page} of K
-//    and V with 128-byte swizzle straight from the pages into a ring of
-//    shared-memory stages.  Stage = [K | V], each [D/64 halves][64 rows][128 B].
+//    positions), one TMA box per 16 slots of a page and per K / V:
+//    {64 dims x 16 slots x D/64 halves} of one KV head, 128-byte swizzled,
+//    straight from the page into a ring of shared-memory stages.  A box
+//    covers whole 256-byte KV rows (both 64-dim halves): TMA throughput on
+//    these gathers is set by the number of boxes, so one box per 16 slots
+//    (not one per half) matters.  Stage = [K | V], each [4 boxes][D/64
+//    halves][16 rows][128 B].
 //  * Compute warp w owns rows 16w..16w+15 of every stage (one TMA box).
 //    S = Q K^T: Q fragments stay in registers for the item; K fragments by
 //    ldmatrix (conflict-free thanks to the swizzle).  Online softmax in base
@@ -49,10 +53,9 @@ struct MmaRowCfg {
   static constexpr int ST = NWARP * ROWS_W;          // KV rows per stage (64)
   static constexpr int BOX = 16;                     // slots per TMA box
   static constexpr int HALVES = D / 64;              // 128-byte swizzle atoms per row
-  static constexpr int HALF_BYTES = ST * 128;        // one half of K (or V) in a stage
-  static constexpr int KV_BYTES = HALVES * HALF_BYTES;
+  static constexpr int BOX_BYTES = BOX * 128 * HALVES;  // one box: [halves][16 rows][128 B]
+  static constexpr int KV_BYTES = NWARP * BOX_BYTES;     // K (or V) of a stage
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
-  static constexpr int BOX_BYTES = BOX * 128;
   static constexpr int KS = D / 16;                  // k-steps of S = Q K^T
   static constexpr int NT = D / 8;                   // n-tiles of O
   static constexpr int SCR_BYTES = NWARP * G * D * 4;
@@ -109,12 +112,13 @@ __device__ inline uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<const uint32_t *>(&v);
 }
 
-// Shared-memory address of 16-byte chunk `c` (0 .. D/8-1) of stage row `r`
-// under the 128-byte swizzle the TMA copies apply (chunk index XOR row % 8
-// inside each 1024-byte atom of 8 rows).
+// Shared-memory address of 16-byte chunk `c` (0 .. D/8-1) of stage row `r`:
+// box r / 16, half c / 8, row r % 16, under the 128-byte swizzle the TMA
+// copies apply (chunk index XOR row % 8 inside each 1024-byte atom).
 template <int D>
 __device__ inline uint32_t swz_addr(uint32_t base, int r, int c) {
-  return base + (c >> 3) * (64 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  return base + (r >> 4) * (16 * 128 * (D / 64)) + (c >> 3) * (16 * 128) + (r & 15) * 128 +
+         (((c & 7) ^ (r & 7)) << 4);
 }
 
 
@@ -214,11 +218,9 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       ++seq;
       if (d.done) break;
       if (d.bad) continue;
-      // stream the split: per stage, lane -> (box, K|V, half)
+      // stream the split: per stage, lane -> (box, K|V)
       const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
-      const int bx = lane / (2 * C::HALVES);
-      const int kv = (lane / C::HALVES) & 1;
-      const int hf = lane % C::HALVES;
+      const int bx = lane >> 1, kv = lane & 1;
       for (int j = 0; j < nst; ++j, ++g) {
         const int b = g % C::NSTAGE;
         const int pos0 = d.kv_lo + j * C::ST;
@@ -227,14 +229,13 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
         const int nbox = min(C::NWARP, (d.kv_hi - pos0 + C::BOX - 1) / C::BOX);
         if (lane == 0) {
           if (g >= C::NSTAGE) mbar_wait(&empty[b], ((g / C::NSTAGE) - 1) & 1, dead, p.status);
-          mbar_arrive_expect_tx(&full[b], nbox * 2 * C::HALVES * C::BOX_BYTES);
+          mbar_arrive_expect_tx(&full[b], nbox * 2 * C::BOX_BYTES);
         }
         __syncwarp();
         if (issue) {
           const int page = s_pages[pos / bs - pfirst];
-          uint8_t *dst = ring + b * C::STAGE_BYTES + kv * C::KV_BYTES + hf * C::HALF_BYTES +
-                         bx * C::BOX_BYTES;
-          tma_load_4d(dst, kv ? &tm_v : &tm_k, hf * 64, d.kvh, pos % bs, page, &full[b]);
+          uint8_t *dst = ring + b * C::STAGE_BYTES + kv * C::KV_BYTES + bx * C::BOX_BYTES;
+          tma_load_5d(dst, kv ? &tm_v : &tm_k, 0, pos % bs, 0, d.kvh, page, &full[b]);
         }
       }
     }
@@ -300,11 +301,11 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       if (nv > 0) {
         if (nv < C::ROWS_W) {
           // zero the V rows past the split's end (this warp's box only)
-          uint8_t *vb = ring + b * C::STAGE_BYTES + C::KV_BYTES;
+          uint8_t *vb = ring + b * C::STAGE_BYTES + C::KV_BYTES + warp * C::BOX_BYTES;
           for (int e = lane; e < (C::ROWS_W - nv) * C::HALVES * 8; e += 32) {
-            const int r = r0 + nv + e / (C::HALVES * 8);
+            const int r = nv + e / (C::HALVES * 8);  // row inside the box
             const int c = e % (C::HALVES * 8);
-            *reinterpret_cast<uint4 *>(vb + (c >> 3) * C::HALF_BYTES + r * 128 + (c & 7) * 16) =
+            *reinterpret_cast<uint4 *>(vb + (c >> 3) * (16 * 128) + r * 128 + (c & 7) * 16) =
                 make_uint4(0u, 0u, 0u, 0u);
           }
           __syncwarp();
