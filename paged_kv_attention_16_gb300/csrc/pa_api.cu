@@ -107,8 +107,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   const long long n_dec = class_tot & mask21, n_ext = (class_tot >> 21) & mask21;
 
   // Decode split: the smallest power of two >= kRowMinSplit that keeps the
-  // item count near 8 items per resident CTA.
-  const long long target = 8ll * (p.row_ctas > 0 ? p.row_ctas : 1);
+  // item count near 8 items per resident CTA
+  // (4 per CTA from G = 8 on: their items carry more work per KV byte)
+  const long long target = (G >= 8 ? 4ll : 8ll) * (p.row_ctas > 0 ? p.row_ctas : 1);
   const long long kv_work = work_tot * Hk;
   int L = kRowMinSplit;
   while (L < kRowMaxSplit && kv_work > (long long)L * target) L <<= 1;

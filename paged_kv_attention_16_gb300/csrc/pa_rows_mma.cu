@@ -246,13 +246,35 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
   const int gq = lane >> 2, tq = lane & 3;  // fragment row group, column pair
   const int r0 = warp * C::ROWS_W;          // this warp's rows in every stage
   const uint32_t ring_s = smem_u32(ring);
-  uint32_t g = 0;
-  for (uint32_t seq = 0;; ++seq) {
-    const int islot = seq & 1;
-    mbar_wait(&item_full[islot], (seq >> 1) & 1, dead, p.status);
-    const MmaRowDesc d = s_desc[islot];
+  uint32_t g = 0, seq = 0;
+  // Descriptor of item `sq` from the producer's two-slot hand-off.
+  auto take = [&](uint32_t sq) {
+    const int islot = sq & 1;
+    mbar_wait(&item_full[islot], (sq >> 1) & 1, dead, p.status);
+    const MmaRowDesc x = s_desc[islot];
     __syncwarp();
     if (lane == 0) mbar_arrive(&item_free[islot]);
+    return x;
+  };
+  // Q of the G heads as A fragments (rows >= G are zero): a0/a2 row gq,
+  // a1/a3 row gq + 8; columns 16 ks + 2 tq (+8 for a2/a3).
+  uint32_t qa[C::KS][4];
+  auto load_q = [&](const MmaRowDesc &x) {
+    const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+        reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((size_t)x.tok * H + x.kvh * G) * D);
+#pragma unroll
+    for (int ks = 0; ks < C::KS; ++ks) {
+      const int c = (ks * 16 + 2 * tq) >> 1;  // in bf16 pairs
+      qa[ks][0] = gq < G ? __ldg(qrow + gq * (D / 2) + c) : 0u;
+      qa[ks][1] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c) : 0u;
+      qa[ks][2] = gq < G ? __ldg(qrow + gq * (D / 2) + c + 4) : 0u;
+      qa[ks][3] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c + 4) : 0u;
+    }
+  };
+  MmaRowDesc nd = take(seq);
+  if (!nd.done && !nd.bad) load_q(nd);
+  for (;;) {
+    const MmaRowDesc d = nd;
     if (d.done) break;
     const int kvh = d.kvh;
     if (d.bad) {
@@ -267,24 +289,11 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
           if (dd == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
         }
       }
+      nd = take(++seq);
+      if (!nd.done && !nd.bad) load_q(nd);
       continue;
     }
 
-    // Q of the G heads as A fragments (rows >= G are zero): a0/a2 row gq,
-    // a1/a3 row gq + 8; columns 16 ks + 2 tq (+8 for a2/a3).
-    uint32_t qa[C::KS][4];
-    {
-      const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
-          reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((size_t)d.tok * H + kvh * G) * D);
-#pragma unroll
-      for (int ks = 0; ks < C::KS; ++ks) {
-        const int c = (ks * 16 + 2 * tq) >> 1;  // in bf16 pairs
-        qa[ks][0] = gq < G ? __ldg(qrow + gq * (D / 2) + c) : 0u;
-        qa[ks][1] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c) : 0u;
-        qa[ks][2] = gq < G ? __ldg(qrow + gq * (D / 2) + c + 4) : 0u;
-        qa[ks][3] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c + 4) : 0u;
-      }
-    }
     float o[C::NT][4];
 #pragma unroll
     for (int n = 0; n < C::NT; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -397,6 +406,11 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[b]);
     }
+
+    // The next item's descriptor and Q now: their latency hides under the
+    // epilogue below (the Q registers are free after the last S product).
+    nd = take(++seq);
+    if (!nd.done && !nd.bad) load_q(nd);
 
     // ---- this warp's (m, l, O) rows to shared memory
     l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
