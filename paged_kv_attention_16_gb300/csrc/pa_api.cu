@@ -748,21 +748,12 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
 
   if (c.num_seqs > 0) {
     const bool mma_rows = row_mma_supported(c.dtype, c.head_dim, group);
-    // K/V pages as 64-element (128-byte) swizzled boxes of 16 slots for the
-    // tile kernel's UMMA operands.
-    CUtensorMap tm_kt, tm_vt;
-    if (tile_ok &&
-        (!encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
-                           c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B) ||
-         !encode_cache_map(&tm_vt, c.v_cache, c.dtype, c.num_blocks, c.block_size,
-                           c.num_kv_heads, c.head_dim, 64, 16, CU_TENSOR_MAP_SWIZZLE_128B)))
-      return PA_ERR_CUDA;
-    cudaError_t row_err;
-    slot = timed ? prof_begin(PA_K_ROW, st) : -1;
-    if (mma_rows) {
-      // One box = 16 slots x both 64-dim halves of one KV head of a page:
-      // dims {64 dims, slots, halves, kv heads, pages} (the slot stride is
-      // larger than the half stride; TMA takes strides in any order).
+    // bf16 K/V boxes of 16 slots x both 64-dim halves of one KV head:
+    // dims {64 dims, slots, halves, kv heads, pages} (the slot stride is
+    // larger than the half stride; TMA takes strides in any order).  The row
+    // kernel reads K and V through them, the tile kernel V.
+    CUtensorMap tm_kr, tm_vr;
+    if (c.dtype == PA_BF16) {
       const unsigned long long es = 2;
       const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
                                           (unsigned long long)(c.head_dim / 64),
@@ -773,10 +764,20 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
           (unsigned long long)c.head_dim * es,
           (unsigned long long)c.block_size * c.num_kv_heads * c.head_dim * es};
       const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
-      CUtensorMap tm_kr, tm_vr;
       if (!encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true) ||
           !encode_tiled(&tm_vr, c.v_cache, c.dtype, 5, dims, strides, box, true))
         return PA_ERR_CUDA;
+    }
+    // The tile kernel's K: one 64-element (128-byte) swizzled box per half
+    // and 16 slots, so the S product sees a uniform row stride.
+    CUtensorMap tm_kt;
+    if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
+                                     c.num_kv_heads, c.head_dim, 64, 16,
+                                     CU_TENSOR_MAP_SWIZZLE_128B))
+      return PA_ERR_CUDA;
+    cudaError_t row_err;
+    slot = timed ? prof_begin(PA_K_ROW, st) : -1;
+    if (mma_rows) {
       row_err = launch_row_mma_kernel(p, tm_kr, tm_vr, row_ctas, st);
     } else {
       // fp32: whole rows of head_dim elements, no swizzle (CUDA-core kernel)
@@ -808,7 +809,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PA_ERR_CUDA;
       slot = timed ? prof_begin(PA_K_TILE, st) : -1;
-      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vt, num_sms, st);
+      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vr, num_sms, st);
       prof_end(slot, st);
       if (tile_err != cudaSuccess) return PA_ERR_CUDA;
     }

@@ -12,9 +12,9 @@
 // one KV head, GQA-packed so the M = 128 MMA is full and the causal diagonal of
 // a tile is only 128/G positions wide) x one KV split.  Per CTA (2 per SM):
 //   warp 4   TMA producer: Q tile (128-byte swizzled boxes of G heads x 128/G
-//            tokens), then per 64-position KV tile the K and V page boxes
-//            {64 dims x 16 slots} named by the block table (K double-buffered,
-//            V one tile behind K);
+//            tokens), then per 64-position KV tile the K page boxes {64 dims x
+//            16 slots} and the V page boxes {16 slots x all dims} named by the
+//            block table (K double-buffered, V one tile behind K);
 //   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
 //            K=head_dim, bf16 in, fp32 in TMEM) into one of two S buffers,
 //            running a tile ahead of the softmax, then O += P V with P read
@@ -62,8 +62,9 @@ template <int D>
 struct TileCfg {
   static constexpr int NH = D / 64;                 // 128-byte halves of a row
   static constexpr int Q_BYTES = NH * 128 * 128;    // 128 rows x 128 B per half
-  static constexpr int KV_HALF = kBN * 128;         // one half of a K or V tile
+  static constexpr int KV_HALF = kBN * 128;         // one half of a K tile
   static constexpr int KV_BYTES = NH * KV_HALF;
+  static constexpr int V_BOX = NH * kBox * 128;     // one V box: [halves][16 rows][128 B]
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
@@ -198,10 +199,19 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           }
           if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * C::NH * kBox * 128);
           __syncwarp();
-          if (ok)
-            for (int h = 0; h < C::NH; ++h)
-              tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh, pos % bs,
-                          page, full);
+          // K: one box per 64-dim half ([halves][64 rows] for the S product's
+          // uniform row stride); V: one box per 16 slots with both halves
+          // ([16-row boxes][halves]: each K = 16 step of the PV product is one
+          // box), half as many TMA boxes.
+          if (ok) {
+            if (which == 0) {
+              for (int h = 0; h < C::NH; ++h)
+                tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh,
+                            pos % bs, page, full);
+            } else {
+              tma_load_5d(dst + lane * C::V_BOX, map, 0, pos % bs, 0, it.kvh, page, full);
+            }
+          }
 
         }
       }
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           const uint32_t vb = sv + vs * C::KV_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = umma_desc_sw128(vb + kk * 16 * 128, C::KV_HALF, 1024);
+            const uint64_t b = umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
             tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
@@ -385,8 +395,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           for (int e = r; e < nchunks; e += 128) {
             const int h = e / ((kBN - first) * 8);
             const int rem = e % ((kBN - first) * 8);
-            *reinterpret_cast<uint4 *>(vs + h * C::KV_HALF + (first + rem / 8) * 128 + (rem % 8) * 16) =
-                make_uint4(0, 0, 0, 0);
+            const int row = first + rem / 8;
+            *reinterpret_cast<uint4 *>(vs + (row / kBox) * C::V_BOX + h * (kBox * 128) +
+                                       (row % kBox) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
         }
