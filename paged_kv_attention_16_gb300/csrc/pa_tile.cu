@@ -35,19 +35,24 @@
 namespace pa {
 namespace {
 
-constexpr int kBN = 64;            // KV positions per tile
+// KV positions per tile.  64: two CTAs per SM with 256 TMEM columns each.
+// 128 also works: the S product is then an N = 128 MMA (an N = 64 one runs
+// the tensor pipe at about half rate) and one CTA per SM holds two S buffers
+// and O in 512 columns, but with one softmax pipeline per SM instead of two
+// it measured slower (mixed batch 2.00 ms against 1.62 ms).
+constexpr int kBN = 64;
 constexpr int kBox = 16;           // slots per TMA box
 constexpr int kTileThreads = 192;  // 4 softmax warps, 1 producer warp, 1 MMA warp
 constexpr int kKStages = 2;        // K tiles in flight per CTA
 constexpr int kVStages = 2;        // V tiles in flight per CTA
-constexpr int kTileCtasPerSm = 2;  // resident CTAs per SM (grid = SMs x this)
+constexpr int kTileCtasPerSm = kBN == 64 ? 2 : 1;  // resident CTAs per SM (grid = SMs x this)
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
-constexpr uint32_t kTmemCols = 256;
-// Tensor memory (256 columns per CTA, two CTAs per SM): two S buffers of 64
-// fp32 columns; P (64 bf16 per row = 32 columns) is written over the first
-// half of its own S buffer; O after them.
-constexpr uint32_t kTmemS = 0;     // S buffer b: columns [64 b, 64 b + 64)
-constexpr uint32_t kTmemO = 128;   // O: columns [128, 128 + head_dim)
+constexpr uint32_t kTmemCols = kBN == 64 ? 256 : 512;
+// Tensor memory: two S buffers of kBN fp32 columns; P (kBN bf16 per row =
+// kBN / 2 columns) is written over the first half of its own S buffer; O after
+// them.
+constexpr uint32_t kTmemS = 0;        // S buffer b: columns [kBN b, kBN b + kBN)
+constexpr uint32_t kTmemO = 2 * kBN;  // O: columns [2 kBN, 2 kBN + head_dim)
 
 // S buffer b = tile & 1: kSFull0 + b (S product done), kPFull0 + b (P
 // written over it), kODone0 + b (the PV product that read P is done: the
@@ -315,15 +320,14 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
         tc_fence_after();
         float s[kBN];
         if (warp_active) {
-          uint32_t raw0[32], raw1[32];
-          tc_ld32(tmem + lane_off + kTmemS + pb * kBN, raw0);
-          tc_ld32(tmem + lane_off + kTmemS + pb * kBN + 32, raw1);
+          uint32_t raw[kBN];
+#pragma unroll
+          for (int c0 = 0; c0 < kBN; c0 += 32)
+            tc_ld32(tmem + lane_off + kTmemS + pb * kBN + c0,
+                    *reinterpret_cast<uint32_t(*)[32]>(raw + c0));
           tc_wait_ld();
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            s[x] = __uint_as_float(raw0[x]);
-            s[32 + x] = __uint_as_float(raw1[x]);
-          }
+          for (int x = 0; x < kBN; ++x) s[x] = __uint_as_float(raw[x]);
         }
         if (warp_active) {
           // Only tiles that cross a row's bound need the select.
@@ -380,7 +384,10 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
             const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
             pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
           }
-          tc_st32(tmem + lane_off + kTmemS + pb * kBN, pw);
+#pragma unroll
+          for (int c0 = 0; c0 < kBN / 2; c0 += 32)
+            tc_st32(tmem + lane_off + kTmemS + pb * kBN + c0,
+                    *reinterpret_cast<const uint32_t(*)[32]>(pw + c0));
           tc_wait_st();
           l += ((suma[0] + suma[1]) + (suma[2] + suma[3])) + ((suma[4] + suma[5]) + (suma[6] + suma[7]));
         }
