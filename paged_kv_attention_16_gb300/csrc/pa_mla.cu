@@ -319,11 +319,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         // stage the partial scores, then one bulk copy to the peer: the staging
         // and the peer's buffer b are free once the peer has consumed tile g - 2
         if (g >= 2) mbar_wait_cluster(&bar[kXFree0 + b], ((g >> 1) - 1) & 1, dead, a.status);
+        // Row r of the partial scores is 8 float4s; float4 v sits in slot
+        // v ^ (r % 8), so the 8 rows a quarter-warp touches hit 8 different
+        // bank groups (plain rows of 128 bytes all start in the same banks).
         float4 *st4 = reinterpret_cast<float4 *>(sXS + b * X_BYTES + r * kMN * 4);
 #pragma unroll
         for (int v = 0; v < kMN / 4; ++v)
-          st4[v] = make_float4(__uint_as_float(raw[4 * v]), __uint_as_float(raw[4 * v + 1]),
-                               __uint_as_float(raw[4 * v + 2]), __uint_as_float(raw[4 * v + 3]));
+          st4[v ^ (r & 7)] = make_float4(__uint_as_float(raw[4 * v]), __uint_as_float(raw[4 * v + 1]),
+                                         __uint_as_float(raw[4 * v + 2]), __uint_as_float(raw[4 * v + 3]));
         fence_proxy_async();
         named_sync(1, 128);
         if (r == 0) {
@@ -335,7 +338,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         const float4 *xr = reinterpret_cast<const float4 *>(sX + b * X_BYTES + r * kMN * 4);
 #pragma unroll
         for (int v = 0; v < kMN / 4; ++v) {
-          const float4 o4 = xr[v];
+          const float4 o4 = xr[v ^ (r & 7)];
           sc[4 * v] = __uint_as_float(raw[4 * v]) + o4.x;
           sc[4 * v + 1] = __uint_as_float(raw[4 * v + 1]) + o4.y;
           sc[4 * v + 2] = __uint_as_float(raw[4 * v + 2]) + o4.z;
