@@ -545,6 +545,14 @@ __device__ inline void mbar_arrive_remote(uint32_t cluster_addr) {
                : "memory");
 }
 
+// Remote arrive without release semantics: for signalling "my reads of a
+// buffer are done" after a CTA barrier that already orders those reads (a
+// cluster-scope release costs on the order of two thousand cycles here).
+__device__ inline void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
+}
+
 __device__ inline bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(

@@ -345,7 +345,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           sc[4 * v + 3] = __uint_as_float(raw[4 * v + 3]) + o4.w;
         }
         named_sync(1, 128);
-        if (r == 0) mbar_arrive_remote(xfree_peer[b]);
+        // Hand our buffer b back to the peer.  Every thread's reads of it have
+        // returned (their sums are in registers) and the CTA barrier above
+        // orders them before this arrive, so a relaxed arrive suffices; a
+        // cluster-scope release arrive cost about 1.8k cycles a tile.
+        if (r == 0) mbar_arrive_remote_relaxed(xfree_peer[b]);
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kMN; ++c) {
