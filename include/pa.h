@@ -181,7 +181,11 @@ pa_status pa_forward_static_scratch(
  *  block_table, seq_lens as for pa_forward (seq_len >= 1)
  *  out       [num_seqs, num_heads, kv_lora_rank] bf16
  *  Supported: num_heads = 128, kv_lora_rank = 512, rope_dim = 64,
- *  block_size a multiple of 64 (at most 256).
+ *  block_size a multiple of 32 (at most 256).
+ *  kv_split_tokens: 0 = automatic; otherwise the KV positions per work item,
+ *  a multiple of 32 (the kernel's tile: a tile never crosses a page).
+ *  Errors as for pa_forward; PA_ERR_UNSUPPORTED for other shapes or a
+ *  kv_split_tokens that is not a multiple of 32.
  */
 pa_status pa_mla_decode(const void *q, const void *kv_cache,
                         const int32_t *block_table, const int32_t *seq_lens,

@@ -92,6 +92,26 @@ def test_forced_splits_match_oracle(kvs):
     parity.compare(got, parity.oracle_forward(b), "bf16", what=f"kvs {kvs}")
 
 
+@pytest.mark.parametrize("kvs", [0, 64])
+def test_more_requests_than_one_planner_block(kvs):
+    """1500 requests (the planner and the merge kernel keep up to 1024
+    requests in shared memory; beyond that they read the lists from global
+    memory): mostly decodes, some extends, a few long contexts whose rows
+    have more than 32 splits at kv_split_tokens = 64."""
+    rng = np.random.default_rng(1500 + kvs)
+    n = 1500
+    q_lens = [1] * n
+    ctx = [int(x) for x in rng.integers(1, 300, n)]
+    for i in range(0, n, 97):  # extends
+        q_lens[i] = int(rng.integers(2, 40))
+        ctx[i] = q_lens[i] + int(rng.integers(0, 200))
+    for i in (5, 700, 1499):  # long rows
+        q_lens[i], ctx[i] = 1, 3000
+    b = inputs.paged_batch(q_lens, ctx, 16, 4, 128, 16, dtype="bf16", seed=1500 + kvs)
+    got = parity.gpu_forward(b, kv_split_tokens=kvs)
+    parity.compare(got, parity.oracle_forward(b), "bf16", what=f"1500 requests kvs {kvs}")
+
+
 # --------------------------------------------------------------------------
 # edge cases
 # --------------------------------------------------------------------------

@@ -87,3 +87,14 @@ def test_mla_graph_replay():
     assert pa.pa_get_device_status() == 0
     parity.compare(out.float().cpu().numpy().astype(np.float64), parity.oracle_mla(m), "bf16",
                    what="mla graph replay")
+
+
+def test_mla_split_not_multiple_of_32_is_refused():
+    """A KV split must start on a 32-position tile (tiles never cross a page)."""
+    m = pa.to_device(inputs.mla_batch([300, 65], seed=5))
+    out = torch.empty((m.num_seqs, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16,
+                      device="cuda")
+    st = pa.pa_mla_decode(m.q, m.kv_cache, m.block_table, m.seq_lens, m.num_heads,
+                          m.kv_lora_rank, m.rope_dim, m.block_size, m.scale, out,
+                          max_seq_len=m.max_seq_len, kv_split_tokens=48, check=False)
+    assert st == pa.PA_ERR_UNSUPPORTED
