@@ -175,3 +175,51 @@ def gather_rows(k_cache, block_table, seq_lens, block_size, max_seq_len):
                                   _ptr(bt, _I32P), _ptr(sl, _I32P), S, int(bt.shape[1]), nb,
                                   block_size, int(max_seq_len), dense.ctypes.data))
     return dense
+
+
+# Status bits, as the library's device status word defines them.
+DEV_BAD_BLOCK, DEV_BAD_QLEN, DEV_BAD_QSL = 0x1, 0x2, 0x8
+
+
+def cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                block_size):
+    """The paged KV-cache write that precedes attention ("vLLM Triton attention
+    backend deep dive", section "Technical implementation of paged
+    attention": the cache is a pool of fixed-size blocks, and a sequence's
+    block table maps its logical block j to a physical block).
+
+    For request s with q_len = qsl[s+1] - qsl[s] new tokens on a context of
+    seq_lens[s] positions (the new tokens included), new token i sits at
+    position pos = seq_lens[s] - q_len + i, in physical block
+    block_table[s][pos // block_size] at slot pos % block_size; its K and V
+    rows ([num_kv_heads, head_dim] each) are copied there.
+
+    k_new, v_new: [T, Hk, D]; k_cache, v_cache: [num_blocks, block_size, Hk, D]
+    (any one dtype: values are copied, not converted).  Returns the two new
+    caches (copies) and the status bits: a request with q_len > seq_len is
+    skipped (DEV_BAD_QLEN); a token whose block id is outside the pool is
+    skipped (DEV_BAD_BLOCK); a query_start_loc that does not start at 0,
+    decreases, or does not end at T writes nothing (DEV_BAD_QSL)."""
+    k_out, v_out = k_cache.copy(), v_cache.copy()
+    qsl = [int(x) for x in query_start_loc]
+    S, T = len(seq_lens), k_new.shape[0]
+    nb = k_cache.shape[0]
+    if qsl[0] != 0 or qsl[S] != T or any(qsl[s + 1] < qsl[s] for s in range(S)):
+        return k_out, v_out, DEV_BAD_QSL
+    status = 0
+    for s in range(S):
+        q_len = qsl[s + 1] - qsl[s]
+        prefix = int(seq_lens[s]) - q_len
+        if prefix < 0:
+            status |= DEV_BAD_QLEN
+            continue
+        for i in range(q_len):
+            pos = prefix + i
+            lp = pos // block_size
+            page = int(block_table[s][lp]) if lp < block_table.shape[1] else -1
+            if page < 0 or page >= nb:
+                status |= DEV_BAD_BLOCK
+                continue
+            k_out[page, pos % block_size] = k_new[qsl[s] + i]
+            v_out[page, pos % block_size] = v_new[qsl[s] + i]
+    return k_out, v_out, status
