@@ -272,6 +272,23 @@ def secondary_workloads(pa, flush, peaks):
                              "tensor_frac": tf / tfl}
     else:
         res["mla_decode"] = {"unavailable": pa.status_string(st)}
+    del m, out
+
+    # KV-cache write of a prefill-sized step: 16 requests x 512 new tokens
+    # (Llama-3.1-8B shapes); bytes = K and V rows read and written
+    hb = inputs.paged_batch([512] * 16, [1024 + 256 * i for i in range(16)], 32, 8, 128, 16,
+                            dtype="bf16", seed=5, poison=False)
+    b = pa.to_device(hb)
+    g = torch.Generator().manual_seed(5)
+    k_new = torch.randn((hb.num_tokens, 8, 128), generator=g).to(torch.bfloat16).cuda()
+    v_new = torch.randn((hb.num_tokens, 8, 128), generator=g).to(torch.bfloat16).cuda()
+    wr = lambda: pa.pa_cache_write(k_new, v_new, b.k_cache, b.v_cache, b.block_table,  # noqa: E731
+                                   b.seq_lens, b.query_start_loc, hb.block_size)
+    wr()
+    ms = time_per_step(wr, 50, flush)
+    nbytes = 2 * 2 * k_new.numel() * k_new.element_size()
+    res["cache_write"] = {"ms": ms, "gbs": nbytes / ms / 1e6, "hbm_frac": nbytes / ms / 1e6 / hbm,
+                          "tokens": hb.num_tokens, "bytes": nbytes}
     return res
 
 

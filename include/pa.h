@@ -220,6 +220,43 @@ const char *pa_status_string(pa_status status);
 int pa_num_sms(void);
 
 /*
+ * pa_cache_write -- the paged KV-cache write that precedes pa_forward ("vLLM
+ * Triton attention backend deep dive", section "Technical implementation of
+ * paged attention": the cache is a pool of fixed-size blocks and a sequence's
+ * block table maps its logical block j to a physical block).  New token i of
+ * request s (q_len_s = qsl[s+1] - qsl[s] new tokens, seq_lens[s] positions
+ * including them) sits at position pos = seq_lens[s] - q_len_s + i; its K and
+ * V rows are copied, bit for bit, to slot pos % block_size of physical block
+ * block_table[s][pos / block_size]:
+ *
+ *  k_new, v_new     [num_tokens, num_kv_heads, head_dim]            dtype
+ *  k_cache, v_cache [num_blocks, block_size, num_kv_heads, head_dim] dtype,
+ *                   written in place; every other slot is left untouched
+ *  block_table, seq_lens, query_start_loc: as for pa_forward (seq_lens are
+ *                   the lengths after this write)
+ *  head_dim x element size a multiple of 16 bytes; any block_size >= 1
+ *
+ * Asynchronous on `stream`, allocation-free after the first call on a device
+ * (it uses 256 bytes of the library workspace), graph-capturable.  Bad device
+ * metadata never traps (status bits as for pa_forward):
+ *   PA_DEV_BAD_QSL    query_start_loc[0] != 0, decreasing, or
+ *                     query_start_loc[num_seqs] != num_tokens: nothing written
+ *   PA_DEV_BAD_QLEN   q_len > seq_len: that request's rows are not written
+ *   PA_DEV_BAD_BLOCK  a block id outside [0, num_blocks) (or past
+ *                     max_blocks_per_seq): that token's rows are not written
+ * Errors: PA_ERR_INVALID_ARG for null pointers with num_tokens > 0, negative
+ * sizes, num_seqs == 0 with num_tokens > 0, or tensors not 16-byte aligned;
+ * PA_ERR_UNSUPPORTED when a row is not a multiple of 16 bytes; PA_ERR_CUDA
+ * when a launch fails.  num_tokens == 0 launches nothing.
+ */
+pa_status pa_cache_write(const void *k_new, const void *v_new, void *k_cache,
+                         void *v_cache, const int32_t *block_table,
+                         const int32_t *seq_lens, const int32_t *query_start_loc,
+                         int num_kv_heads, int head_dim, int block_size,
+                         void *stream, pa_dtype dtype, int num_seqs,
+                         int num_tokens, int max_blocks_per_seq, int num_blocks);
+
+/*
  * pa_debug_gather -- the page-gather indexing alone, for bit-exact tests:
  *   dense_out[s][j][:] = k_cache[block_table[s][j / bs]][j % bs][0:row_elems]
  * for j < seq_lens[s] (raw element bits copied, elem_bytes 2 or 4); positions

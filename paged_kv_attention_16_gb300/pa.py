@@ -25,7 +25,7 @@ PA_DEV_OVERFLOW = 0x10
 PA_DEV_TIMEOUT = 0x20
 
 # Every entry point declared in include/pa.h.
-EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode",
+EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cache_write",
            "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
            "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch")
@@ -68,6 +68,9 @@ def lib():
         L.pa_status_string.restype = ctypes.c_char_p
         L.pa_num_sms.argtypes = []
         L.pa_num_sms.restype = c_int
+        L.pa_cache_write.argtypes = [vp, vp, vp, vp, i32p, i32p, i32p, c_int, c_int, c_int, vp,
+                                     c_int, c_int, c_int, c_int, c_int]
+        L.pa_cache_write.restype = c_int
         L.pa_debug_gather.argtypes = [vp, i32p, i32p, c_int, c_int, c_int, c_int, c_int, c_int,
                                       c_int, vp, vp]
         L.pa_debug_gather.restype = c_int
@@ -213,6 +216,21 @@ def pa_kernel_name(kernel_id):
 
 def pa_num_sms():
     return int(lib().pa_num_sms())
+
+
+def pa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
+                   block_size, stream=None, check=True):
+    """pa_cache_write on torch tensors: k_new/v_new [T, Hk, D], caches
+    [num_blocks, block_size, Hk, D] (written in place)."""
+    dt = PA_BF16 if k_new.dtype == torch.bfloat16 else PA_F32
+    st = lib().pa_cache_write(
+        _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
+        _ptr(seq_lens), _ptr(query_start_loc), int(k_new.shape[1]), int(k_new.shape[2]),
+        int(block_size), _stream_ptr(stream), dt, int(seq_lens.shape[0]), int(k_new.shape[0]),
+        int(block_table.shape[1]), int(k_cache.shape[0]))
+    if check:
+        _check(st, "pa_cache_write")
+    return st
 
 
 def pa_debug_gather(k_cache, block_table, seq_lens, block_size, max_seq_len, dense_out,

@@ -78,3 +78,25 @@ def test_workspace_bytes_grow_with_splits(lib):
     small = f(1, 64, 64, 32, 8, 128, 8192, 0)
     big = f(1, 64, 64, 32, 8, 128, 131072, 0)
     assert 0 < small < big
+
+
+def _cache_write(lib, **kw):
+    args = dict(kn=1 << 20, vn=1 << 20, kc=1 << 20, vc=1 << 20, bt=1 << 20, sl=1 << 20,
+                qsl=1 << 20, Hk=2, D=128, bs=16, stream=None, dtype=1, S=1, T=1, mbps=4, nb=4)
+    args.update(kw)
+    f = lib.pa_cache_write
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [vp] * 7 + [ctypes.c_int] * 3 + [vp] + [ctypes.c_int] * 5
+    a = args
+    return f(a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["sl"], a["qsl"], a["Hk"], a["D"],
+             a["bs"], a["stream"], a["dtype"], a["S"], a["T"], a["mbps"], a["nb"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(Hk=0), 1), (dict(D=-1), 1), (dict(bs=0), 1), (dict(S=-1), 1), (dict(dtype=5), 1),
+    (dict(D=4), 2), (dict(D=6, dtype=0), 2), (dict(T=0), 0), (dict(kn=0), 1), (dict(S=0), 1),
+    (dict(kc=(1 << 20) + 8), 1), (dict(nb=0), 1),
+])
+def test_cache_write_host_argument_checks(lib, kw, want):
+    assert _cache_write(lib, **kw) == want
