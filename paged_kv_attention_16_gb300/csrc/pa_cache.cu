@@ -11,8 +11,9 @@
 //  * a one-block check of query_start_loc (starts at 0, non-decreasing, ends
 //    at num_tokens), which leaves a flag in the library workspace: a bad
 //    query_start_loc writes nothing;
-//  * the copy, launched programmatically after the check: one warp per (new
-//    token, KV head) row; the token's request by binary search over
+//  * the copy, launched programmatically after the check: min(32, row bytes /
+//    16) lanes per (new token, KV head) row, several rows per warp when
+//    they are short; the token's request by binary search over
 //    query_start_loc, its slot through the block table, then the K and the V
 //    row copied with 16-byte vector accesses.  HBM-bound: it reads and writes
 //    2 x num_tokens x num_kv_heads x head_dim elements.
@@ -51,12 +52,17 @@ __global__ void __launch_bounds__(kCheckThreads) cache_check_kernel(const CacheW
 __global__ void __launch_bounds__(kCopyThreads) cache_copy_kernel(const CacheWriteArgs a) {
   pdl_wait();  // the check
   if (!*a.qsl_ok) return;
-  const int lane = threadIdx.x & 31;
+  // A row takes min(32, row_bytes / 16) lanes; a warp moves 32 / that rows
+  // at once (two 256-byte bf16 rows, four 128-byte ones).
+  const int lpr = min(32, a.row_bytes / 16);
+  const int rpw = 32 / lpr;
+  const int lane = (threadIdx.x & 31) % lpr, sub = (threadIdx.x & 31) / lpr;
+  if (sub >= rpw) return;  // lanes left over when lpr does not divide 32
   const long long gw = ((long long)blockIdx.x * kCopyThreads + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * kCopyThreads) >> 5;
   const long long nrows = (long long)a.num_tokens * a.num_kv_heads;
   const int S = a.num_seqs, bs = a.block_size;
-  for (long long row = gw; row < nrows; row += nw) {
+  for (long long row = gw * rpw + sub; row < nrows; row += nw * rpw) {
     const int t = (int)(row / a.num_kv_heads), h = (int)(row % a.num_kv_heads);
     // the request: the last s with qsl[s] <= t (qsl checked non-decreasing)
     int lo = 0, hi = S - 1;
@@ -82,7 +88,7 @@ __global__ void __launch_bounds__(kCopyThreads) cache_copy_kernel(const CacheWri
     }
     const size_t src = ((size_t)t * a.num_kv_heads + h) * a.row_bytes;
     const size_t dst = (((size_t)page * bs + pos % bs) * a.num_kv_heads + h) * a.row_bytes;
-    for (int c = lane * 16; c < a.row_bytes; c += 32 * 16) {
+    for (int c = lane * 16; c < a.row_bytes; c += lpr * 16) {
       const uint4 kv = *reinterpret_cast<const uint4 *>(a.k_new + src + c);
       const uint4 vv = *reinterpret_cast<const uint4 *>(a.v_new + src + c);
       *reinterpret_cast<uint4 *>(a.k_cache + dst + c) = kv;
@@ -140,9 +146,12 @@ extern "C" pa_status pa_cache_write(const void *k_new, const void *v_new, void *
   a.status = status;
   if (launch_dependent(cache_check_kernel, dim3(1), dim3(kCheckThreads), 0, st, a) != cudaSuccess)
     return PA_ERR_CUDA;
+  // enough warps for every row (many copies in flight), at most 32 blocks per SM
+  const int lpr = (head_dim * es / 16) < 32 ? head_dim * es / 16 : 32;
   const long long rows = (long long)num_tokens * num_kv_heads;
-  long long blocks = (rows + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
-  if (blocks > (long long)num_sms * 8) blocks = (long long)num_sms * 8;
+  const long long warps = (rows + (32 / lpr) - 1) / (32 / lpr);
+  long long blocks = (warps + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  if (blocks > (long long)num_sms * 32) blocks = (long long)num_sms * 32;
   if (launch_dependent(cache_copy_kernel, dim3((unsigned)blocks), dim3(kCopyThreads), 0, st, a) !=
       cudaSuccess)
     return PA_ERR_CUDA;
