@@ -83,13 +83,21 @@ def _check(rc):
 
 def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
                     num_heads, num_kv_heads, head_dim, block_size, scale,
-                    rows=None, kv_window=None, lib=None, with_lse=False):
+                    rows=None, kv_window=None, lib=None, with_lse=False, sinks=None):
     """fp64 unified paged attention.  Shapes:
     q [T, H, D]; k_cache, v_cache [num_blocks, block_size, Hk, D];
     block_table [S, max_blocks]; seq_lens [S]; query_start_loc [S+1].
     rows: optional int64 array of flat (token * H + head) indices to compute;
     rows not listed come back as NaN.  kv_window=(lo, hi) restricts every
     request to KV positions in [lo, hi) (used to form split-KV partials).
+    sinks: optional [H] sink logits ("vLLM Triton attention backend deep
+    dive", section "Usage scenarios": sink tokens are one of the model
+    features the unified backend supports): head h's softmax denominator
+    gains exp(sinks[h]) while the sink contributes no value, so
+      out = sum_j exp(s_j) v_j / (sum_j exp(s_j) + exp(sinks[h]))
+          = out_keys / (1 + exp(sinks[h] - lse)),
+    lse = log sum_j exp(s_j) over the row's visible keys (s_j = scale q.k_j).
+    The returned lse stays that of the keys alone.
     Returns out [T, H, D] float64 (and lse [T, H] when with_lse)."""
     lib = lib or _lib()
     q = np.ascontiguousarray(q)
@@ -118,6 +126,9 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
         float(scale), int(lo), int(hi), rows_p, nrows, _ptr(out, _F64P),
         _ptr(lse, _F64P))
     _check(rc)
+    if sinks is not None:
+        sk = np.asarray(sinks, dtype=np.float64).reshape(1, num_heads)
+        out = out / (1.0 + np.exp(sk - lse))[:, :, None]
     return (out, lse) if with_lse else out
 
 
