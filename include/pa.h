@@ -113,6 +113,35 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
                      int num_seqs, int num_tokens, int max_blocks_per_seq,
                      int num_blocks, int max_seq_len, int kv_split_tokens);
 
+/*
+ * pa_forward_ex -- pa_forward with per-call options.
+ *
+ * Arguments: those of pa_forward, plus `options` (host pointer, read during
+ * the call only; NULL = pa_forward exactly).  Options:
+ *   sinks  device array of num_heads fp32 sink logits in natural-log units,
+ *          or NULL.  "vLLM Triton attention backend deep dive", section
+ *          "Usage scenarios", lists sink tokens among the model features of
+ *          the unified backend: head h's softmax denominator gains
+ *          exp(sinks[h]) while the sink adds no value row, so
+ *            out = sum_j exp(s_j) v_j / (sum_j exp(s_j) + exp(sinks[h])).
+ *          Owned by the caller; must stay valid until the call's kernels
+ *          have run; 4-byte aligned (PA_ERR_INVALID_ARG otherwise).  A row
+ *          with no visible key returns zeros.  pa_mla_decode takes no sinks.
+ * Errors as for pa_forward.
+ */
+typedef struct {
+  const float *sinks;
+} pa_forward_options;
+
+pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        const int32_t *query_start_loc, int num_heads,
+                        int num_kv_heads, int head_dim, int block_size,
+                        float scale, void *out, void *stream, pa_dtype dtype,
+                        int num_seqs, int num_tokens, int max_blocks_per_seq,
+                        int num_blocks, int max_seq_len, int kv_split_tokens,
+                        const pa_forward_options *options);
+
 /* Workspace bytes pa_forward needs for these host-known extents. */
 size_t pa_forward_workspace_bytes(pa_dtype dtype, int num_seqs, int num_tokens,
                                   int num_heads, int num_kv_heads,

@@ -342,10 +342,14 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
       M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       bad |= __shfl_xor_sync(0xffffffffu, bad, o);
     }
+    // a sink joins the max and the denominator once, with no value
+    const float sink2 = p.sinks ? __ldg(p.sinks + mr.h) * kLog2eF : -INFINITY;
+    M = fmaxf(M, sink2);
     const float w_own = (lane < mr.nn && !bad) ? fast_exp2(lse - M) : 0.f;
     float L = w_own;
 #pragma unroll
     for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (p.sinks) L += fast_exp2(sink2 - M);
     // partial rows in groups of 8: the loads of a group are independent
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const float *src0 = p.part_o + (size_t)mr.base * D + lane * dpl;
@@ -410,6 +414,9 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
       M = fmaxf(M, s_m[w]);
       bad |= s_bad[w];
     }
+    // a sink joins the max and the denominator once, with no value
+    const float sink2 = p.sinks ? __ldg(p.sinks + mr.h) * kLog2eF : -INFINITY;
+    M = fmaxf(M, sink2);
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float wl = 0.f;
     if (!bad && M != -INFINITY) {
@@ -440,6 +447,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
         a += s_red[w][tid];
         L += s_wl[w];
       }
+      if (p.sinks) L += fast_exp2(sink2 - M);
       const float v = (bad || !(L > 0.f)) ? 0.f : a / L;
       store_out<T>(out + ((size_t)mr.tok * H + mr.h) * D + tid, v);
     }
@@ -734,6 +742,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.part_lse = reinterpret_cast<float *>(ws + lay.part_lse);
   p.part_cap = lay.part_cap;
   p.status = status;
+  p.sinks = c.sinks;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
   // One thread per request, whole warps, at most kPlanThreads: small batches
@@ -921,9 +930,27 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
                      int head_dim, int block_size, float scale, void *out, void *stream,
                      pa_dtype dtype, int num_seqs, int num_tokens, int max_blocks_per_seq,
                      int num_blocks, int max_seq_len, int kv_split_tokens) {
-  const FwdCall c{q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
-                  num_kv_heads, head_dim, block_size, scale, out, dtype, num_seqs, num_tokens,
-                  max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens};
+  return pa_forward_ex(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
+                       num_kv_heads, head_dim, block_size, scale, out, stream, dtype, num_seqs,
+                       num_tokens, max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens,
+                       nullptr);
+}
+
+pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_table, const int32_t *seq_lens,
+                        const int32_t *query_start_loc, int num_heads, int num_kv_heads,
+                        int head_dim, int block_size, float scale, void *out, void *stream,
+                        pa_dtype dtype, int num_seqs, int num_tokens, int max_blocks_per_seq,
+                        int num_blocks, int max_seq_len, int kv_split_tokens,
+                        const pa_forward_options *options) {
+  FwdCall c{q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
+            num_kv_heads, head_dim, block_size, scale, out, dtype, num_seqs, num_tokens,
+            max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens};
+  if (options) {
+    if (options->sinks && (reinterpret_cast<uintptr_t>(options->sinks) & 3))
+      return PA_ERR_INVALID_ARG;
+    c.sinks = options->sinks;
+  }
   pa_status s = fwd_check(c);
   if (s != PA_OK || num_tokens == 0) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);

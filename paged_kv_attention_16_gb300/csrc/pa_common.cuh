@@ -83,7 +83,19 @@ struct FwdParams {
   float *part_lse;          // [part_cap] (base-2 log-sum-exp; NaN marks a bad split)
   long long part_cap;
   unsigned int *status;
+  const float *sinks;       // [num_heads] sink logits (natural-log units) or null
 };
+
+constexpr float kLog2eF = 1.4426950408889634f;
+
+// Attention sinks ("vLLM Triton attention backend deep dive", section "Usage
+// scenarios": sink tokens): head h's softmax denominator gains exp(sink_h),
+// and the sink carries no value.  With a row's keys reduced to (m, l) in the
+// base-2 domain (l = sum 2^(s - m)), the reciprocal of the full denominator.
+__device__ inline float sink_inv(const float *sinks, int head, float m, float l) {
+  const float den = sinks ? l + exp2f(__ldg(sinks + head) * kLog2eF - m) : l;
+  return den > 0.f ? 1.f / den : 0.f;
+}
 
 // Largest split length of the row kernel (bounds its per-item page list).
 constexpr int kRowMaxSplit = 8192;

@@ -434,9 +434,10 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
       if (d.direct) {
+        const float dinv = sink_inv(p.sinks, kvh * G + h, M, L);  // the row's own output
         T *dst = reinterpret_cast<T *>(p.out) + ((size_t)d.tok * H + kvh * G + h) * D + d0;
 #pragma unroll
-        for (int x = 0; x < C::OPT; ++x) store_elem(dst + x, acc[x] * inv);
+        for (int x = 0; x < C::OPT; ++x) store_elem(dst + x, acc[x] * dinv);
       } else {
         const long long prow = d.prow0 + (long long)h * d.nsplit;
 #pragma unroll

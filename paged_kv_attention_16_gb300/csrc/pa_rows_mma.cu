@@ -464,10 +464,11 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       }
       const float inv = L > 0.f ? 1.f / L : 0.f;
       if (d.direct) {
+        const float dinv = sink_inv(p.sinks, kvh * G + h, M, L);  // the row's own output
         __nv_bfloat16 *dst =
             reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)d.tok * H + kvh * G + h) * D + d0;
 #pragma unroll
-        for (int x = 0; x < C::OPT; ++x) dst[x] = __float2bfloat16_rn(acc[x] * inv);
+        for (int x = 0; x < C::OPT; ++x) dst[x] = __float2bfloat16_rn(acc[x] * dinv);
       } else {
         const long long prow = d.prow0 + (long long)h * d.nsplit;
 #pragma unroll

@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       tc_fence_after();
       const bool write = row_valid && row_hi > it.kv_lo;
       const bool direct = ceil_div_ll(row_hi_full, it.split_len) == 1;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+      // partials are normalised by their own l; a row's own output also
+      // counts its head's sink
+      const float inv = direct ? sink_inv(p.sinks, head, m, l) : (l > 0.f ? 1.f / l : 0.f);
       const uint32_t keep = item_bad ? 0u : 0xffffffffu;  // bad items write exact zeros
       const size_t tok = (size_t)it.q_start + i;
       const long long prow = it.partial_base + ((long long)i * H + head) * it.nsplit + it.split;

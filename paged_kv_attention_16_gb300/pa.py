@@ -28,8 +28,14 @@ PA_DEV_TIMEOUT = 0x20
 EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cache_write",
            "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
-           "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch")
+           "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch", "pa_forward_ex")
 PA_K_COUNT = 8
+
+
+class ForwardOptions(ctypes.Structure):
+    """pa_forward_options: sinks = device pointer to [num_heads] fp32 sink
+    logits, or None."""
+    _fields_ = [("sinks", ctypes.c_void_p)]
 
 
 class PaError(RuntimeError):
@@ -80,6 +86,8 @@ def lib():
         L.pa_profile_read.restype = c_int
         L.pa_forward_static_scratch.argtypes = L.pa_forward.argtypes + [vp]
         L.pa_forward_static_scratch.restype = c_int
+        L.pa_forward_ex.argtypes = L.pa_forward.argtypes + [ctypes.POINTER(ForwardOptions)]
+        L.pa_forward_ex.restype = c_int
         L.pa_kernel_name.argtypes = [c_int]
         L.pa_kernel_name.restype = ctypes.c_char_p
         _lib = L
@@ -121,18 +129,28 @@ def _check(status, where):
 
 def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
                num_kv_heads, head_dim, block_size, scale, out, stream=None, *, max_seq_len,
-               kv_split_tokens=0, num_blocks=None, check=True):
+               kv_split_tokens=0, num_blocks=None, sinks=None, check=True):
     """Unified paged attention (see include/pa.h).  Shapes are read from the
-    tensors; max_seq_len is the host-known bound on seq_lens."""
-    st = lib().pa_forward(
+    tensors; max_seq_len is the host-known bound on seq_lens.  sinks: an
+    optional fp32 device tensor of num_heads sink logits, passed through
+    pa_forward_ex."""
+    args = (
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(query_start_loc), int(num_heads), int(num_kv_heads), int(head_dim),
         int(block_size), float(scale), _ptr(out), _stream_ptr(stream), _dtype_code(q),
         int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
         int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
         int(kv_split_tokens))
+    if sinks is None:
+        st, where = lib().pa_forward(*args), "pa_forward"
+    else:
+        if isinstance(sinks, torch.Tensor) and (sinks.dtype != torch.float32
+                                                or sinks.numel() != num_heads):
+            raise TypeError("sinks must be a float32 tensor of num_heads elements")
+        opts = ForwardOptions(_ptr(sinks))
+        st, where = lib().pa_forward_ex(*args, ctypes.byref(opts)), "pa_forward_ex"
     if check:
-        _check(st, "pa_forward")
+        _check(st, where)
     return st
 
 
@@ -258,14 +276,16 @@ def to_device(batch, device="cuda"):
     return type(batch)(**fields)
 
 
-def forward(b, out=None, stream=None, kv_split_tokens=None):
-    """pa_forward on a device-resident PagedBatch; returns `out`."""
+def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None):
+    """pa_forward on a device-resident PagedBatch (pa_forward_ex when sinks,
+    an fp32 device tensor of num_heads logits, is given); returns `out`."""
     if out is None:
         out = torch.empty_like(b.q)
     pa_forward(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc,
                b.num_heads, b.num_kv_heads, b.head_dim, b.block_size, b.scale, out, stream,
                max_seq_len=b.max_seq_len,
-               kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens)
+               kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens,
+               sinks=sinks)
     return out
 
 

@@ -11,12 +11,12 @@ from paged_kv_attention_16_gb300 import inputs, pa
 TOL = {"f32": dict(max_abs=1e-4, mean_abs=1e-4), "bf16": dict(max_abs=2e-2, mean_abs=2e-3)}
 
 
-def oracle_forward(b, rows=None):
+def oracle_forward(b, rows=None, sinks=None):
     return orc.paged_attention(
         inputs.storage_array(b.q), inputs.storage_array(b.k_cache),
         inputs.storage_array(b.v_cache), b.block_table.numpy(), b.seq_lens.numpy(),
         b.query_start_loc.numpy(), b.num_heads, b.num_kv_heads, b.head_dim, b.block_size,
-        b.scale, rows=rows)
+        b.scale, rows=rows, sinks=None if sinks is None else np.asarray(sinks, np.float64))
 
 
 def oracle_mla(b, rows=None):
@@ -25,9 +25,11 @@ def oracle_mla(b, rows=None):
                           b.block_size, b.scale, rows=rows)
 
 
-def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0):
+def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0, sinks=None):
     d = pa.to_device(b)
-    got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens)
+    if sinks is not None:
+        sinks = torch.as_tensor(sinks, dtype=torch.float32).cuda()
+    got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens, sinks=sinks)
     status = pa.pa_get_device_status()
     assert status == expect_status, f"device status {status:#x}, expected {expect_status:#x}"
     return got.float().cpu().numpy().astype(np.float64)

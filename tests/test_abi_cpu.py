@@ -100,3 +100,37 @@ def _cache_write(lib, **kw):
 ])
 def test_cache_write_host_argument_checks(lib, kw, want):
     assert _cache_write(lib, **kw) == want
+
+
+class _Options(ctypes.Structure):
+    _fields_ = [("sinks", ctypes.c_void_p)]
+
+
+def _forward_ex(lib, options, **kw):
+    args = dict(q=1 << 20, k=1 << 20, v=1 << 20, bt=1 << 20, sl=1 << 20, qsl=1 << 20, H=8, Hk=2,
+                D=128, bs=16, scale=0.1, out=1 << 20, stream=None, dtype=1, S=1, T=1, mbps=4,
+                nb=4, msl=64, kvs=0)
+    args.update(kw)
+    f = lib.pa_forward_ex
+    f.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    f.argtypes = [vp, vp, vp, vp, vp, vp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                  ctypes.c_float, vp, vp] + [ctypes.c_int] * 7 + [ctypes.POINTER(_Options)]
+    a = args
+    return f(a["q"], a["k"], a["v"], a["bt"], a["sl"], a["qsl"], a["H"], a["Hk"], a["D"], a["bs"],
+             a["scale"], a["out"], a["stream"], a["dtype"], a["S"], a["T"], a["mbps"], a["nb"],
+             a["msl"], a["kvs"], options)
+
+
+@pytest.mark.parametrize("sinks,kw,want", [
+    (None, dict(H=0), 1),              # the checks of pa_forward still apply
+    (None, dict(D=96), 2),
+    (1 << 20, dict(T=0), 0),           # nothing to do: no launch
+    ((1 << 20) + 2, dict(T=0), 1),     # a sinks array that is not 4-byte aligned
+    ((1 << 20) + 2, dict(), 1),
+])
+def test_forward_ex_host_argument_checks(lib, sinks, kw, want):
+    opts = _Options(sinks)
+    assert _forward_ex(lib, ctypes.byref(opts), **kw) == want
+    if sinks is None:
+        assert _forward_ex(lib, None, **kw) == want  # null options: pa_forward
