@@ -81,9 +81,24 @@ def _check(rc):
         raise OracleError(_ERR.get(rc, f"oracle error {rc}"))
 
 
+def nhd_view(cache, kv_layout):
+    """A paged cache seen as [num_blocks, block_size, Hk, D] (a numpy view,
+    writes go through).  kv_layout "nhd" stores it that way; "hnd" stores
+    [num_blocks, Hk, block_size, D], i.e. element (page, slot, head, d) at
+    flat offset ((page * Hk + head) * block_size + slot) * D + d ("vLLM AMD
+    ROCm attention backend optimisation", section "ROCM_AITER_FA": a KV cache
+    laid out for the hardware's access pattern)."""
+    if kv_layout == "nhd":
+        return cache
+    if kv_layout == "hnd":
+        return cache.transpose(0, 2, 1, 3)
+    raise ValueError(kv_layout)
+
+
 def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
                     num_heads, num_kv_heads, head_dim, block_size, scale,
-                    rows=None, kv_window=None, lib=None, with_lse=False, sinks=None):
+                    rows=None, kv_window=None, lib=None, with_lse=False, sinks=None,
+                    kv_layout="nhd"):
     """fp64 unified paged attention.  Shapes:
     q [T, H, D]; k_cache, v_cache [num_blocks, block_size, Hk, D];
     block_table [S, max_blocks]; seq_lens [S]; query_start_loc [S+1].
@@ -98,11 +113,12 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
           = out_keys / (1 + exp(sinks[h] - lse)),
     lse = log sum_j exp(s_j) over the row's visible keys (s_j = scale q.k_j).
     The returned lse stays that of the keys alone.
+    kv_layout: "nhd" or "hnd" storage of the caches (see nhd_view).
     Returns out [T, H, D] float64 (and lse [T, H] when with_lse)."""
     lib = lib or _lib()
     q = np.ascontiguousarray(q)
-    k_cache = np.ascontiguousarray(k_cache)
-    v_cache = np.ascontiguousarray(v_cache)
+    k_cache = np.ascontiguousarray(nhd_view(k_cache, kv_layout))
+    v_cache = np.ascontiguousarray(nhd_view(v_cache, kv_layout))
     dt = _dtype_code(q)
     assert _dtype_code(k_cache) == dt and _dtype_code(v_cache) == dt
     bt = _i32(block_table)
@@ -193,7 +209,7 @@ DEV_BAD_BLOCK, DEV_BAD_QLEN, DEV_BAD_QSL = 0x1, 0x2, 0x8
 
 
 def cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
-                block_size):
+                block_size, kv_layout="nhd"):
     """The paged KV-cache write that precedes attention ("vLLM Triton attention
     backend deep dive", section "Technical implementation of paged
     attention": the cache is a pool of fixed-size blocks, and a sequence's
@@ -210,13 +226,16 @@ def cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_sta
     caches (copies) and the status bits: a request with q_len > seq_len is
     skipped (DEV_BAD_QLEN); a token whose block id is outside the pool is
     skipped (DEV_BAD_BLOCK); a query_start_loc that does not start at 0,
-    decreases, or does not end at T writes nothing (DEV_BAD_QSL)."""
-    k_out, v_out = k_cache.copy(), v_cache.copy()
+    decreases, or does not end at T writes nothing (DEV_BAD_QSL).
+    kv_layout "hnd": the caches are stored [num_blocks, Hk, block_size, D]
+    (see nhd_view); the same rows land in that storage."""
+    k_store, v_store = k_cache.copy(), v_cache.copy()
+    k_out, v_out = nhd_view(k_store, kv_layout), nhd_view(v_store, kv_layout)
     qsl = [int(x) for x in query_start_loc]
     S, T = len(seq_lens), k_new.shape[0]
-    nb = k_cache.shape[0]
+    nb = k_out.shape[0]
     if qsl[0] != 0 or qsl[S] != T or any(qsl[s + 1] < qsl[s] for s in range(S)):
-        return k_out, v_out, DEV_BAD_QSL
+        return k_store, v_store, DEV_BAD_QSL
     status = 0
     for s in range(S):
         q_len = qsl[s + 1] - qsl[s]
@@ -233,4 +252,4 @@ def cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_sta
                 continue
             k_out[page, pos % block_size] = k_new[qsl[s] + i]
             v_out[page, pos % block_size] = v_new[qsl[s] + i]
-    return k_out, v_out, status
+    return k_store, v_store, status
