@@ -238,6 +238,38 @@ def secondary_workloads(pa, flush, peaks):
                               "note": "2 MB of KV: launch-latency bound"}
     del b, out
 
+    # the headline decode batch with NHD and with head-major (HND) caches
+    # (one (page, kv head) run of 16 slots is one contiguous 4 KB box), timed
+    # the same way as the headline (back-to-back steps, KV >> L2, no flush),
+    # alternating layouts over 5 rounds; median ms per step of each
+    hn = inputs.llama_decode(64, poison=False)
+    runs = {}
+    for name, h in (("nhd", hn), ("hnd", inputs.as_hnd(hn))):
+        d = pa.to_device(h)
+        o = torch.empty_like(d.q)
+        pa.forward(d, out=o)
+        runs[name] = (d, o)
+    per = {"nhd": [], "hnd": []}
+    st = torch.cuda.current_stream()
+    for _ in range(5):
+        for name, (d, o) in runs.items():
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(st)
+            for _ in range(100):
+                pa.forward(d, out=o)
+            e1.record(st)
+            e1.synchronize()
+            per[name].append(e0.elapsed_time(e1) / 100)
+    lay = {}
+    for name in ("nhd", "hnd"):
+        ms = statistics.median(per[name])
+        gbs = kv_bytes(hn) / ms / 1e6
+        lay[name] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm}
+    lay["hnd_over_nhd"] = lay["nhd"]["ms"] / lay["hnd"]["ms"]
+    res["llama_decode_b64_layouts"] = lay
+    del runs
+
     hb = inputs.mixed_qwen3(poison=False)
     b = pa.to_device(hb)
     out = torch.empty_like(b.q)

@@ -50,6 +50,18 @@ extern "C" {
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
 
+/*
+ * Memory layout of a paged K or V cache.  "vLLM AMD ROCm attention backend
+ * optimisation", section "ROCM_AITER_FA" ("Hardware-Optimized KV Cache
+ * Layout"), reports that a cache laid out for the hardware's access pattern
+ * speeds decode up; PA_KV_HND is this library's counterpart: one (page, KV
+ * head) pair is one contiguous run of block_size x head_dim elements, which
+ * one bulk copy moves.
+ *   PA_KV_NHD  [num_blocks, block_size, num_kv_heads, head_dim]  (default)
+ *   PA_KV_HND  [num_blocks, num_kv_heads, block_size, head_dim]
+ */
+typedef enum { PA_KV_NHD = 0, PA_KV_HND = 1 } pa_kv_layout;
+
 typedef enum {
   PA_OK = 0,
   PA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad alignment ...   */
@@ -82,6 +94,7 @@ typedef enum {
  *
  *  q               [num_tokens, num_heads, head_dim]                 dtype
  *  k_cache,v_cache [num_blocks, block_size, num_kv_heads, head_dim]  dtype
+ *                  (pa_forward_ex also takes the PA_KV_HND layout)
  *  block_table     [num_seqs, max_blocks_per_seq] int32; entries past
  *                  ceil(seq_len / block_size) are never read (may hold -1)
  *  seq_lens        [num_seqs] int32: context length INCLUDING this step's
@@ -127,10 +140,13 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
  *          Owned by the caller; must stay valid until the call's kernels
  *          have run; 4-byte aligned (PA_ERR_INVALID_ARG otherwise).  A row
  *          with no visible key returns zeros.  pa_mla_decode takes no sinks.
+ *   kv_layout  layout of k_cache and v_cache (PA_KV_NHD when options is
+ *          NULL); any other value is PA_ERR_INVALID_ARG.
  * Errors as for pa_forward.
  */
 typedef struct {
   const float *sinks;
+  pa_kv_layout kv_layout;
 } pa_forward_options;
 
 pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
@@ -259,8 +275,10 @@ int pa_num_sms(void);
  * block_table[s][pos / block_size]:
  *
  *  k_new, v_new     [num_tokens, num_kv_heads, head_dim]            dtype
- *  k_cache, v_cache [num_blocks, block_size, num_kv_heads, head_dim] dtype,
- *                   written in place; every other slot is left untouched
+ *  k_cache, v_cache [num_blocks, block_size, num_kv_heads, head_dim] dtype
+ *                   (PA_KV_NHD) or [num_blocks, num_kv_heads, block_size,
+ *                   head_dim] (PA_KV_HND), written in place; every other slot
+ *                   is left untouched
  *  block_table, seq_lens, query_start_loc: as for pa_forward (seq_lens are
  *                   the lengths after this write)
  *  head_dim x element size a multiple of 16 bytes; any block_size >= 1
@@ -276,17 +294,20 @@ int pa_num_sms(void);
  * Errors: PA_ERR_INVALID_ARG for null pointers with num_tokens > 0, negative
  * sizes, num_seqs == 0 with num_tokens > 0, or tensors not 16-byte aligned;
  * PA_ERR_UNSUPPORTED when a row is not a multiple of 16 bytes; PA_ERR_CUDA
- * when a launch fails.  num_tokens == 0 launches nothing.
+ * when a launch fails; PA_ERR_INVALID_ARG for an unknown kv_layout.
+ * num_tokens == 0 launches nothing.
  */
 pa_status pa_cache_write(const void *k_new, const void *v_new, void *k_cache,
                          void *v_cache, const int32_t *block_table,
                          const int32_t *seq_lens, const int32_t *query_start_loc,
                          int num_kv_heads, int head_dim, int block_size,
                          void *stream, pa_dtype dtype, int num_seqs,
-                         int num_tokens, int max_blocks_per_seq, int num_blocks);
+                         int num_tokens, int max_blocks_per_seq, int num_blocks,
+                         pa_kv_layout kv_layout);
 
 /*
- * pa_debug_gather -- the page-gather indexing alone, for bit-exact tests:
+ * pa_debug_gather -- the page-gather indexing alone (PA_KV_NHD), for
+ * bit-exact tests:
  *   dense_out[s][j][:] = k_cache[block_table[s][j / bs]][j % bs][0:row_elems]
  * for j < seq_lens[s] (raw element bits copied, elem_bytes 2 or 4); positions
  * j >= seq_lens[s] are left untouched.  dense_out is

@@ -624,18 +624,23 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Tensor map over a paged cache [num_blocks, block_size, heads, dim] with a
-// box of {dim, 1, box_slots, 1}: one (page, kv head) run of slots per copy.
-bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int num_blocks,
-                      int block_size, int heads, int dim, int box_dim0, int box_slots,
-                      CUtensorMapSwizzle swz) {
+// Tensor map over a paged cache with coordinates (dim, kv head, slot, page)
+// and a box of {box_dim0, 1, box_slots, 1}: one (page, kv head) run of slots
+// per copy.  The layout only changes the strides: [num_blocks, block_size,
+// heads, dim] (PA_KV_NHD) or [num_blocks, heads, block_size, dim] (PA_KV_HND).
+bool encode_cache_map(CUtensorMap *map, const void *base, int dtype, int kv_layout,
+                      int num_blocks, int block_size, int heads, int dim, int box_dim0,
+                      int box_slots, CUtensorMapSwizzle swz) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const size_t es = dtype == PA_F32 ? 4 : 2;
+  const bool hnd = kv_layout == PA_KV_HND;
   cuuint64_t dims[4] = {(cuuint64_t)dim, (cuuint64_t)heads, (cuuint64_t)block_size,
                         (cuuint64_t)num_blocks};
-  cuuint64_t strides[3] = {(cuuint64_t)(dim * es), (cuuint64_t)(heads * dim * es),
-                           (cuuint64_t)((size_t)block_size * heads * dim * es)};
+  const cuuint64_t row = dim * es;  // one (slot, head) row
+  cuuint64_t strides[3] = {hnd ? (cuuint64_t)block_size * row : row,
+                           hnd ? row : (cuuint64_t)heads * row,
+                           (cuuint64_t)block_size * heads * row};
   cuuint32_t box[4] = {(cuuint32_t)box_dim0, 1, (cuuint32_t)box_slots, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType t =
@@ -760,18 +765,20 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     // bf16 K/V boxes of 16 slots x both 64-dim halves of one KV head:
     // dims {64 dims, slots, halves, kv heads, pages} (the slot stride is
     // larger than the half stride; TMA takes strides in any order).  The row
-    // kernel reads K and V through them, the tile kernel V.
+    // kernel reads K and V through them, the tile kernel V.  In the HND
+    // layout a box is one contiguous run of 16 x head_dim elements.
     CUtensorMap tm_kr, tm_vr;
     if (c.dtype == PA_BF16) {
-      const unsigned long long es = 2;
+      const unsigned long long es = 2, row = (unsigned long long)c.head_dim * es;
+      const bool hnd = c.kv_layout == PA_KV_HND;
       const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
                                           (unsigned long long)(c.head_dim / 64),
                                           (unsigned long long)c.num_kv_heads,
                                           (unsigned long long)c.num_blocks};
       const unsigned long long strides[4] = {
-          (unsigned long long)c.num_kv_heads * c.head_dim * es, 64 * es,
-          (unsigned long long)c.head_dim * es,
-          (unsigned long long)c.block_size * c.num_kv_heads * c.head_dim * es};
+          hnd ? row : (unsigned long long)c.num_kv_heads * row, 64 * es,
+          hnd ? (unsigned long long)c.block_size * row : row,
+          (unsigned long long)c.block_size * c.num_kv_heads * row};
       const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
       if (!encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true) ||
           !encode_tiled(&tm_vr, c.v_cache, c.dtype, 5, dims, strides, box, true))
@@ -780,8 +787,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     // The tile kernel's K: one 64-element (128-byte) swizzled box per half
     // and 16 slots, so the S product sees a uniform row stride.
     CUtensorMap tm_kt;
-    if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.num_blocks, c.block_size,
-                                     c.num_kv_heads, c.head_dim, 64, 16,
+    if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.kv_layout, c.num_blocks,
+                                     c.block_size, c.num_kv_heads, c.head_dim, 64, 16,
                                      CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
     cudaError_t row_err;
@@ -791,10 +798,10 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     } else {
       // fp32: whole rows of head_dim elements, no swizzle (CUDA-core kernel)
       CUtensorMap tm_k, tm_v;
-      if (!encode_cache_map(&tm_k, c.k_cache, c.dtype, c.num_blocks, c.block_size,
+      if (!encode_cache_map(&tm_k, c.k_cache, c.dtype, c.kv_layout, c.num_blocks, c.block_size,
                             c.num_kv_heads, c.head_dim, c.head_dim, 16,
                             CU_TENSOR_MAP_SWIZZLE_NONE) ||
-          !encode_cache_map(&tm_v, c.v_cache, c.dtype, c.num_blocks, c.block_size,
+          !encode_cache_map(&tm_v, c.v_cache, c.dtype, c.kv_layout, c.num_blocks, c.block_size,
                             c.num_kv_heads, c.head_dim, c.head_dim, 16,
                             CU_TENSOR_MAP_SWIZZLE_NONE))
         return PA_ERR_CUDA;
@@ -949,7 +956,10 @@ pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
   if (options) {
     if (options->sinks && (reinterpret_cast<uintptr_t>(options->sinks) & 3))
       return PA_ERR_INVALID_ARG;
+    if (options->kv_layout != PA_KV_NHD && options->kv_layout != PA_KV_HND)
+      return PA_ERR_INVALID_ARG;
     c.sinks = options->sinks;
+    c.kv_layout = options->kv_layout;
   }
   pa_status s = fwd_check(c);
   if (s != PA_OK || num_tokens == 0) return s;

@@ -17,6 +17,8 @@
 //    query_start_loc, its slot through the block table, then the K and the V
 //    row copied with 16-byte vector accesses.  HBM-bound: it reads and writes
 //    2 x num_tokens x num_kv_heads x head_dim elements.
+// The cache layout (NHD or HND) only changes where a (page, slot, head) row
+// lands.
 #include "pa_internal.h"
 
 namespace pa {
@@ -30,6 +32,7 @@ struct CacheWriteArgs {
   uint8_t *k_cache, *v_cache;
   const int32_t *block_table, *seq_lens, *qsl;
   int num_seqs, num_tokens, num_kv_heads, row_bytes, block_size, max_blocks_per_seq, num_blocks;
+  int hnd;      // 1: caches are [num_blocks, num_kv_heads, block_size, head_dim]
   int *qsl_ok;  // workspace flag written by the check
   unsigned int *status;
 };
@@ -87,7 +90,10 @@ __global__ void __launch_bounds__(kCopyThreads) cache_copy_kernel(const CacheWri
       continue;
     }
     const size_t src = ((size_t)t * a.num_kv_heads + h) * a.row_bytes;
-    const size_t dst = (((size_t)page * bs + pos % bs) * a.num_kv_heads + h) * a.row_bytes;
+    const size_t dst =
+        (a.hnd ? ((size_t)page * a.num_kv_heads + h) * bs + pos % bs
+               : ((size_t)page * bs + pos % bs) * a.num_kv_heads + h) *
+        a.row_bytes;
     for (int c = lane * 16; c < a.row_bytes; c += lpr * 16) {
       const uint4 kv = *reinterpret_cast<const uint4 *>(a.k_new + src + c);
       const uint4 vv = *reinterpret_cast<const uint4 *>(a.v_new + src + c);
@@ -109,9 +115,11 @@ extern "C" pa_status pa_cache_write(const void *k_new, const void *v_new, void *
                                     const int32_t *seq_lens, const int32_t *query_start_loc,
                                     int num_kv_heads, int head_dim, int block_size, void *stream,
                                     pa_dtype dtype, int num_seqs, int num_tokens,
-                                    int max_blocks_per_seq, int num_blocks) {
+                                    int max_blocks_per_seq, int num_blocks,
+                                    pa_kv_layout kv_layout) {
   if (num_seqs < 0 || num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 ||
-      max_blocks_per_seq < 0 || num_blocks < 0 || (dtype != PA_F32 && dtype != PA_BF16))
+      max_blocks_per_seq < 0 || num_blocks < 0 || (dtype != PA_F32 && dtype != PA_BF16) ||
+      (kv_layout != PA_KV_NHD && kv_layout != PA_KV_HND))
     return PA_ERR_INVALID_ARG;
   const int es = dtype == PA_F32 ? 4 : 2;
   if ((head_dim * es) % 16 != 0) return PA_ERR_UNSUPPORTED;
@@ -142,6 +150,7 @@ extern "C" pa_status pa_cache_write(const void *k_new, const void *v_new, void *
   a.block_size = block_size;
   a.max_blocks_per_seq = max_blocks_per_seq;
   a.num_blocks = num_blocks;
+  a.hnd = kv_layout == PA_KV_HND;
   a.qsl_ok = static_cast<int *>(ws);
   a.status = status;
   if (launch_dependent(cache_check_kernel, dim3(1), dim3(kCheckThreads), 0, st, a) != cudaSuccess)

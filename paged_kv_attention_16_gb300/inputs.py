@@ -20,6 +20,7 @@ in use plus slack.  With poison=True, unused pool pages, tail slots of each
 request's last page and unused block-table entries hold NaN / invalid ids, so
 a kernel that reads outside the visible range shows it.
 """
+import dataclasses
 from dataclasses import dataclass, field
 import math
 
@@ -46,6 +47,7 @@ class PagedBatch:
     max_seq_len: int
     kv_split_tokens: int = 0
     kinds: list = field(default_factory=list)
+    kv_layout: str = "nhd"  # "nhd": caches [nb, bs, Hk, D]; "hnd": [nb, Hk, bs, D]
 
     @property
     def num_seqs(self):
@@ -281,3 +283,13 @@ def storage_array(t):
     if t.dtype == torch.int32:
         return t.numpy()
     raise TypeError(t.dtype)
+
+
+def as_hnd(b):
+    """The same batch with its caches stored head-major, [nb, Hk, bs, D]
+    (a copy; values and block table unchanged)."""
+    fields = {f.name: getattr(b, f.name) for f in dataclasses.fields(b)}
+    fields["k_cache"] = b.k_cache.permute(0, 2, 1, 3).contiguous()
+    fields["v_cache"] = b.v_cache.permute(0, 2, 1, 3).contiguous()
+    fields["kv_layout"] = "hnd"
+    return type(b)(**fields)

@@ -23,6 +23,7 @@ PA_DEV_BAD_SEQLEN = 0x4
 PA_DEV_BAD_QSL = 0x8
 PA_DEV_OVERFLOW = 0x10
 PA_DEV_TIMEOUT = 0x20
+PA_KV_NHD, PA_KV_HND = 0, 1  # pa_kv_layout
 
 # Every entry point declared in include/pa.h.
 EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cache_write",
@@ -35,7 +36,15 @@ PA_K_COUNT = 8
 class ForwardOptions(ctypes.Structure):
     """pa_forward_options: sinks = device pointer to [num_heads] fp32 sink
     logits, or None."""
-    _fields_ = [("sinks", ctypes.c_void_p)]
+    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int)]
+
+
+def layout_code(kv_layout):
+    """pa_kv_layout of "nhd" ([num_blocks, block_size, Hk, D]) or "hnd"
+    ([num_blocks, Hk, block_size, D]); ints pass through."""
+    if isinstance(kv_layout, int):
+        return kv_layout
+    return {"nhd": PA_KV_NHD, "hnd": PA_KV_HND}[kv_layout]
 
 
 class PaError(RuntimeError):
@@ -75,7 +84,7 @@ def lib():
         L.pa_num_sms.argtypes = []
         L.pa_num_sms.restype = c_int
         L.pa_cache_write.argtypes = [vp, vp, vp, vp, i32p, i32p, i32p, c_int, c_int, c_int, vp,
-                                     c_int, c_int, c_int, c_int, c_int]
+                                     c_int, c_int, c_int, c_int, c_int, c_int]
         L.pa_cache_write.restype = c_int
         L.pa_debug_gather.argtypes = [vp, i32p, i32p, c_int, c_int, c_int, c_int, c_int, c_int,
                                       c_int, vp, vp]
@@ -129,11 +138,12 @@ def _check(status, where):
 
 def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
                num_kv_heads, head_dim, block_size, scale, out, stream=None, *, max_seq_len,
-               kv_split_tokens=0, num_blocks=None, sinks=None, check=True):
+               kv_split_tokens=0, num_blocks=None, sinks=None, kv_layout="nhd", check=True):
     """Unified paged attention (see include/pa.h).  Shapes are read from the
-    tensors; max_seq_len is the host-known bound on seq_lens.  sinks: an
-    optional fp32 device tensor of num_heads sink logits, passed through
-    pa_forward_ex."""
+    tensors; max_seq_len is the host-known bound on seq_lens.  sinks (an
+    optional fp32 device tensor of num_heads sink logits) and an HND
+    kv_layout go through pa_forward_ex."""
+    layout = layout_code(kv_layout)
     args = (
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(query_start_loc), int(num_heads), int(num_kv_heads), int(head_dim),
@@ -141,13 +151,13 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
         int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
         int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
         int(kv_split_tokens))
-    if sinks is None:
+    if sinks is None and layout == PA_KV_NHD:
         st, where = lib().pa_forward(*args), "pa_forward"
     else:
         if isinstance(sinks, torch.Tensor) and (sinks.dtype != torch.float32
                                                 or sinks.numel() != num_heads):
             raise TypeError("sinks must be a float32 tensor of num_heads elements")
-        opts = ForwardOptions(_ptr(sinks))
+        opts = ForwardOptions(_ptr(sinks), layout)
         st, where = lib().pa_forward_ex(*args, ctypes.byref(opts)), "pa_forward_ex"
     if check:
         _check(st, where)
@@ -237,15 +247,16 @@ def pa_num_sms():
 
 
 def pa_cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_start_loc,
-                   block_size, stream=None, check=True):
+                   block_size, stream=None, kv_layout="nhd", check=True):
     """pa_cache_write on torch tensors: k_new/v_new [T, Hk, D], caches
-    [num_blocks, block_size, Hk, D] (written in place)."""
+    [num_blocks, block_size, Hk, D] ("nhd") or [num_blocks, Hk, block_size, D]
+    ("hnd"), written in place."""
     dt = PA_BF16 if k_new.dtype == torch.bfloat16 else PA_F32
     st = lib().pa_cache_write(
         _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table),
         _ptr(seq_lens), _ptr(query_start_loc), int(k_new.shape[1]), int(k_new.shape[2]),
         int(block_size), _stream_ptr(stream), dt, int(seq_lens.shape[0]), int(k_new.shape[0]),
-        int(block_table.shape[1]), int(k_cache.shape[0]))
+        int(block_table.shape[1]), int(k_cache.shape[0]), layout_code(kv_layout))
     if check:
         _check(st, "pa_cache_write")
     return st
@@ -285,7 +296,7 @@ def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None):
                b.num_heads, b.num_kv_heads, b.head_dim, b.block_size, b.scale, out, stream,
                max_seq_len=b.max_seq_len,
                kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens,
-               sinks=sinks)
+               sinks=sinks, kv_layout=b.kv_layout)
     return out
 
 

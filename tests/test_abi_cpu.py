@@ -82,28 +82,30 @@ def test_workspace_bytes_grow_with_splits(lib):
 
 def _cache_write(lib, **kw):
     args = dict(kn=1 << 20, vn=1 << 20, kc=1 << 20, vc=1 << 20, bt=1 << 20, sl=1 << 20,
-                qsl=1 << 20, Hk=2, D=128, bs=16, stream=None, dtype=1, S=1, T=1, mbps=4, nb=4)
+                qsl=1 << 20, Hk=2, D=128, bs=16, stream=None, dtype=1, S=1, T=1, mbps=4, nb=4,
+                layout=0)
     args.update(kw)
     f = lib.pa_cache_write
     f.restype = ctypes.c_int
     vp = ctypes.c_void_p
-    f.argtypes = [vp] * 7 + [ctypes.c_int] * 3 + [vp] + [ctypes.c_int] * 5
+    f.argtypes = [vp] * 7 + [ctypes.c_int] * 3 + [vp] + [ctypes.c_int] * 6
     a = args
     return f(a["kn"], a["vn"], a["kc"], a["vc"], a["bt"], a["sl"], a["qsl"], a["Hk"], a["D"],
-             a["bs"], a["stream"], a["dtype"], a["S"], a["T"], a["mbps"], a["nb"])
+             a["bs"], a["stream"], a["dtype"], a["S"], a["T"], a["mbps"], a["nb"], a["layout"])
 
 
 @pytest.mark.parametrize("kw,want", [
     (dict(Hk=0), 1), (dict(D=-1), 1), (dict(bs=0), 1), (dict(S=-1), 1), (dict(dtype=5), 1),
     (dict(D=4), 2), (dict(D=6, dtype=0), 2), (dict(T=0), 0), (dict(kn=0), 1), (dict(S=0), 1),
-    (dict(kc=(1 << 20) + 8), 1), (dict(nb=0), 1),
+    (dict(kc=(1 << 20) + 8), 1), (dict(nb=0), 1), (dict(layout=2), 1), (dict(layout=-1), 1),
+    (dict(layout=1, T=0), 0),
 ])
 def test_cache_write_host_argument_checks(lib, kw, want):
     assert _cache_write(lib, **kw) == want
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("sinks", ctypes.c_void_p)]
+    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int)]
 
 
 def _forward_ex(lib, options, **kw):
@@ -122,15 +124,18 @@ def _forward_ex(lib, options, **kw):
              a["msl"], a["kvs"], options)
 
 
-@pytest.mark.parametrize("sinks,kw,want", [
-    (None, dict(H=0), 1),              # the checks of pa_forward still apply
-    (None, dict(D=96), 2),
-    (1 << 20, dict(T=0), 0),           # nothing to do: no launch
-    ((1 << 20) + 2, dict(T=0), 1),     # a sinks array that is not 4-byte aligned
-    ((1 << 20) + 2, dict(), 1),
+@pytest.mark.parametrize("sinks,layout,kw,want", [
+    (None, 0, dict(H=0), 1),              # the checks of pa_forward still apply
+    (None, 0, dict(D=96), 2),
+    (1 << 20, 0, dict(T=0), 0),           # nothing to do: no launch
+    ((1 << 20) + 2, 0, dict(T=0), 1),     # a sinks array that is not 4-byte aligned
+    ((1 << 20) + 2, 0, dict(), 1),
+    (None, 1, dict(T=0), 0),              # HND
+    (None, 2, dict(T=0), 1),              # no such layout
+    (None, -1, dict(), 1),
 ])
-def test_forward_ex_host_argument_checks(lib, sinks, kw, want):
-    opts = _Options(sinks)
+def test_forward_ex_host_argument_checks(lib, sinks, layout, kw, want):
+    opts = _Options(sinks, layout)
     assert _forward_ex(lib, ctypes.byref(opts), **kw) == want
-    if sinks is None:
+    if sinks is None and layout == 0:
         assert _forward_ex(lib, None, **kw) == want  # null options: pa_forward
