@@ -30,7 +30,15 @@
  *   - the new tokens' K/V are already in the cache (seq_len includes them);
  *   - head h reads KV head floor(h / G), G = num_heads / num_kv_heads;
  *   - absorbed MLA: the value of a cached latent row is its first
- *     kv_lora_rank entries; the trailing rope entries only enter the score.
+ *     kv_lora_rank entries; the trailing rope entries only enter the score;
+ *   - model variants ("vLLM Triton attention backend deep dive", section
+ *     "Usage scenarios": ALiBi sqrt, sink tokens, GPT-OSS behaviour), which
+ *     the pages name but do not define:
+ *       sliding window W (GPT-OSS local attention): the query at position i
+ *       sees only the W most recent positions, i - W < j <= i;
+ *       ALiBi (linear biases, one slope m_h per head, slopes supplied by
+ *       the caller): score_ij += -m_h * (i - j);
+ *       ALiBi sqrt: score_ij += -m_h * sqrt(i - j).
  *
  * Softmax is the two-pass textbook form: max, then exp(s - max) / sum.
  */
@@ -71,7 +79,9 @@ static long long cache_row(const int32_t *block_table, int max_blocks_per_seq,
 
 /* Attention for one query row over the visible KV positions in
  * [kv_begin, kv_end) of request s.
- *   score_j = scale * sum_d q[d] * K_j[d]         (d < dk)
+ *   score_j = scale * sum_d q[d] * K_j[d] + bias_j (d < dk)
+ *   bias_j  = -slope * (qpos - j), or -slope * sqrt(qpos - j) with bias_sqrt
+ *             (ALiBi; slope 0 adds -0.0, which changes no score)
  *   p_j     = exp(score_j - max) / sum exp(score - max)
  *   out[e]  = sum_j p_j * V_j[e]                   (e < dv)
  * K_j[d] = kc[row_j*kstride + koff + d], V_j[e] = vc[row_j*vstride + voff + e].
@@ -83,6 +93,7 @@ static int attend_row(const double *qrow, int dk, int dv,
                       const int32_t *block_table, int max_blocks_per_seq,
                       int num_blocks, int block_size, int s,
                       long long kv_begin, long long kv_end, double scale,
+                      double slope, int bias_sqrt, long long qpos,
                       double *scores, double *out, double *lse) {
   long long n = kv_end - kv_begin;
   for (int e = 0; e < dv; ++e) out[e] = 0.0;
@@ -98,7 +109,9 @@ static int attend_row(const double *qrow, int dk, int dv,
     double acc = 0.0;
     for (int d = 0; d < dk; ++d)
       acc += qrow[d] * widen(kc, dtype, (size_t)row * kstride + koff + d);
-    scores[t] = scale * acc;
+    const double dist = (double)(qpos - (kv_begin + t));
+    const double bias = bias_sqrt ? -slope * sqrt(dist) : -slope * dist;
+    scores[t] = scale * acc + bias;
     if (scores[t] > mx) mx = scores[t];
   }
   double denom = 0.0;
@@ -133,6 +146,10 @@ static int token_owner(const int32_t *qsl, int num_seqs, int num_tokens,
  * [kv_begin, kv_end) of every request (kv_begin = 0, kv_end = INT64_MAX gives
  * the full definition).  The restriction exists only so that tests can form
  * split-KV partial results; it does not change the definition.
+ * sliding_window > 0: query i of a request (absolute position p) sees only
+ * positions p - sliding_window < j <= p.  alibi_slopes (one per query head,
+ * or NULL) adds -slope_h * (p - j), or -slope_h * sqrt(p - j) when
+ * alibi_sqrt is set, to every score of head h.
  *
  *   q        [num_tokens, num_heads, head_dim]
  *   k_cache  [num_blocks, block_size, num_kv_heads, head_dim]
@@ -141,17 +158,18 @@ static int token_owner(const int32_t *qsl, int num_seqs, int num_tokens,
  *   lse      [num_tokens, num_heads] (double, may be NULL)
  *   rows     optional list of (token * num_heads + head) to compute; NULL = all
  */
-int oracle_paged_attention_window(
+int oracle_paged_attention_ex(
     const void *q, const void *k_cache, const void *v_cache, int dtype,
     const int32_t *block_table, const int32_t *seq_lens,
     const int32_t *query_start_loc, int num_seqs, int num_tokens,
     int num_heads, int num_kv_heads, int head_dim, int block_size,
     int max_blocks_per_seq, int num_blocks, double scale,
-    long long kv_begin, long long kv_end, const int64_t *rows,
+    long long kv_begin, long long kv_end, long long sliding_window,
+    const double *alibi_slopes, int alibi_sqrt, const int64_t *rows,
     long long num_rows, double *out, double *lse) {
   if (num_seqs < 0 || num_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
       num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 ||
-      (dtype != OR_F32 && dtype != OR_BF16))
+      sliding_window < 0 || (dtype != OR_F32 && dtype != OR_BF16))
     return OR_BAD_ARGS;
   const int group = num_heads / num_kv_heads;
   int32_t *owner = (int32_t *)malloc(sizeof(int32_t) * (num_tokens + 1));
@@ -189,10 +207,14 @@ int oracle_paged_attention_window(
       int q_len = query_start_loc[s + 1] - query_start_loc[s];
       long long prefix = (long long)seq_lens[s] - q_len;
       long long i = tok - query_start_loc[s];
-      /* Visible positions: 0 .. prefix + i (causal, bottom-right). */
+      /* Visible positions: 0 .. prefix + i (causal, bottom-right), and with
+       * a sliding window only the last sliding_window of them. */
+      long long qpos = prefix + i;
       long long lo = kv_begin > 0 ? kv_begin : 0;
-      long long hi = prefix + i + 1;
+      if (sliding_window > 0 && qpos - sliding_window + 1 > lo) lo = qpos - sliding_window + 1;
+      long long hi = qpos + 1;
       if (kv_end < hi) hi = kv_end;
+      double slope = alibi_slopes ? alibi_slopes[h] : 0.0;
       int kvh = h / group;
       for (int d = 0; d < head_dim; ++d)
         qrow[d] = widen(q, dtype, (size_t)flat * head_dim + d);
@@ -201,7 +223,8 @@ int oracle_paged_attention_window(
                           kstride, (size_t)kvh * head_dim, kstride,
                           (size_t)kvh * head_dim, block_table,
                           max_blocks_per_seq, num_blocks, block_size, s, lo, hi,
-                          scale, scores, out + (size_t)flat * head_dim, &row_lse);
+                          scale, slope, alibi_sqrt, qpos, scores,
+                          out + (size_t)flat * head_dim, &row_lse);
       if (lse) lse[flat] = row_lse;
       if (rr != OR_OK) {
 #pragma omp atomic write
@@ -213,6 +236,21 @@ int oracle_paged_attention_window(
   }
   free(owner);
   return status;
+}
+
+int oracle_paged_attention_window(
+    const void *q, const void *k_cache, const void *v_cache, int dtype,
+    const int32_t *block_table, const int32_t *seq_lens,
+    const int32_t *query_start_loc, int num_seqs, int num_tokens,
+    int num_heads, int num_kv_heads, int head_dim, int block_size,
+    int max_blocks_per_seq, int num_blocks, double scale,
+    long long kv_begin, long long kv_end, const int64_t *rows,
+    long long num_rows, double *out, double *lse) {
+  return oracle_paged_attention_ex(
+      q, k_cache, v_cache, dtype, block_table, seq_lens, query_start_loc,
+      num_seqs, num_tokens, num_heads, num_kv_heads, head_dim, block_size,
+      max_blocks_per_seq, num_blocks, scale, kv_begin, kv_end, 0, NULL, 0,
+      rows, num_rows, out, lse);
 }
 
 int oracle_paged_attention(const void *q, const void *k_cache,
@@ -314,7 +352,7 @@ int oracle_mla_decode(const void *q, const void *kv_cache, int dtype,
       int rr = attend_row(qrow, dk, kv_lora_rank, kv_cache, kv_cache, dtype,
                           (size_t)dk, 0, (size_t)dk, 0, block_table,
                           max_blocks_per_seq, num_blocks, block_size, s, 0,
-                          seq_lens[s], scale, scores,
+                          seq_lens[s], scale, 0.0, 0, 0, scores,
                           out + (size_t)flat * kv_lora_rank, &row_lse);
       if (rr != OR_OK) {
 #pragma omp atomic write

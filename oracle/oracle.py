@@ -36,6 +36,12 @@ def load(path=None):
         ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, _I64P, ctypes.c_longlong,
         _F64P, _F64P]
     lib.oracle_paged_attention_window.restype = ctypes.c_int
+    lib.oracle_paged_attention_ex.argtypes = [
+        _VP, _VP, _VP, ctypes.c_int, _I32P, _I32P, _I32P, ctypes.c_int, ctypes.c_int,
+        ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+        ctypes.c_double, ctypes.c_longlong, ctypes.c_longlong, ctypes.c_longlong, _F64P,
+        ctypes.c_int, _I64P, ctypes.c_longlong, _F64P, _F64P]
+    lib.oracle_paged_attention_ex.restype = ctypes.c_int
     lib.oracle_lse_merge.argtypes = [ctypes.c_int, ctypes.c_int, _F64P, _F64P, _F64P, _F64P]
     lib.oracle_lse_merge.restype = ctypes.c_int
     lib.oracle_mla_decode.argtypes = [
@@ -98,7 +104,7 @@ def nhd_view(cache, kv_layout):
 def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
                     num_heads, num_kv_heads, head_dim, block_size, scale,
                     rows=None, kv_window=None, lib=None, with_lse=False, sinks=None,
-                    kv_layout="nhd"):
+                    kv_layout="nhd", sliding_window=0, alibi_slopes=None, alibi_sqrt=False):
     """fp64 unified paged attention.  Shapes:
     q [T, H, D]; k_cache, v_cache [num_blocks, block_size, Hk, D];
     block_table [S, max_blocks]; seq_lens [S]; query_start_loc [S+1].
@@ -114,6 +120,12 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
     lse = log sum_j exp(s_j) over the row's visible keys (s_j = scale q.k_j).
     The returned lse stays that of the keys alone.
     kv_layout: "nhd" or "hnd" storage of the caches (see nhd_view).
+    sliding_window W > 0: the query at position p sees p - W < j <= p only.
+    alibi_slopes: optional [H] slopes m_h (natural-log units per position):
+    every score of head h gains -m_h * (p - j), or -m_h * sqrt(p - j) with
+    alibi_sqrt.  (The pages name ALiBi sqrt and GPT-OSS behaviour among the
+    unified backend's model features without defining them; these are the
+    readings.)
     Returns out [T, H, D] float64 (and lse [T, H] when with_lse)."""
     lib = lib or _lib()
     q = np.ascontiguousarray(q)
@@ -135,12 +147,17 @@ def paged_attention(q, k_cache, v_cache, block_table, seq_lens, query_start_loc,
         rows_p, nrows = None, 0
     lo, hi = (0, 2**62) if kv_window is None else kv_window
     max_blocks = int(bt.shape[1]) if bt.ndim == 2 else 0
-    rc = lib.oracle_paged_attention_window(
+    slopes = None
+    if alibi_slopes is not None:
+        slopes = np.ascontiguousarray(np.asarray(alibi_slopes, dtype=np.float64).reshape(-1))
+        assert slopes.shape[0] == num_heads
+    rc = lib.oracle_paged_attention_ex(
         q.ctypes.data, k_cache.ctypes.data, v_cache.ctypes.data, dt,
         _ptr(bt, _I32P), _ptr(sl, _I32P), _ptr(qsl, _I32P), S, T, num_heads,
         num_kv_heads, head_dim, block_size, max_blocks, int(k_cache.shape[0]),
-        float(scale), int(lo), int(hi), rows_p, nrows, _ptr(out, _F64P),
-        _ptr(lse, _F64P))
+        float(scale), int(lo), int(hi), int(sliding_window),
+        None if slopes is None else _ptr(slopes, _F64P), int(bool(alibi_sqrt)), rows_p, nrows,
+        _ptr(out, _F64P), _ptr(lse, _F64P))
     _check(rc)
     if sinks is not None:
         sk = np.asarray(sinks, dtype=np.float64).reshape(1, num_heads)

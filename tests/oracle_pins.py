@@ -293,7 +293,110 @@ def pin_golden_two_key(lib):
     np.testing.assert_allclose(out[0, 0], vals["expected"], rtol=0, atol=1e-14)
 
 
+def sdpa_request_masked(q, k, v, ctx, scale, window=0, slopes=None, use_sqrt=False):
+    """torch SDPA in fp64 for one request with an additive float mask written
+    from the definitions: -inf outside p - window < j <= p (p the query's
+    position; no lower bound without a window), plus the ALiBi term
+    -m_h (p - j) or -m_h sqrt(p - j) per head."""
+    ql, H, D = q.shape
+    G = H // k.shape[1]
+    qt = torch.from_numpy(q.astype(np.float64)).permute(1, 0, 2)[None]
+    kt = torch.from_numpy(k.astype(np.float64)).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    vt = torch.from_numpy(v.astype(np.float64)).repeat_interleave(G, dim=1).permute(1, 0, 2)[None]
+    pos = (ctx - ql + torch.arange(ql, dtype=torch.float64))[:, None]   # [ql, 1]
+    j = torch.arange(ctx, dtype=torch.float64)[None, :]                 # [1, ctx]
+    visible = j <= pos
+    if window:
+        visible &= j > pos - window
+    dist = (pos - j).clamp(min=0)
+    bias = torch.zeros((H, ql, ctx), dtype=torch.float64)
+    if slopes is not None:
+        m = torch.as_tensor(np.asarray(slopes, np.float64))[:, None, None]
+        bias = -m * (dist.sqrt() if use_sqrt else dist)[None]
+    mask = torch.where(visible[None], bias, torch.tensor(-math.inf, dtype=torch.float64))
+    out = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt, attn_mask=mask[None],
+                                                           scale=scale)
+    return out[0].permute(1, 0, 2).numpy()
+
+
+def alibi_slopes(H):
+    """The geometric ALiBi slopes 2^(-8 h / H), h = 1..H."""
+    return np.array([2.0 ** (-8.0 * (h + 1) / H) for h in range(H)])
+
+
+def pin_window_alibi_vs_sdpa(lib):
+    """Sliding windows, linear and sqrt ALiBi, alone and together, on a
+    decode + extend + prefill batch: each request equals SDPA with the mask
+    and bias written out densely."""
+    H, Hk, D, bs = 6, 2, 8, 4
+    q_lens = [1, 5, 9, 1, 4]
+    ctx = [23, 22, 9, 1, 4]
+    qs, ks, vs = make_dense(q_lens, ctx, H, Hk, D, seed=21)
+    scale = 1 / math.sqrt(D)
+    sl = alibi_slopes(H)
+    for window, slopes, use_sqrt in ((3, None, False), (7, None, False), (0, sl, False),
+                                     (0, sl, True), (5, sl, False), (4, sl * 3, True)):
+        out = run_oracle(lib, qs, ks, vs, q_lens, ctx, H, Hk, D, bs, scale, seed=9,
+                         sliding_window=window, alibi_slopes=slopes, alibi_sqrt=use_sqrt)
+        off = 0
+        for s in range(len(q_lens)):
+            ref = sdpa_request_masked(qs[s], ks[s], vs[s], ctx[s], scale, window, slopes,
+                                      use_sqrt)
+            np.testing.assert_allclose(out[off:off + q_lens[s]], ref, rtol=0, atol=1e-12)
+            off += q_lens[s]
+
+
+def pin_window_of_one_is_own_value(lib):
+    """A window of one position: every query sees only its own key, so the
+    output is exactly its own value row (whatever the ALiBi slopes)."""
+    H, Hk, D, bs = 4, 2, 8, 4
+    q_lens, ctx = [1, 6, 3], [10, 6, 11]
+    qs, ks, vs = make_dense(q_lens, ctx, H, Hk, D, seed=22)
+    for slopes in (None, alibi_slopes(H)):
+        out = run_oracle(lib, qs, ks, vs, q_lens, ctx, H, Hk, D, bs, 0.5, seed=3,
+                         sliding_window=1, alibi_slopes=slopes)
+        off = 0
+        for s in range(len(q_lens)):
+            own = vs[s][ctx[s] - q_lens[s]:].astype(np.float64)   # [ql, Hk, D]
+            want = np.repeat(own, H // Hk, axis=1)
+            np.testing.assert_array_equal(out[off:off + q_lens[s]], want)
+            off += q_lens[s]
+
+
+def pin_wide_window_and_zero_slopes_are_plain(lib):
+    """A window covering every context, and ALiBi slopes of zero, change
+    nothing: bit-identical to plain attention."""
+    H, Hk, D, bs = 4, 1, 8, 4
+    q_lens, ctx = [1, 7, 5], [19, 12, 5]
+    qs, ks, vs = make_dense(q_lens, ctx, H, Hk, D, seed=23)
+    plain = run_oracle(lib, qs, ks, vs, q_lens, ctx, H, Hk, D, bs, 0.4, seed=4)
+    for kw in (dict(sliding_window=19), dict(sliding_window=1000),
+               dict(alibi_slopes=np.zeros(H)), dict(alibi_slopes=np.zeros(H), alibi_sqrt=True)):
+        got = run_oracle(lib, qs, ks, vs, q_lens, ctx, H, Hk, D, bs, 0.4, seed=4, **kw)
+        np.testing.assert_array_equal(got, plain)
+
+
+def pin_alibi_geometric_closed_form(lib):
+    """q = 0 makes every dot product 0, so with linear ALiBi the decode
+    query at position p weighs key j by r^(p - j) / Z, r = e^(-m).  With
+    values V_j = (1, j): out = (1, p - S1 / S0), S0 = sum_k r^k and
+    S1 = sum_k k r^k over k = 0..p, in closed form."""
+    p, m = 12, 0.3
+    ctx = p + 1
+    q = np.zeros((1, 1, 2), np.float32)
+    k = np.random.default_rng(24).standard_normal((ctx, 1, 2)).astype(np.float32)
+    v = np.stack([np.ones(ctx), np.arange(ctx)], axis=1)[:, None, :].astype(np.float32)
+    out = run_oracle(lib, [q], [k], [v], [1], [ctx], 1, 1, 2, 4, 1.0, seed=2,
+                     alibi_slopes=np.array([m]))
+    r = math.exp(-m)
+    s0 = (1 - r ** (p + 1)) / (1 - r)
+    s1 = r * (1 - (p + 1) * r ** p + p * r ** (p + 1)) / (1 - r) ** 2
+    np.testing.assert_allclose(out[0, 0], [1.0, p - s1 / s0], rtol=0, atol=1e-12)
+
+
 ALL_PINS = [pin_sdpa_prefill_causal, pin_sdpa_mixed_batch, pin_extend_is_tail_of_prefill,
             pin_single_key, pin_identical_keys_mean, pin_rows_sum_to_one,
             pin_page_placement_invariance, pin_request_order_invariance, pin_split_merge,
-            pin_merge_closed_form, pin_mla_vs_sdpa, pin_bf16_widening, pin_golden_two_key]
+            pin_merge_closed_form, pin_mla_vs_sdpa, pin_bf16_widening, pin_golden_two_key,
+            pin_window_alibi_vs_sdpa, pin_window_of_one_is_own_value,
+            pin_wide_window_and_zero_slopes_are_plain, pin_alibi_geometric_closed_form]

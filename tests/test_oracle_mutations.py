@@ -11,11 +11,11 @@ from oracle import oracle as orc
 from tests import oracle_pins
 
 MUTATIONS = {
-    "causal_off_by_one": ("long long hi = prefix + i + 1;", "long long hi = prefix + i;"),
+    "causal_off_by_one": ("long long hi = qpos + 1;", "long long hi = qpos;"),
     "top_left_causal": ("long long prefix = (long long)seq_lens[s] - q_len;",
                         "long long prefix = 0;"),
     "gqa_head_map": ("int kvh = h / group;", "int kvh = h % num_kv_heads;"),
-    "dropped_scale": ("scores[t] = scale * acc;", "scores[t] = acc;"),
+    "dropped_scale": ("scores[t] = scale * acc + bias;", "scores[t] = acc + bias;"),
     "slot_reversed": ("return (long long)page * block_size + (j % block_size);",
                       "return (long long)page * block_size + (block_size - 1 - j % block_size);"),
     "keys_read_from_values": ("acc += qrow[d] * widen(kc,", "acc += qrow[d] * widen(vc,"),
@@ -25,6 +25,10 @@ MUTATIONS = {
     "mla_value_offset": ("(size_t)dk, 0, (size_t)dk, 0, block_table,",
                          "(size_t)dk, 0, (size_t)dk, (size_t)rope_dim, block_table,"),
     "bf16_widening": ("[idx]) << 16;", "[idx]) << 15;"),
+    "window_off_by_one": ("lo = qpos - sliding_window + 1;", "lo = qpos - sliding_window;"),
+    "alibi_sign": (": -slope * dist;", ": slope * dist;"),
+    "alibi_sqrt_ignored": ("bias_sqrt ? -slope * sqrt(dist) :", "bias_sqrt ? -slope * dist :"),
+    "alibi_slope_per_kv_head": ("alibi_slopes[h] : 0.0", "alibi_slopes[h / group] : 0.0"),
     "denominator_dropped_term": ("for (long long t = 0; t < n; ++t) {\n    scores[t] = exp(",
                                  "for (long long t = 1; t < n; ++t) {\n    scores[t] = exp("),
 }
