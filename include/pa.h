@@ -142,11 +142,26 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
  *          with no visible key returns zeros.  pa_mla_decode takes no sinks.
  *   kv_layout  layout of k_cache and v_cache (PA_KV_NHD when options is
  *          NULL); any other value is PA_ERR_INVALID_ARG.
+ *   sliding_window  0 = none; W > 0: the query at position p (p = seq_len -
+ *          q_len + i for new token i) sees only the W most recent positions
+ *          p - W < j <= p (the local attention of "GPT-OSS behaviour", named
+ *          in the same section).  Pages wholly below every window of a
+ *          request are never read, so their block-table entries may be -1.
+ *          Negative: PA_ERR_INVALID_ARG.
+ *   alibi_slopes  device array of num_heads fp32 ALiBi slopes m_h (natural-
+ *          log units per position), or NULL; "ALiBi sqrt" is named in the
+ *          same section.  Every score of head h gains -m_h * (p - j), or
+ *          -m_h * sqrt(p - j) when alibi_sqrt is 1.  Caller-owned, 4-byte
+ *          aligned, valid until the call's kernels have run.
+ *   alibi_sqrt  0 or 1 (else PA_ERR_INVALID_ARG); ignored without slopes.
  * Errors as for pa_forward.
  */
 typedef struct {
   const float *sinks;
   pa_kv_layout kv_layout;
+  int sliding_window;
+  const float *alibi_slopes;
+  int alibi_sqrt;
 } pa_forward_options;
 
 pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     const int4 q = raw(s);
     const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
     v1[0] += 1ll << (21 * r.cls);
-    if (r.valid && r.q_len == 1) v1[1] += r.ctx;
+    if (r.valid && r.q_len == 1) v1[1] += p.window > 0 ? min(r.ctx, p.window) : r.ctx;
     if (!qsl_bad && !r.valid) {
       if (r.q_len < 0 || r.q_len > r.ctx) metabad |= PA_DEV_BAD_QLEN;
       if (r.ctx < 0 || r.ctx > p.max_seq_len ||
@@ -166,7 +166,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
       } else {
         len = row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens : (r.ctx > 0 ? r.ctx : 1));
       }
-      int nsplit = (int)ceil_div_ll(r.ctx > 0 ? r.ctx : 1, len);
+      // With a sliding window no row looks below the first row's window:
+      // splits start there (16-aligned, so that no copy box crosses a page).
+      const int kv_base = window_lo(r.ctx - r.q_len, p.window) & ~15;
+      int nsplit = (int)ceil_div_ll(r.ctx - kv_base > 0 ? r.ctx - kv_base : 1, len);
       if (nsplit < 1) nsplit = 1;
       info.q_start = r.q_start;
       info.q_len = r.q_len;
@@ -174,14 +177,17 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
       info.flags = r.cls | (r.valid ? kFlagValid : 0) | (row_path ? kFlagRowPath : 0);
       info.nsplit = nsplit;
       info.split_len = len;
+      info.kv_base = kv_base;
       if (r.valid && r.q_len > 0) {
         if (row_path) cnt[kListRow] = (long long)Hk * r.q_len * nsplit;
         else cnt[kListTile] = (long long)Hk * ceil_div_ll((long long)r.q_len * G, kTileRows) * nsplit;
         if (nsplit > 1) {
-          // row i has ceil((ctx - q_len + i + 1) / len) non-empty splits:
-          // more than kWarpMergeSplits from i = W * len - (ctx - q_len) on
+          // row i reaches split ceil((ctx - q_len + i + 1 - kv_base) / len)
+          // - 1: more than kWarpMergeSplits splits from
+          // i = W * len - (ctx - q_len - kv_base) on (a sliding window can
+          // leave fewer non-empty ones; the long pass skips those rows)
           const long long i_long =
-              max(0ll, (long long)kWarpMergeSplits * len - (r.ctx - r.q_len));
+              max(0ll, (long long)kWarpMergeSplits * len - (r.ctx - r.q_len - kv_base));
           if (i_long < r.q_len) cnt[kListMergeLong] = (r.q_len - i_long) * H;
           cnt[kListMerge] = (long long)r.q_len * H;
           cnt[kNumLists] = (long long)r.q_len * H * nsplit;
@@ -238,6 +244,20 @@ struct MergeRow {
   int h, nn;
 };
 
+// Row i, head h of request r: its non-empty splits are first .. last, the
+// splits holding its first and its last visible position.
+__device__ inline MergeRow merge_row_of(const FwdParams &p, const ReqInfo &r, int i, int h) {
+  const int pos = r.ctx - r.q_len + i;
+  const int first = (window_lo(pos, p.window) - r.kv_base) / r.split_len;
+  const int last = (pos - r.kv_base) / r.split_len;
+  MergeRow m;
+  m.h = h;
+  m.tok = r.q_start + i;
+  m.nn = last - first + 1;
+  m.base = r.partial_base + ((long long)i * p.num_heads + h) * r.nsplit + first;
+  return m;
+}
+
 // mend / ord: the merge list's ends and the request order, in global memory
 // or (shared = true) as shared-memory copies.
 __device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, const int *ord,
@@ -246,17 +266,11 @@ __device__ inline MergeRow merge_row(const FwdParams &p, const long long *mend, 
   const int k = shared ? list_find_shared(mend, S, row) : list_find(mend, S, row);
   const long long local = row - (k ? mend[k - 1] : 0);
   const ReqInfo r = p.req[ord[k]];
-  const int i = (int)(local / H);
-  MergeRow m;
-  m.h = (int)(local % H);
-  m.tok = r.q_start + i;
-  m.nn = (int)ceil_div_ll(r.ctx - r.q_len + i + 1, r.split_len);  // non-empty splits
-  m.base = r.partial_base + ((long long)i * H + m.h) * r.nsplit;
-  return m;
+  return merge_row_of(p, r, (int)(local / H), (int)(local % H));
 }
 
-// Entry `row` of the long-row list: request k's rows i >= i_long (those with
-// more than kWarpMergeSplits non-empty splits), H heads each.
+// Entry `row` of the long-row list: request k's rows i >= i_long (those that
+// reach past split kWarpMergeSplits - 1), H heads each.
 __device__ inline MergeRow merge_row_long(const FwdParams &p, const long long *lend,
                                           long long row) {
   const int S = p.num_seqs, H = p.num_heads;
@@ -264,14 +278,8 @@ __device__ inline MergeRow merge_row_long(const FwdParams &p, const long long *l
   const long long local = row - (k ? lend[k - 1] : 0);
   const ReqInfo r = p.req[p.ord[k]];
   const long long i_long =
-      max(0ll, (long long)kWarpMergeSplits * r.split_len - (r.ctx - r.q_len));
-  const int i = (int)(i_long + local / H);
-  MergeRow m;
-  m.h = (int)(local % H);
-  m.tok = r.q_start + i;
-  m.nn = (int)ceil_div_ll(r.ctx - r.q_len + i + 1, r.split_len);
-  m.base = r.partial_base + ((long long)i * H + m.h) * r.nsplit;
-  return m;
+      max(0ll, (long long)kWarpMergeSplits * r.split_len - (r.ctx - r.q_len - r.kv_base));
+  return merge_row_of(p, r, (int)(i_long + local / H), (int)(local % H));
 }
 
 template <typename T>
@@ -392,6 +400,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_kernel(const FwdParams p)
   const long long *lend = p.list_end + (size_t)kListMergeLong * S;
   for (long long row = blockIdx.x; row < nl; row += gridDim.x) {
     const MergeRow mr = merge_row_long(p, lend, row);
+    if (mr.nn <= kWarpMergeSplits) continue;  // a windowed row: the warp pass has it
     float M = -INFINITY;
     int bad = 0;
     for (int q = tid; q < mr.nn; q += kMergeThreads) {
@@ -748,6 +757,9 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.part_cap = lay.part_cap;
   p.status = status;
   p.sinks = c.sinks;
+  p.window = c.sliding_window;
+  p.alibi = c.alibi_slopes;
+  p.alibi_sqrt = c.alibi_sqrt;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
   // One thread per request, whole warps, at most kPlanThreads: small batches
@@ -958,8 +970,15 @@ pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
       return PA_ERR_INVALID_ARG;
     if (options->kv_layout != PA_KV_NHD && options->kv_layout != PA_KV_HND)
       return PA_ERR_INVALID_ARG;
+    if (options->sliding_window < 0 || (options->alibi_sqrt != 0 && options->alibi_sqrt != 1))
+      return PA_ERR_INVALID_ARG;
+    if (options->alibi_slopes && (reinterpret_cast<uintptr_t>(options->alibi_slopes) & 3))
+      return PA_ERR_INVALID_ARG;
     c.sinks = options->sinks;
     c.kv_layout = options->kv_layout;
+    c.sliding_window = options->sliding_window;
+    c.alibi_slopes = options->alibi_slopes;
+    c.alibi_sqrt = options->alibi_sqrt;
   }
   pa_status s = fwd_check(c);
   if (s != PA_OK || num_tokens == 0) return s;

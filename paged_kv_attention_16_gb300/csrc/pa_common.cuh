@@ -31,6 +31,8 @@ struct ReqInfo {
   int flags;          // ReqClass in bits 0..3, ReqFlags above
   int nsplit;         // KV splits per row (>= 1)
   int split_len;      // KV positions per split
+  int kv_base;        // first KV position of split 0 (16-aligned; > 0 only
+                      // with a sliding window, below which no row looks)
   long long partial_base;  // first partial row of this request (nsplit > 1)
 };
 
@@ -84,7 +86,24 @@ struct FwdParams {
   long long part_cap;
   unsigned int *status;
   const float *sinks;       // [num_heads] sink logits (natural-log units) or null
+  int window;               // sliding window in positions (0: none)
+  const float *alibi;       // [num_heads] ALiBi slopes (natural-log units) or null
+  int alibi_sqrt;           // 1: the bias grows with the square root of the distance
 };
+
+// First KV position the query at position `pos` sees: with a sliding window
+// W the W most recent positions pos - W < j <= pos ("vLLM Triton attention
+// backend deep dive", section "Usage scenarios": GPT-OSS behaviour).
+__host__ __device__ inline int window_lo(int pos, int window) {
+  return window > 0 && pos - window + 1 > 0 ? pos - window + 1 : 0;
+}
+
+// ALiBi bias of a key `dist` = pos - j positions back, in the base-2 score
+// domain (slope2 = slope * log2 e): -slope2 * dist, or -slope2 * sqrt(dist).
+// dist < 0 (a masked future key) is clamped so that sqrt stays defined.
+__device__ inline float alibi_bias(float slope2, float dist, int use_sqrt) {
+  return -slope2 * (use_sqrt ? sqrtf(fmaxf(dist, 0.f)) : dist);
+}
 
 constexpr float kLog2eF = 1.4426950408889634f;
 

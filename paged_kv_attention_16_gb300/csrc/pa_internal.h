@@ -62,6 +62,9 @@ struct FwdCall {
   int num_seqs, num_tokens, max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
   const float *sinks = nullptr;  // [num_heads] device array of sink logits, or null
   int kv_layout = PA_KV_NHD;     // pa_kv_layout of k_cache / v_cache
+  int sliding_window = 0;        // 0: none
+  const float *alibi_slopes = nullptr;  // [num_heads] device array, or null
+  int alibi_sqrt = 0;
 };
 // Host-side argument checks of pa_forward (PA_OK also when num_tokens == 0).
 pa_status fwd_check(const FwdCall &c);

@@ -108,6 +108,8 @@ struct RowDesc {
   int bad;        // a page of the split is outside the pool
   int tok, kvh, i, split, kv_lo, kv_hi, direct;
   int nsplit;
+  int mask_lo;      // first visible position (kv_lo is rounded down to a box)
+  int qpos;         // the query's position
   long long prow0;  // partial row of head 0 of the group (split partials)
 };
 
@@ -204,11 +206,13 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
         d.i = rem % r.q_len;
         d.tok = r.q_start + d.i;
         d.kvh = kvh;
-        const int kv_row_hi = r.ctx - r.q_len + d.i + 1;  // causal: 0 .. prefix + i
-        d.kv_lo = d.split * r.split_len;
-        d.kv_hi = min(kv_row_hi, d.kv_lo + r.split_len);
-        if (d.kv_lo >= d.kv_hi) continue;  // split past this row's causal bound
-        d.direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
+        d.qpos = r.ctx - r.q_len + d.i;  // causal: positions up to qpos
+        d.mask_lo = window_lo(d.qpos, p.window);
+        const int s_lo = r.kv_base + d.split * r.split_len;
+        d.kv_hi = min(d.qpos + 1, s_lo + r.split_len);
+        if (max(s_lo, d.mask_lo) >= d.kv_hi) continue;  // no visible position in this split
+        d.kv_lo = max(s_lo, d.mask_lo & ~15);  // copy boxes start on 16-slot bounds
+        d.direct = (d.mask_lo - r.kv_base) / r.split_len == (d.qpos - r.kv_base) / r.split_len;
         d.nsplit = r.nsplit;
         d.prow0 = r.partial_base + ((long long)d.i * H + kvh * G) * r.nsplit + d.split;
         pfirst = d.kv_lo / bs;
@@ -302,6 +306,11 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
 #pragma unroll
         for (int e = 0; e < C::E; ++e) qv[h][v * C::E + e] *= p.scale_log2;
       }
+    // ALiBi slopes of this thread's heads (base 2; zero without ALiBi)
+    float al[C::HPT];
+#pragma unroll
+    for (int h = 0; h < C::HPT; ++h)
+      al[h] = p.alibi ? __ldg(p.alibi + kvh * G + hg * C::HPT + h) * kLog2eF : 0.f;
     float m[C::HPT], l[C::HPT], o[C::HPT][C::DPT];
 #pragma unroll
     for (int h = 0; h < C::HPT; ++h) {
@@ -325,7 +334,8 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
 #pragma unroll
         for (int nb = 0; nb < C::NB; ++nb) {
           const int tl = (sb + nb) * C::TPS + slot_tok;
-          valid[nb] = d.kv_lo + j * C::ST + tl < d.kv_hi;
+          const int kpos = d.kv_lo + j * C::ST + tl;
+          valid[nb] = kpos < d.kv_hi && kpos >= d.mask_lo;
           float kf[C::DPT];
 #pragma unroll
           for (int v = 0; v < C::VPT; ++v)
@@ -340,6 +350,11 @@ __global__ void __maxnreg__(168) row_kernel(const __grid_constant__ CUtensorMap 
             part[h] = a0 + a1;
           }
           reduce_scores<C::HPT, C::LPT, C::LOG2_HPT>(part, sc[nb], lane, c);
+          if (p.alibi) {
+#pragma unroll
+            for (int h = 0; h < C::HPT; ++h)
+              sc[nb][h] += alibi_bias(al[h], (float)(d.qpos - kpos), p.alibi_sqrt);
+          }
         }
         // one max update for the batch (lazy: only when it grows by > 8)
 #pragma unroll

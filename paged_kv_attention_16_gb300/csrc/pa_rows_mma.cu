@@ -79,6 +79,8 @@ struct MmaRowCfg {
 struct MmaRowDesc {
   int done, bad;
   int tok, kvh, i, split, kv_lo, kv_hi, direct, nsplit;
+  int mask_lo;      // first visible position (kv_lo is rounded down to a box)
+  int qpos;         // the query's position
   long long prow0;  // partial row of head 0 of the group (split partials)
 };
 static_assert(sizeof(MmaRowDesc) <= 64, "descriptor slot is 64 bytes");
@@ -186,11 +188,13 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
         d.split = rem / r.q_len;
         d.i = rem % r.q_len;
         d.tok = r.q_start + d.i;
-        const int kv_row_hi = r.ctx - r.q_len + d.i + 1;  // causal: 0 .. prefix + i
-        d.kv_lo = d.split * r.split_len;
-        d.kv_hi = min(kv_row_hi, d.kv_lo + r.split_len);
-        if (d.kv_lo >= d.kv_hi) continue;  // split past this row's causal bound
-        d.direct = ceil_div_ll(kv_row_hi, r.split_len) == 1;
+        d.qpos = r.ctx - r.q_len + d.i;  // causal: positions up to qpos
+        d.mask_lo = window_lo(d.qpos, p.window);
+        const int s_lo = r.kv_base + d.split * r.split_len;
+        d.kv_hi = min(d.qpos + 1, s_lo + r.split_len);
+        if (max(s_lo, d.mask_lo) >= d.kv_hi) continue;  // no visible position in this split
+        d.kv_lo = max(s_lo, d.mask_lo & ~15);  // copy boxes start on 16-slot bounds
+        d.direct = (d.mask_lo - r.kv_base) / r.split_len == (d.qpos - r.kv_base) / r.split_len;
         d.nsplit = r.nsplit;
         d.prow0 = r.partial_base + ((long long)d.i * H + d.kvh * G) * r.nsplit + d.split;
         pfirst = d.kv_lo / bs;
@@ -259,7 +263,13 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
   // Q of the G heads as A fragments (rows >= G are zero): a0/a2 row gq,
   // a1/a3 row gq + 8; columns 16 ks + 2 tq (+8 for a2/a3).
   uint32_t qa[C::KS][4];
+  // ALiBi slopes of rows gq and gq + 8 (base 2; zero without ALiBi)
+  float al_lo = 0.f, al_hi = 0.f;
   auto load_q = [&](const MmaRowDesc &x) {
+    if (p.alibi) {
+      al_lo = gq < G ? __ldg(p.alibi + x.kvh * G + gq) * kLog2eF : 0.f;
+      al_hi = gq + 8 < G ? __ldg(p.alibi + x.kvh * G + gq + 8) * kLog2eF : 0.f;
+    }
     const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
         reinterpret_cast<const __nv_bfloat16 *>(p.q) + ((size_t)x.tok * H + x.kvh * G) * D);
 #pragma unroll
@@ -304,7 +314,9 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
     for (int j = 0; j < nst; ++j, ++g) {
       const int b = g % C::NSTAGE;
       mbar_wait(&full[b], (g / C::NSTAGE) & 1, dead, p.status);
-      const int nv = min(C::ROWS_W, d.kv_hi - (d.kv_lo + j * C::ST + r0));
+      const int box0 = d.kv_lo + j * C::ST + r0;  // position of this warp's first row
+      const int nv = min(C::ROWS_W, d.kv_hi - box0);
+      const int hv = d.mask_lo - box0;  // rows below it are outside the window
       const uint32_t kbase = ring_s + b * C::STAGE_BYTES;
       const uint32_t vbase = kbase + C::KV_BYTES;
       if (nv > 0) {
@@ -332,14 +344,17 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
             mma_16816(s[1], qa[ks], kb[2], kb[3]);
           }
         }
-        // ---- scale, mask, online softmax (rows gq and gq + 8)
+        // ---- scale, bias, mask, online softmax (rows gq and gq + 8)
         float mx_lo = -INFINITY, mx_hi = -INFINITY;
+        const float dist0 = (float)(d.qpos - box0);  // distance back to row 0 of the box
 #pragma unroll
         for (int n = 0; n < 2; ++n)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int col = n * 8 + 2 * tq + (e & 1);
-            s[n][e] = col < nv ? s[n][e] * sl2 : -INFINITY;
+            float v = s[n][e] * sl2;
+            if (p.alibi) v += alibi_bias(e < 2 ? al_lo : al_hi, dist0 - (float)col, p.alibi_sqrt);
+            s[n][e] = (col < nv && col >= hv) ? v : -INFINITY;
             if (e < 2) mx_lo = fmaxf(mx_lo, s[n][e]);
             else mx_hi = fmaxf(mx_hi, s[n][e]);
           }

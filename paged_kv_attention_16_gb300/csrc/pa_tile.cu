@@ -82,9 +82,10 @@ struct TileCfg {
 
 struct TileItem {
   int s, kvh, split, t0;
-  int q_start, q_len, prefix, nsplit, split_len;
+  int q_start, q_len, prefix, nsplit, split_len, kv_base;
   long long partial_base;
-  int kv_lo, kv_hi, nt;
+  int split_lo;           // first position of the split
+  int kv_lo, kv_hi, nt;   // loaded range (kv_lo on a 16-slot bound) and its tiles
 };
 
 __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int G, TileItem &it) {
@@ -107,12 +108,17 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
   it.prefix = r.ctx - r.q_len;
   it.nsplit = r.nsplit;
   it.split_len = r.split_len;
+  it.kv_base = r.kv_base;
   it.partial_base = r.partial_base;
   const int t_last = min(it.t0 + TQ, r.q_len) - 1;
-  it.kv_lo = it.split * r.split_len;
-  it.kv_hi = min(it.kv_lo + r.split_len, it.prefix + t_last + 1);
-  it.nt = it.kv_hi > it.kv_lo ? (it.kv_hi - it.kv_lo + kBN - 1) / kBN : 0;
-  return it.nt > 0;
+  // the first row of the tile sees the lowest positions (sliding window)
+  const int lo0 = window_lo(it.prefix + it.t0, p.window);
+  it.split_lo = r.kv_base + it.split * r.split_len;
+  it.kv_hi = min(it.split_lo + r.split_len, it.prefix + t_last + 1);
+  if (max(it.split_lo, lo0) >= it.kv_hi) return false;  // nothing visible in this split
+  it.kv_lo = max(it.split_lo, lo0 & ~15);
+  it.nt = (it.kv_hi - it.kv_lo + kBN - 1) / kBN;
+  return true;
 }
 
 template <int D>
@@ -303,14 +309,20 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       const int i = it.t0 + r / G;
       const int head = it.kvh * G + r % G;
       const bool row_valid = i < it.q_len;
-      const int row_hi_full = it.prefix + i + 1;
-      const int row_hi = row_valid ? min(row_hi_full, it.kv_lo + it.split_len) : it.kv_lo;
+      const int qpos = it.prefix + i;
+      const int row_hi_full = qpos + 1;
+      const int row_lo = window_lo(qpos, p.window);
+      const int row_hi = row_valid ? min(row_hi_full, it.split_lo + it.split_len) : it.kv_lo;
+      // this row has visible positions in the split
+      const bool row_in = row_valid && max(row_lo, it.split_lo) < row_hi;
+      const float al = p.alibi ? __ldg(p.alibi + head) * kLog2eF : 0.f;  // base-2 slope
       // Warps whose 32 rows are all padding (a decode tile holds G rows) keep
       // the barrier protocol but skip the TMEM traffic and the exponentials.
-      const bool warp_active = __any_sync(0xffffffffu, row_hi > it.kv_lo);
-      // exp2(s * c - m) as one FFMA needs c > 0; otherwise scale first.
+      const bool warp_active = __any_sync(0xffffffffu, row_in);
+      // exp2(s * c - m) as one FFMA needs c > 0 and no bias; otherwise scale
+      // (and bias) first, then mask, so that the mask wins whatever c's sign.
       const float c2 = p.scale_log2;
-      const bool fold = c2 > 0.f;
+      const bool fold = c2 > 0.f && !p.alibi;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.nt; ++j) {
         const uint32_t g = tiles + j;
@@ -330,14 +342,22 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           for (int x = 0; x < kBN; ++x) s[x] = __uint_as_float(raw[x]);
         }
         if (warp_active) {
-          // Only tiles that cross a row's bound need the select.
-          if (__any_sync(0xffffffffu, base + kBN > row_hi)) {
-#pragma unroll
-            for (int c = 0; c < kBN; ++c) s[c] = (base + c < row_hi) ? s[c] : -INFINITY;
-          }
           if (!fold) {
+            if (p.alibi) {
+              const float dist0 = (float)(qpos - base);
 #pragma unroll
-            for (int c = 0; c < kBN; ++c) s[c] *= c2;
+              for (int c = 0; c < kBN; ++c)
+                s[c] = fmaf(s[c], c2, alibi_bias(al, dist0 - (float)c, p.alibi_sqrt));
+            } else {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c) s[c] *= c2;
+            }
+          }
+          // Only tiles that cross a row's bounds need the select.
+          if (__any_sync(0xffffffffu, base + kBN > row_hi || base < row_lo)) {
+#pragma unroll
+            for (int c = 0; c < kBN; ++c)
+              s[c] = (base + c < row_hi && base + c >= row_lo) ? s[c] : -INFINITY;
           }
           // row max with 8 independent chains (a single chain is 64 deep)
           float mxa[8];
@@ -416,8 +436,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       const uint32_t glast = tiles + it.nt - 1;
       mbar_wait(&bar[kODone0 + (glast & 1)], (glast >> 1) & 1, dead, p.status);
       tc_fence_after();
-      const bool write = row_valid && row_hi > it.kv_lo;
-      const bool direct = ceil_div_ll(row_hi_full, it.split_len) == 1;
+      const bool write = row_in;
+      const bool direct =
+          (row_lo - it.kv_base) / it.split_len == (qpos - it.kv_base) / it.split_len;
       // partials are normalised by their own l; a row's own output also
       // counts its head's sink
       const float inv = direct ? sink_inv(p.sinks, head, m, l) : (l > 0.f ? 1.f / l : 0.f);

@@ -36,7 +36,9 @@ PA_K_COUNT = 8
 class ForwardOptions(ctypes.Structure):
     """pa_forward_options: sinks = device pointer to [num_heads] fp32 sink
     logits, or None."""
-    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int)]
+    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int),
+                ("sliding_window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("alibi_sqrt", ctypes.c_int)]
 
 
 def layout_code(kv_layout):
@@ -138,11 +140,12 @@ def _check(status, where):
 
 def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
                num_kv_heads, head_dim, block_size, scale, out, stream=None, *, max_seq_len,
-               kv_split_tokens=0, num_blocks=None, sinks=None, kv_layout="nhd", check=True):
+               kv_split_tokens=0, num_blocks=None, sinks=None, kv_layout="nhd",
+               sliding_window=0, alibi_slopes=None, alibi_sqrt=False, check=True):
     """Unified paged attention (see include/pa.h).  Shapes are read from the
-    tensors; max_seq_len is the host-known bound on seq_lens.  sinks (an
-    optional fp32 device tensor of num_heads sink logits) and an HND
-    kv_layout go through pa_forward_ex."""
+    tensors; max_seq_len is the host-known bound on seq_lens.  The options --
+    sinks and alibi_slopes (fp32 device tensors of num_heads values), an HND
+    kv_layout, a sliding window, sqrt ALiBi -- go through pa_forward_ex."""
     layout = layout_code(kv_layout)
     args = (
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
@@ -151,13 +154,16 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
         int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
         int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
         int(kv_split_tokens))
-    if sinks is None and layout == PA_KV_NHD:
+    if (sinks is None and layout == PA_KV_NHD and not sliding_window
+            and alibi_slopes is None):
         st, where = lib().pa_forward(*args), "pa_forward"
     else:
-        if isinstance(sinks, torch.Tensor) and (sinks.dtype != torch.float32
-                                                or sinks.numel() != num_heads):
-            raise TypeError("sinks must be a float32 tensor of num_heads elements")
-        opts = ForwardOptions(_ptr(sinks), layout)
+        for name, t in (("sinks", sinks), ("alibi_slopes", alibi_slopes)):
+            if isinstance(t, torch.Tensor) and (t.dtype != torch.float32
+                                                or t.numel() != num_heads):
+                raise TypeError(f"{name} must be a float32 tensor of num_heads elements")
+        opts = ForwardOptions(_ptr(sinks), layout, int(sliding_window), _ptr(alibi_slopes),
+                              int(bool(alibi_sqrt)))
         st, where = lib().pa_forward_ex(*args, ctypes.byref(opts)), "pa_forward_ex"
     if check:
         _check(st, where)
@@ -287,16 +293,20 @@ def to_device(batch, device="cuda"):
     return type(batch)(**fields)
 
 
-def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None):
-    """pa_forward on a device-resident PagedBatch (pa_forward_ex when sinks,
-    an fp32 device tensor of num_heads logits, is given); returns `out`."""
+def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None, sliding_window=0,
+            alibi_slopes=None, alibi_sqrt=False):
+    """pa_forward on a device-resident PagedBatch (pa_forward_ex when an
+    option is set: sinks / alibi_slopes as fp32 device tensors of num_heads
+    values, a sliding window, sqrt ALiBi, the batch's HND layout); returns
+    `out`."""
     if out is None:
         out = torch.empty_like(b.q)
     pa_forward(b.q, b.k_cache, b.v_cache, b.block_table, b.seq_lens, b.query_start_loc,
                b.num_heads, b.num_kv_heads, b.head_dim, b.block_size, b.scale, out, stream,
                max_seq_len=b.max_seq_len,
                kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens,
-               sinks=sinks, kv_layout=b.kv_layout)
+               sinks=sinks, kv_layout=b.kv_layout, sliding_window=sliding_window,
+               alibi_slopes=alibi_slopes, alibi_sqrt=alibi_sqrt)
     return out
 
 

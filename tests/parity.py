@@ -11,12 +11,15 @@ from paged_kv_attention_16_gb300 import inputs, pa
 TOL = {"f32": dict(max_abs=1e-4, mean_abs=1e-4), "bf16": dict(max_abs=2e-2, mean_abs=2e-3)}
 
 
-def oracle_forward(b, rows=None, sinks=None):
+def oracle_forward(b, rows=None, sinks=None, **variant):
+    """The oracle on batch b; variant: sliding_window, alibi_slopes,
+    alibi_sqrt (see oracle.paged_attention)."""
     return orc.paged_attention(
         inputs.storage_array(b.q), inputs.storage_array(b.k_cache),
         inputs.storage_array(b.v_cache), b.block_table.numpy(), b.seq_lens.numpy(),
         b.query_start_loc.numpy(), b.num_heads, b.num_kv_heads, b.head_dim, b.block_size,
-        b.scale, rows=rows, sinks=None if sinks is None else np.asarray(sinks, np.float64))
+        b.scale, rows=rows, sinks=None if sinks is None else np.asarray(sinks, np.float64),
+        kv_layout=b.kv_layout, **variant)
 
 
 def oracle_mla(b, rows=None):
@@ -25,11 +28,16 @@ def oracle_mla(b, rows=None):
                           b.block_size, b.scale, rows=rows)
 
 
-def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0, sinks=None):
+def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0, sinks=None,
+                sliding_window=0, alibi_slopes=None, alibi_sqrt=False):
     d = pa.to_device(b)
     if sinks is not None:
         sinks = torch.as_tensor(sinks, dtype=torch.float32).cuda()
-    got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens, sinks=sinks)
+    if alibi_slopes is not None:
+        alibi_slopes = torch.as_tensor(alibi_slopes, dtype=torch.float32).cuda()
+    got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens, sinks=sinks,
+                     sliding_window=sliding_window, alibi_slopes=alibi_slopes,
+                     alibi_sqrt=alibi_sqrt)
     status = pa.pa_get_device_status()
     assert status == expect_status, f"device status {status:#x}, expected {expect_status:#x}"
     return got.float().cpu().numpy().astype(np.float64)

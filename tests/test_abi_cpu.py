@@ -105,7 +105,9 @@ def test_cache_write_host_argument_checks(lib, kw, want):
 
 
 class _Options(ctypes.Structure):
-    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int)]
+    _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int),
+                ("sliding_window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
+                ("alibi_sqrt", ctypes.c_int)]
 
 
 def _forward_ex(lib, options, **kw):
@@ -135,7 +137,19 @@ def _forward_ex(lib, options, **kw):
     (None, -1, dict(), 1),
 ])
 def test_forward_ex_host_argument_checks(lib, sinks, layout, kw, want):
-    opts = _Options(sinks, layout)
+    opts = _Options(sinks, layout, 0, None, 0)
     assert _forward_ex(lib, ctypes.byref(opts), **kw) == want
     if sinks is None and layout == 0:
         assert _forward_ex(lib, None, **kw) == want  # null options: pa_forward
+
+
+@pytest.mark.parametrize("window,slopes,use_sqrt,kw,want", [
+    (128, 1 << 20, 1, dict(T=0), 0),
+    (-1, None, 0, dict(T=0), 1),            # negative window
+    (0, None, 2, dict(T=0), 1),             # alibi_sqrt neither 0 nor 1
+    (0, (1 << 20) + 2, 0, dict(T=0), 1),    # slopes not 4-byte aligned
+    (16, None, 0, dict(D=96), 2),           # the shape checks still apply
+])
+def test_forward_ex_variant_checks(lib, window, slopes, use_sqrt, kw, want):
+    opts = _Options(None, 0, window, slopes, use_sqrt)
+    assert _forward_ex(lib, ctypes.byref(opts), **kw) == want
