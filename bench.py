@@ -59,25 +59,37 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def kv_bytes(b):
+def kv_bytes(b, window=0):
+    """K and V bytes a step must read: every position some row of its request
+    sees (with a sliding window, from the first row's window start on)."""
     es = b.k_cache.element_size()
-    return int(b.seq_lens.to(torch.int64).sum()) * b.num_kv_heads * b.head_dim * es * 2
+    ctx = b.seq_lens.to(torch.int64)
+    if window:
+        qsl = b.query_start_loc.to(torch.int64)
+        first = (ctx - (qsl[1:] - qsl[:-1]) - window + 1).clamp(min=0)
+        ctx = ctx - first
+    return int(ctx.sum()) * b.num_kv_heads * b.head_dim * es * 2
 
 
 def io_bytes(b):
     return 2 * b.q.numel() * b.q.element_size()
 
 
-def attn_flops(b):
-    """4 * head_dim flops (QK and PV multiply-adds) per visible (row, key) pair."""
+def attn_flops(b, window=0):
+    """4 * head_dim flops (QK and PV multiply-adds) per visible (row, key)
+    pair; row i of a request sees pre + i + 1 keys, at most `window`."""
     qsl = b.query_start_loc.numpy().astype(np.int64)
     ctx = b.seq_lens.numpy().astype(np.int64)
     total = 0
     for s in range(b.num_seqs):
         ql = qsl[s + 1] - qsl[s]
         pre = ctx[s] - ql
-        # sum over i < ql of (pre + i + 1)
-        total += ql * pre + ql * (ql + 1) // 2
+        if window:
+            seen = np.minimum(pre + np.arange(ql, dtype=np.int64) + 1, window)
+            total += int(seen.sum())
+        else:
+            # sum over i < ql of (pre + i + 1)
+            total += ql * pre + ql * (ql + 1) // 2
     return 4 * b.head_dim * b.num_heads * total
 
 
@@ -281,6 +293,48 @@ def secondary_workloads(pa, flush, peaks):
                           "tokens": hb.num_tokens, "requests": hb.num_seqs,
                           "kernel_ms": kms}
     del b, out
+
+    # the model variants on the decode batch and the mixed batch: sinks, a
+    # sliding window (GB/s and TFLOPS count only what the window leaves
+    # visible), ALiBi and sqrt ALiBi; median of 5 rounds of 50 back-to-back
+    # steps, inputs larger than L2
+    var = {}
+    st = torch.cuda.current_stream()
+    for wl, maker in (("llama_decode_b64", lambda: inputs.llama_decode(64, poison=False)),
+                      ("mixed_qwen3", lambda: inputs.mixed_qwen3(poison=False))):
+        hb = maker()
+        b = pa.to_device(hb)
+        out = torch.empty_like(b.q)
+        H = hb.num_heads
+        g = torch.Generator().manual_seed(11)
+        sk = torch.randn(H, generator=g).cuda()
+        al = (2.0 ** (-8.0 * torch.arange(1, H + 1, dtype=torch.float32) / H)).cuda()
+        cases = {"plain": {}, "sinks": dict(sinks=sk), "window_128": dict(sliding_window=128),
+                 "window_1024": dict(sliding_window=1024), "alibi": dict(alibi_slopes=al),
+                 "alibi_sqrt": dict(alibi_slopes=al, alibi_sqrt=True)}
+        res_wl = {}
+        for name, kw in cases.items():
+            fn = lambda: pa.forward(b, out=out, **kw)  # noqa: E731
+            fn()
+            per = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda.synchronize()
+                e0.record(st)
+                for _ in range(50):
+                    fn()
+                e1.record(st)
+                e1.synchronize()
+                per.append(e0.elapsed_time(e1) / 50)
+            ms = statistics.median(per)
+            w = kw.get("sliding_window", 0)
+            gbs = kv_bytes(hb, w) / ms / 1e6
+            tf = attn_flops(hb, w) / ms / 1e9
+            res_wl[name] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm, "tflops": tf,
+                            "tensor_frac": tf / tfl}
+        var[wl] = res_wl
+        del b, out
+    res["variants"] = var
 
     hb = inputs.long_chunked(poison=False)
     b = pa.to_device(hb)

@@ -100,9 +100,15 @@ __host__ __device__ inline int window_lo(int pos, int window) {
 
 // ALiBi bias of a key `dist` = pos - j positions back, in the base-2 score
 // domain (slope2 = slope * log2 e): -slope2 * dist, or -slope2 * sqrt(dist).
-// dist < 0 (a masked future key) is clamped so that sqrt stays defined.
+// dist < 0 (a masked future key) is clamped so that sqrt stays defined.  The
+// square root is the single-instruction approximate one (relative error of
+// a few ulp): the bias feeds a softmax whose inputs are rounded far more
+// coarsely, and the exact root costs several instructions per score.
 __device__ inline float alibi_bias(float slope2, float dist, int use_sqrt) {
-  return -slope2 * (use_sqrt ? sqrtf(fmaxf(dist, 0.f)) : dist);
+  if (!use_sqrt) return -slope2 * dist;
+  float r;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(fmaxf(dist, 0.f)));
+  return -slope2 * r;
 }
 
 constexpr float kLog2eF = 1.4426950408889634f;
