@@ -270,3 +270,92 @@ def cache_write(k_new, v_new, k_cache, v_cache, block_table, seq_lens, query_sta
             k_out[page, pos % block_size] = k_new[qsl[s] + i]
             v_out[page, pos % block_size] = v_new[qsl[s] + i]
     return k_store, v_store, status
+
+
+def widen(a):
+    """Stored values as float64: float32 as is, uint16 bf16 bit patterns as
+    the exact binary32 they encode."""
+    a = np.asarray(a)
+    if a.dtype == np.uint16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    if a.dtype == np.float32:
+        return a.astype(np.float64)
+    raise TypeError(f"oracle inputs must be float32 or uint16 (bf16 bits), got {a.dtype}")
+
+
+def mla_prefill(q, kv_cache, w_kv, block_table, seq_lens, query_start_loc, kv_lora_rank,
+                qk_nope_dim, rope_dim, v_head_dim, block_size, scale, rows=None, q_block=64):
+    """fp64 non-absorbed MLA prefill / extend ("vLLM AMD ROCm attention backend
+    optimisation", section "AITER MLA backend: optimised for DeepSeek": prefill
+    and extend run a standard multi-head attention on the uncompressed
+    representation; decode works on the 576-wide compressed latent).
+
+    q        [T, H, qk_nope_dim + rope_dim]: each head's no-position part,
+             then its rotary part
+    kv_cache [num_blocks, block_size, kv_lora_rank + rope_dim]: per position
+             the latent c_j, then the rotary key k^R_j shared by all heads
+    w_kv     [H, qk_nope_dim + v_head_dim, kv_lora_rank]: head h's
+             up-projection; its first qk_nope_dim rows make the key, the
+             rest the value
+
+    The cache is decompressed position by position (a matrix product is the
+    step): for every visible position j of a request,
+        k_{j,h} = [ W_K,h c_j ; k^R_j ],   v_{j,h} = W_V,h c_j,
+    and query i of request s, at position p = seq_len - q_len + i, attends to
+    j <= p with the causal softmax of scale * q_{i,h} . k_{j,h}:
+        out_{i,h} = sum_j softmax_j(scale q_{i,h} . k_{j,h}) v_{j,h}.
+    rows: optional flat (token * H + head) indices; other rows are NaN.
+    Returns out [T, H, v_head_dim] float64."""
+    q = widen(q)
+    cache = widen(kv_cache)
+    w = widen(w_kv)
+    T, H, dqk = q.shape
+    assert dqk == qk_nope_dim + rope_dim
+    assert cache.shape[2] == kv_lora_rank + rope_dim
+    assert w.shape == (H, qk_nope_dim + v_head_dim, kv_lora_rank)
+    w_k, w_v = w[:, :qk_nope_dim, :], w[:, qk_nope_dim:, :]
+    qsl = [int(x) for x in query_start_loc]
+    S = len(seq_lens)
+    nb = cache.shape[0]
+    out = np.full((T, H, v_head_dim), np.nan)
+    want_tok = None
+    if rows is not None:
+        want_tok = np.zeros(T, bool)
+        want_tok[np.asarray(rows, np.int64) // H] = True
+    for s in range(S):
+        q_len, ctx = qsl[s + 1] - qsl[s], int(seq_lens[s])
+        if q_len <= 0:
+            continue
+        if q_len > ctx:
+            raise OracleError("q_len above the context")
+        toks = np.arange(qsl[s], qsl[s + 1])
+        if want_tok is not None and not want_tok[toks].any():
+            continue
+        # the request's latent rows through its block table
+        j = np.arange(ctx)
+        pages = np.asarray(block_table)[s, j // block_size].astype(np.int64)
+        if (pages < 0).any() or (pages >= nb).any():
+            raise OracleError("block id outside the pool")
+        lat = cache[pages, j % block_size]                    # [ctx, L + R]
+        c, k_rope = lat[:, :kv_lora_rank], lat[:, kv_lora_rank:]
+        k_nope = np.einsum("jl,hdl->jhd", c, w_k)              # [ctx, H, nope]
+        v = np.einsum("jl,hdl->jhd", c, w_v)                   # [ctx, H, dv]
+        prefix = ctx - q_len
+        for b0 in range(0, q_len, q_block):
+            ii = np.arange(b0, min(b0 + q_block, q_len))
+            if want_tok is not None and not want_tok[qsl[s] + ii].any():
+                continue
+            qb = q[qsl[s] + ii]                                # [n, H, dqk]
+            sc = (np.einsum("ihd,jhd->hij", qb[:, :, :qk_nope_dim], k_nope)
+                  + np.einsum("ihd,jd->hij", qb[:, :, qk_nope_dim:], k_rope)) * scale
+            visible = j[None, :] <= (prefix + ii)[:, None]      # [n, ctx]
+            sc = np.where(visible[None], sc, -np.inf)
+            mx = sc.max(axis=2, keepdims=True)
+            p = np.exp(sc - mx)
+            p /= p.sum(axis=2, keepdims=True)
+            out[qsl[s] + ii] = np.einsum("hij,jhd->ihd", p, v)
+    if rows is not None:
+        keep = np.zeros(T * H, bool)
+        keep[np.asarray(rows, np.int64)] = True
+        out.reshape(T * H, v_head_dim)[~keep] = np.nan
+    return out
