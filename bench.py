@@ -364,6 +364,38 @@ def secondary_workloads(pa, flush, peaks):
         res["mla_decode"] = {"unavailable": pa.status_string(st)}
     del m, out
 
+    # non-absorbed MLA prefill / extend: decompression (two GEMMs over every
+    # cached position) plus causal attention with 192-wide keys
+    hp = inputs.mla_prefill_deepseek(poison=False)
+    mp = pa.to_device(hp)
+    outp = torch.empty((hp.num_tokens, hp.num_heads, hp.v_head_dim), dtype=torch.bfloat16,
+                       device="cuda")
+    st = pa.pa_mla_prefill(mp.q, mp.kv_cache, mp.w_kv, mp.block_table, mp.seq_lens,
+                           mp.query_start_loc, hp.num_heads, hp.kv_lora_rank, hp.qk_nope_dim,
+                           hp.rope_dim, hp.v_head_dim, hp.block_size, hp.scale, outp,
+                           max_seq_len=hp.max_seq_len, max_total_kv=hp.max_total_kv,
+                           check=False)
+    if st == pa.PA_OK:
+        ms, kms = plain_and_profiled(pa, lambda: pa.mla_prefill(mp, out=outp), 10, flush)
+        ctx = hp.seq_lens.numpy().astype(np.int64)
+        qsl = hp.query_start_loc.numpy().astype(np.int64)
+        pairs = 0
+        for s_ in range(hp.num_seqs):
+            ql = qsl[s_ + 1] - qsl[s_]
+            pairs += ql * (ctx[s_] - ql) + ql * (ql + 1) // 2
+        att = pairs * hp.num_heads * 2 * (hp.qk_nope_dim + hp.rope_dim + hp.v_head_dim)
+        up = int(ctx.sum()) * hp.num_heads * 2 * hp.kv_lora_rank * (hp.qk_nope_dim + hp.v_head_dim)
+        tf = (att + up) / ms / 1e9
+        res["mla_prefill"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
+                              "attention_flops": att, "up_projection_flops": up,
+                              "tokens": hp.num_tokens, "kv_positions": int(ctx.sum()),
+                              "kernel_ms": kms}
+        if "tile" in kms:
+            res["mla_prefill"]["tile_tflops"] = att / kms["tile"] / 1e9
+    else:
+        res["mla_prefill"] = {"unavailable": pa.status_string(st)}
+    del mp, outp
+
     # KV-cache write of a prefill-sized step: 16 requests x 512 new tokens
     # (Llama-3.1-8B shapes); bytes = K and V rows read and written
     hb = inputs.paged_batch([512] * 16, [1024 + 256 * i for i in range(16)], 32, 8, 128, 16,
@@ -623,6 +655,12 @@ def run_only(args):
         out = torch.empty((m.num_seqs, m.num_heads, m.kv_lora_rank), dtype=torch.bfloat16,
                           device="cuda")
         fn = lambda: pa.mla_decode(m, out=out)  # noqa: E731
+    elif name == "mla_prefill":
+        host = inputs.mla_prefill_deepseek(poison=False)
+        m = pa.to_device(host)
+        out = torch.empty((host.num_tokens, host.num_heads, host.v_head_dim),
+                          dtype=torch.bfloat16, device="cuda")
+        fn = lambda: pa.mla_prefill(m, out=out)  # noqa: E731
     else:
         host = inputs.WORKLOADS[name](poison=False)
         b = pa.to_device(host)

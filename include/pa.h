@@ -259,6 +259,57 @@ size_t pa_mla_decode_workspace_bytes(int num_seqs, int num_heads,
                                      int kv_split_tokens);
 
 /*
+ * pa_mla_prefill -- non-absorbed MLA prefill and extend ("vLLM AMD ROCm
+ * attention backend optimisation", section "AITER MLA backend: optimised for
+ * DeepSeek": prefill and extend run a standard multi-head attention on the
+ * uncompressed representation, decode runs absorbed on the latent).  The
+ * latent cache is decompressed for every position a request can see,
+ *   k_{j,h} = [ W_K,h c_j ; k^R_j ]  (qk_nope_dim + rope_dim),
+ *   v_{j,h} = W_V,h c_j              (v_head_dim),
+ * and query i of request s, at position p = seq_len - q_len + i, attends
+ * causally (j <= p) with softmax(scale q_{i,h} . k_{j,h}).
+ *
+ *  q          [num_tokens, num_heads, qk_nope_dim + rope_dim] bf16: each
+ *             head's no-position part, then its rotary part
+ *  kv_cache   [num_blocks, block_size, kv_lora_rank + rope_dim] bf16: per
+ *             position the latent c_j, then the rotary key k^R_j shared by
+ *             all heads (the pa_mla_decode cache)
+ *  w_kv       [num_heads, qk_nope_dim + v_head_dim, kv_lora_rank] bf16:
+ *             head h's up-projection, key rows first, then value rows
+ *  block_table, seq_lens, query_start_loc: as for pa_forward (seq_lens
+ *             include the new tokens, whose latents are already cached)
+ *  out        [num_tokens, num_heads, v_head_dim] bf16, fully overwritten
+ *  A bad block id in a request's context sets PA_DEV_BAD_BLOCK and zeroes
+ *  that request's rows.
+ *  Supported: kv_lora_rank 512, rope_dim 64, qk_nope_dim 128, v_head_dim
+ *  128, any num_heads and block_size >= 1; kv_split_tokens as for pa_forward.
+ *  max_seq_len    host-known bound on seq_lens
+ *  max_total_kv   host-known bound on the sum of seq_lens (sizes the
+ *                 decompressed keys and values: about 81 KB per position at
+ *                 128 heads); a batch beyond it sets PA_DEV_OVERFLOW and
+ *                 writes zeros
+ * The up-projection runs as two cuBLAS GEMMs (bf16 in, fp32 accumulation,
+ * bf16 keys and values), loaded at run time; without cuBLAS the call returns
+ * PA_ERR_UNSUPPORTED.  The attention is pa_forward's tensor-core tile kernel
+ * with q and k rows of 192 and v rows of 128.  Status bits and errors as for
+ * pa_forward; PA_ERR_UNSUPPORTED for other dimensions.
+ */
+pa_status pa_mla_prefill(const void *q, const void *kv_cache, const void *w_kv,
+                         const int32_t *block_table, const int32_t *seq_lens,
+                         const int32_t *query_start_loc, int num_heads,
+                         int kv_lora_rank, int qk_nope_dim, int rope_dim,
+                         int v_head_dim, int block_size, float scale, void *out,
+                         void *stream, int num_seqs, int num_tokens,
+                         int max_blocks_per_seq, int num_blocks, int max_seq_len,
+                         long long max_total_kv, int kv_split_tokens);
+
+/* Workspace bytes pa_mla_prefill needs for these host-known extents. */
+size_t pa_mla_prefill_workspace_bytes(int num_seqs, int num_tokens,
+                                      int num_heads, int max_seq_len,
+                                      long long max_total_kv,
+                                      int kv_split_tokens);
+
+/*
  * pa_reserve -- make sure the calling thread's current device has at least
  * `bytes` of library-owned workspace (split partials, planner tables, work
  * counters).  Call it before capturing a graph: during capture the library

@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
       // Decode rows stream through the row kernel (warp MMAs for bf16, at
       // most 16 query rows per KV head); extend and prefill rows fill
       // 128-row tiles of the tcgen05 tile kernel when it applies.
-      const bool row_path = !p.tile_ok || r.cls == kDecode;
+      const bool row_path = !p.tile_ok || (r.cls == kDecode && !p.all_tile);
       int len;
       if (r.cls == kDecode) {
         len = L;
@@ -722,7 +722,8 @@ size_t fwd_workspace_bytes(const FwdCall &c) {
 pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, int num_sms,
                      cudaStream_t st, bool timed) {
   const int group = c.num_heads / c.num_kv_heads;
-  const bool tile_ok = tile_path_ok(c.dtype, c.head_dim, group);
+  const int dqk = c.head_dim_qk > 0 ? c.head_dim_qk : c.head_dim;
+  const bool tile_ok = c.all_tile || tile_path_ok(c.dtype, c.head_dim, group);
   const FwdLayout lay = fwd_layout(c.num_seqs, c.num_tokens, c.num_heads, c.head_dim,
                                    c.max_seq_len, c.kv_split_tokens, tile_ok);
   const int row_ctas = row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * num_sms;
@@ -760,6 +761,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.window = c.sliding_window;
   p.alibi = c.alibi_slopes;
   p.alibi_sqrt = c.alibi_sqrt;
+  p.head_dim_qk = dqk;
+  p.all_tile = c.all_tile ? 1 : 0;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
   // One thread per request, whole warps, at most kPlanThreads: small batches
@@ -792,7 +795,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
           hnd ? (unsigned long long)c.block_size * row : row,
           (unsigned long long)c.block_size * c.num_kv_heads * row};
       const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
-      if (!encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true) ||
+      // (all-tile calls have no row items: their K rows may be wider than V's)
+      if ((!c.all_tile && !encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true)) ||
           !encode_tiled(&tm_vr, c.v_cache, c.dtype, 5, dims, strides, box, true))
         return PA_ERR_CUDA;
     }
@@ -800,12 +804,14 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     // and 16 slots, so the S product sees a uniform row stride.
     CUtensorMap tm_kt;
     if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.kv_layout, c.num_blocks,
-                                     c.block_size, c.num_kv_heads, c.head_dim, 64, 16,
+                                     c.block_size, c.num_kv_heads, dqk, 64, 16,
                                      CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
-    cudaError_t row_err;
+    cudaError_t row_err = cudaSuccess;
     slot = timed ? prof_begin(PA_K_ROW, st) : -1;
-    if (mma_rows) {
+    if (c.all_tile) {
+      // no row items: the row kernel is not launched
+    } else if (mma_rows) {
       row_err = launch_row_mma_kernel(p, tm_kr, tm_vr, row_ctas, st);
     } else {
       // fp32: whole rows of head_dim elements, no swizzle (CUDA-core kernel)
@@ -826,9 +832,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
       // G heads x (128 / G) tokens.
       CUtensorMap tm_q;
       EncodeTiledFn fn = encode_fn();
-      cuuint64_t qd[3] = {(cuuint64_t)c.head_dim, (cuuint64_t)c.num_heads,
-                          (cuuint64_t)c.num_tokens};
-      cuuint64_t qs[2] = {(cuuint64_t)c.head_dim * 2, (cuuint64_t)c.num_heads * c.head_dim * 2};
+      cuuint64_t qd[3] = {(cuuint64_t)dqk, (cuuint64_t)c.num_heads, (cuuint64_t)c.num_tokens};
+      cuuint64_t qs[2] = {(cuuint64_t)dqk * 2, (cuuint64_t)c.num_heads * dqk * 2};
       cuuint32_t qb[3] = {64, (cuuint32_t)group, (cuuint32_t)(kTileRows / group)};
       cuuint32_t qe[3] = {1, 1, 1};
       if (!fn ||

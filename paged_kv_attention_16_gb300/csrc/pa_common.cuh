@@ -87,6 +87,9 @@ struct FwdParams {
   unsigned int *status;
   const float *sinks;       // [num_heads] sink logits (natural-log units) or null
   int window;               // sliding window in positions (0: none)
+  int head_dim_qk;          // width of q / k rows when it differs from head_dim
+                            // (the value / output width); 0: the same
+  int all_tile;             // 1: every row, decode included, on the tile kernel
   const float *alibi;       // [num_heads] ALiBi slopes (natural-log units) or null
   int alibi_sqrt;           // 1: the bias grows with the square root of the distance
 };

@@ -65,6 +65,10 @@ struct FwdCall {
   int sliding_window = 0;        // 0: none
   const float *alibi_slopes = nullptr;  // [num_heads] device array, or null
   int alibi_sqrt = 0;
+  // Non-absorbed MLA prefill: q and k rows of head_dim_qk (0: head_dim)
+  // elements, v and out rows of head_dim, every row on the tile kernel.
+  int head_dim_qk = 0;
+  bool all_tile = false;
 };
 // Host-side argument checks of pa_forward (PA_OK also when num_tokens == 0).
 pa_status fwd_check(const FwdCall &c);

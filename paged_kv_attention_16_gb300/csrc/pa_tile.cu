@@ -43,7 +43,7 @@ namespace {
 constexpr int kBN = 64;
 constexpr int kBox = 16;           // slots per TMA box
 constexpr int kTileThreads = 192;  // 4 softmax warps, 1 producer warp, 1 MMA warp
-constexpr int kKStages = 2;        // K tiles in flight per CTA
+constexpr int kKStages = 2;        // K tiles in flight per CTA (at most; see TileCfg::KST)
 constexpr int kVStages = 2;        // V tiles in flight per CTA
 constexpr int kTileCtasPerSm = kBN == 64 ? 2 : 1;  // resident CTAs per SM (grid = SMs x this)
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
@@ -53,6 +53,7 @@ constexpr uint32_t kTmemCols = kBN == 64 ? 256 : 512;
 // them.
 constexpr uint32_t kTmemS = 0;        // S buffer b: columns [kBN b, kBN b + kBN)
 constexpr uint32_t kTmemO = 2 * kBN;  // O: columns [2 kBN, 2 kBN + head_dim)
+constexpr uint32_t kSBufsCols = kTmemO;
 
 // S buffer b = tile & 1: kSFull0 + b (S product done), kPFull0 + b (P
 // written over it), kODone0 + b (the PV product that read P is done: the
@@ -63,21 +64,30 @@ constexpr int kVFull0 = kKFree0 + kKStages;
 constexpr int kVFree0 = kVFull0 + kVStages;
 constexpr int kNumBars = kVFree0 + kVStages;
 
-template <int D>
+// DQK: width of the query / key rows (the S product's K dimension); DV:
+// width of the value / output rows.  They differ for the non-absorbed MLA
+// prefill (192 = 128 + 64 rotary, and 128).
+template <int DQK, int DV>
 struct TileCfg {
-  static constexpr int NH = D / 64;                 // 128-byte halves of a row
-  static constexpr int Q_BYTES = NH * 128 * 128;    // 128 rows x 128 B per half
-  static constexpr int KV_HALF = kBN * 128;         // one half of a K tile
-  static constexpr int KV_BYTES = NH * KV_HALF;
-  static constexpr int V_BOX = NH * kBox * 128;     // one V box: [halves][16 rows][128 B]
+  static constexpr int NHQ = DQK / 64;              // 128-byte chunks of a Q / K row
+  static constexpr int NHV = DV / 64;               // 128-byte chunks of a V / O row
+  static constexpr int Q_BYTES = NHQ * 128 * 128;   // 128 rows x 128 B per chunk
+  static constexpr int KV_HALF = kBN * 128;         // one 64-wide chunk of a K tile
+  static constexpr int K_BYTES = NHQ * KV_HALF;
+  static constexpr int V_BYTES = NHV * KV_HALF;
+  static constexpr int V_BOX = NHV * kBox * 128;    // one V box: [chunks][16 rows][128 B]
+  // K stages: two while they fit two CTAs per SM beside Q and two V stages
+  static constexpr int KST = Q_BYTES + 2 * K_BYTES + kVStages * V_BYTES <= 100 * 1024 ? 2 : 1;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + kKStages * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_V + kVStages * KV_BYTES;
+  static constexpr int OFF_V = OFF_K + KST * K_BYTES;
+  static constexpr int OFF_BAR = OFF_V + kVStages * V_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
   static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
-  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, D, 1);
+  static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, DV, 1);
+  static_assert(DQK % 64 == 0 && DQK <= 256 && (DV == 64 || DV == 128), "tile widths");
+  static_assert(kSBufsCols + DV <= kTmemCols, "TMEM budget");
 };
 
 struct TileItem {
@@ -121,11 +131,11 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
   return true;
 }
 
-template <int D>
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
-  using C = TileCfg<D>;
+  using C = TileCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled operand tiles need 1024-byte alignment.
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -174,7 +184,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       if (lane == 0) {
         if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
         mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
-        for (int h = 0; h < C::NH; ++h)
+        for (int h = 0; h < C::NHQ; ++h)
           tma_load_3d(sQ + h * 128 * 128, &tm_q, h * 64, it.kvh * G, it.q_start + it.t0,
                       &bar[kQFull]);
       }
@@ -194,21 +204,22 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           uint8_t *dst;
           const CUtensorMap *map;
           if (which == 0) {
-            const int st = g % kKStages;
+            const int st = g % C::KST;
             full = &bar[kKFull0 + st];
-            dst = sK + st * C::KV_BYTES;
+            dst = sK + st * C::K_BYTES;
             map = &tm_k;
-            if (lane == 0 && g >= kKStages)
-              mbar_wait(&bar[kKFree0 + st], ((g / kKStages) - 1) & 1, dead, p.status);
+            if (lane == 0 && g >= C::KST)
+              mbar_wait(&bar[kKFree0 + st], ((g / C::KST) - 1) & 1, dead, p.status);
           } else {
             const int st = g % kVStages;
             full = &bar[kVFull0 + st];
-            dst = sV + st * C::KV_BYTES;
+            dst = sV + st * C::V_BYTES;
             map = &tm_v;
             if (lane == 0 && g >= kVStages)
               mbar_wait(&bar[kVFree0 + st], ((g / kVStages) - 1) & 1, dead, p.status);
           }
-          if (lane == 0) mbar_arrive_expect_tx(full, __popc(mask) * C::NH * kBox * 128);
+          if (lane == 0)
+            mbar_arrive_expect_tx(full, __popc(mask) * (which == 0 ? C::NHQ : C::NHV) * kBox * 128);
           __syncwarp();
           // K: one box per 64-dim half ([halves][64 rows] for the S product's
           // uniform row stride); V: one box per 16 slots with both halves
@@ -216,7 +227,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           // box), half as many TMA boxes.
           if (ok) {
             if (which == 0) {
-              for (int h = 0; h < C::NH; ++h)
+              for (int h = 0; h < C::NHQ; ++h)
                 tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh,
                             pos % bs, page, full);
             } else {
@@ -237,13 +248,13 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       // S of tile g into buffer g & 1, once the PV product of tile g - 2
       // (which read P from that buffer) is done.
       auto issue_s = [&](uint32_t g) {
-        const int st = g % kKStages, sb = g & 1;
-        mbar_wait(&bar[kKFull0 + st], (g / kKStages) & 1, dead, p.status);
+        const int st = g % C::KST, sb = g & 1;
+        mbar_wait(&bar[kKFull0 + st], (g / C::KST) & 1, dead, p.status);
         if (g >= 2) mbar_wait(&bar[kODone0 + sb], ((g - 2) >> 1) & 1, dead, p.status);
         tc_fence_after();
-        const uint32_t kb = sk + st * C::KV_BYTES;
+        const uint32_t kb = sk + st * C::K_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
+        for (int kk = 0; kk < DQK / 16; ++kk) {
           const int h = kk / 4, sub = kk % 4;
           const uint64_t a = umma_desc_sw128(sq + h * 128 * 128 + sub * 32, 16, 1024);
           const uint64_t b = umma_desc_sw128(kb + h * C::KV_HALF + sub * 32, 16, 1024);
@@ -265,7 +276,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           mbar_wait(&bar[kVFull0 + vs], (g / kVStages) & 1, dead, p.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
           tc_fence_after();
-          const uint32_t vb = sv + vs * C::KV_BYTES;
+          const uint32_t vb = sv + vs * C::V_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
             const uint64_t b = umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
@@ -382,7 +393,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
             tc_fence_after();
             const float a = rescale ? alpha : 1.f;
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int c0 = 0; c0 < DV; c0 += 32) {
               uint32_t raw[32];
               tc_ld32(tmem + lane_off + kTmemO + c0, raw);
               tc_wait_ld();
@@ -417,8 +428,8 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           const int vst = g % kVStages;
           mbar_wait(&bar[kVFull0 + vst], (g / kVStages) & 1, dead, p.status);
           const int first = it.kv_hi - base;
-          const int nchunks = (kBN - first) * 8 * C::NH;
-          uint8_t *vs = sV + vst * C::KV_BYTES;
+          const int nchunks = (kBN - first) * 8 * C::NHV;
+          uint8_t *vs = sV + vst * C::V_BYTES;
           for (int e = r; e < nchunks; e += 128) {
             const int h = e / ((kBN - first) * 8);
             const int rem = e % ((kBN - first) * 8);
@@ -446,7 +457,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       const size_t tok = (size_t)it.q_start + i;
       const long long prow = it.partial_base + ((long long)i * H + head) * it.nsplit + it.split;
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
+      for (int c0 = 0; c0 < DV; c0 += 32) {
         if (!warp_active) break;
         uint32_t raw[32];
         tc_ld32(tmem + lane_off + kTmemO + c0, raw);
@@ -456,7 +467,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
         if (write) {
           if (direct) {
             uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) +
-                                                   (tok * H + head) * D + c0);
+                                                   (tok * H + head) * DV + c0);
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               uint32_t w[4];
@@ -470,7 +481,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
               dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
             }
           } else {
-            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * D + c0);
+            float4 *dst = reinterpret_cast<float4 *>(p.part_o + prow * DV + c0);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[v] = make_float4(__uint_as_float(raw[4 * v]) * inv,
@@ -495,18 +506,18 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   if (warp == 5) tc_dealloc(tmem, kTmemCols);
 }
 
-template <int D>
+template <int DQK, int DV>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                      const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
-  using C = TileCfg<D>;
-  cudaError_t e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       C::SMEM);
+  using C = TileCfg<DQK, DV>;
+  cudaError_t e = cudaFuncSetAttribute(tile_kernel<DQK, DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tile_kernel<D>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(tile_kernel<DQK, DV>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_dependent(tile_kernel<D>, dim3(num_sms * kTileCtasPerSm), dim3(kTileThreads), C::SMEM,
-                          stream, tq, tk, tv, p);
+  return launch_dependent(tile_kernel<DQK, DV>, dim3(num_sms * kTileCtasPerSm),
+                          dim3(kTileThreads), C::SMEM, stream, tq, tk, tv, p);
 }
 
 }  // namespace
@@ -519,8 +530,10 @@ bool tile_kernel_supported(int dtype, int head_dim, int group) {
 cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
                                const CUtensorMap &tm_k, const CUtensorMap &tm_v, int num_sms,
                                cudaStream_t stream) {
-  if (p.head_dim == 128) return launch_d<128>(p, tm_q, tm_k, tm_v, num_sms, stream);
-  if (p.head_dim == 64) return launch_d<64>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  const int dqk = p.head_dim_qk > 0 ? p.head_dim_qk : p.head_dim;
+  if (dqk == 128 && p.head_dim == 128) return launch_d<128, 128>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  if (dqk == 64 && p.head_dim == 64) return launch_d<64, 64>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  if (dqk == 192 && p.head_dim == 128) return launch_d<192, 128>(p, tm_q, tm_k, tm_v, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -197,6 +197,64 @@ def mla_batch(ctx_lens, num_heads=128, kv_lora_rank=512, rope_dim=64, block_size
                     kv_split_tokens=kv_split_tokens)
 
 
+@dataclass
+class MlaPrefillBatch:
+    q: torch.Tensor          # [T, H, qk_nope_dim + rope_dim]
+    kv_cache: torch.Tensor   # [num_blocks, block_size, kv_lora_rank + rope_dim]
+    w_kv: torch.Tensor       # [H, qk_nope_dim + v_head_dim, kv_lora_rank]
+    block_table: torch.Tensor
+    seq_lens: torch.Tensor
+    query_start_loc: torch.Tensor
+    num_heads: int
+    kv_lora_rank: int
+    qk_nope_dim: int
+    rope_dim: int
+    v_head_dim: int
+    block_size: int
+    scale: float
+    dtype: str
+    max_seq_len: int
+    max_total_kv: int
+    kv_split_tokens: int = 0
+
+    @property
+    def num_seqs(self):
+        return int(self.seq_lens.shape[0])
+
+    @property
+    def num_tokens(self):
+        return int(self.q.shape[0])
+
+
+def mla_prefill_batch(q_lens, ctx_lens, num_heads=128, kv_lora_rank=512, qk_nope_dim=128,
+                      rope_dim=64, v_head_dim=128, block_size=64, seed=0, poison=True,
+                      slack=0.1, kv_split_tokens=0):
+    """Non-absorbed MLA prefill / extend inputs: queries of qk_nope_dim +
+    rope_dim per head, the latent cache of pa_mla_decode, and a synthetic
+    up-projection w_kv drawn N(0, 1 / kv_lora_rank) (so decompressed keys
+    and values have unit variance); scale 1/sqrt(qk_nope_dim + rope_dim)."""
+    q_lens = [int(x) for x in q_lens]
+    ctx_lens = [int(x) for x in ctx_lens]
+    g_layout = _gen(seed * 7919 + 5)
+    g_vals = _gen(seed * 104729 + 6)
+    table, pool, _ = _place_pages(ctx_lens, block_size, g_layout, slack, None, poison)
+    dqk = qk_nope_dim + rope_dim
+    q = _normal((sum(q_lens), num_heads, dqk), g_vals, "bf16")
+    kv = _normal((pool, block_size, kv_lora_rank + rope_dim), g_vals, "bf16")
+    w = (torch.randn((num_heads, qk_nope_dim + v_head_dim, kv_lora_rank), generator=g_vals)
+         / math.sqrt(kv_lora_rank)).to(torch.bfloat16)
+    if poison:
+        _poison_cache([kv], table, ctx_lens, block_size, pool)
+    qsl = torch.tensor([0] + list(np.cumsum(q_lens)), dtype=torch.int32)
+    return MlaPrefillBatch(q=q, kv_cache=kv, w_kv=w, block_table=table,
+                           seq_lens=torch.tensor(ctx_lens, dtype=torch.int32),
+                           query_start_loc=qsl, num_heads=num_heads, kv_lora_rank=kv_lora_rank,
+                           qk_nope_dim=qk_nope_dim, rope_dim=rope_dim, v_head_dim=v_head_dim,
+                           block_size=block_size, scale=1.0 / math.sqrt(dqk), dtype="bf16",
+                           max_seq_len=max(ctx_lens + [1]), max_total_kv=sum(ctx_lens),
+                           kv_split_tokens=kv_split_tokens)
+
+
 def _uniform_ints(gen, n, lo, hi):
     """n integers uniform on [lo, hi] (both ends included)."""
     if n == 0:
@@ -262,6 +320,20 @@ def mla_decode_batch(batch=64, poison=True, seed=4):
     return mla_batch(ctx, 128, 512, 64, 64, dtype="bf16", seed=seed, poison=poison)
 
 
+def mla_prefill_deepseek(poison=True, seed=5, n_prefill=4, n_extend=4):
+    """DeepSeek-style non-absorbed MLA prefill / extend: 128 heads, latent 512
+    + rope 64, key rows 128 + 64, value rows 128, block_size 64, bf16; 4
+    prefills of 512-2048 tokens and 4 extends of 128-512 new tokens on 1K-4K
+    cached."""
+    g = _gen(1234 + 5)
+    pre = _uniform_ints(g, n_prefill, 512, 2048)
+    ext_new = _uniform_ints(g, n_extend, 128, 512)
+    ext_pre = _uniform_ints(g, n_extend, 1024, 4096)
+    q_lens = pre + ext_new
+    ctx = pre + [a + b for a, b in zip(ext_new, ext_pre)]
+    return mla_prefill_batch(q_lens, ctx, seed=seed, poison=poison)
+
+
 WORKLOADS = {
     "tiny_decode_f32": tiny_decode_f32,
     "llama_decode_b1": lambda poison=True: llama_decode(1, poison),
@@ -269,6 +341,7 @@ WORKLOADS = {
     "mixed_qwen3": mixed_qwen3,
     "long_chunked": long_chunked,
     "mla_decode": mla_decode_batch,
+    "mla_prefill": mla_prefill_deepseek,
 }
 
 

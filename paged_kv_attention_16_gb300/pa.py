@@ -29,7 +29,8 @@ PA_KV_NHD, PA_KV_HND = 0, 1  # pa_kv_layout
 EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cache_write",
            "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
-           "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch", "pa_forward_ex")
+           "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch", "pa_forward_ex",
+           "pa_mla_prefill", "pa_mla_prefill_workspace_bytes")
 PA_K_COUNT = 8
 
 
@@ -99,6 +100,13 @@ def lib():
         L.pa_forward_static_scratch.restype = c_int
         L.pa_forward_ex.argtypes = L.pa_forward.argtypes + [ctypes.POINTER(ForwardOptions)]
         L.pa_forward_ex.restype = c_int
+        L.pa_mla_prefill.argtypes = [vp, vp, vp, i32p, i32p, i32p, c_int, c_int, c_int, c_int,
+                                     c_int, c_int, c_float, vp, vp, c_int, c_int, c_int, c_int,
+                                     c_int, ctypes.c_longlong, c_int]
+        L.pa_mla_prefill.restype = c_int
+        L.pa_mla_prefill_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int,
+                                                     ctypes.c_longlong, c_int]
+        L.pa_mla_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.pa_kernel_name.argtypes = [c_int]
         L.pa_kernel_name.restype = ctypes.c_char_p
         _lib = L
@@ -307,6 +315,37 @@ def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None, sliding_
                kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens,
                sinks=sinks, kv_layout=b.kv_layout, sliding_window=sliding_window,
                alibi_slopes=alibi_slopes, alibi_sqrt=alibi_sqrt)
+    return out
+
+
+def pa_mla_prefill(q, kv_cache, w_kv, block_table, seq_lens, query_start_loc, num_heads,
+                   kv_lora_rank, qk_nope_dim, rope_dim, v_head_dim, block_size, scale, out,
+                   stream=None, *, max_seq_len, max_total_kv, kv_split_tokens=0, num_blocks=None,
+                   check=True):
+    """Non-absorbed MLA prefill / extend (see include/pa.h)."""
+    st = lib().pa_mla_prefill(
+        _ptr(q), _ptr(kv_cache), _ptr(w_kv), _ptr(block_table), _ptr(seq_lens),
+        _ptr(query_start_loc), int(num_heads), int(kv_lora_rank), int(qk_nope_dim),
+        int(rope_dim), int(v_head_dim), int(block_size), float(scale), _ptr(out),
+        _stream_ptr(stream), int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
+        int(num_blocks if num_blocks is not None else kv_cache.shape[0]), int(max_seq_len),
+        int(max_total_kv), int(kv_split_tokens))
+    if check:
+        _check(st, "pa_mla_prefill")
+    return st
+
+
+def mla_prefill(b, out=None, stream=None, kv_split_tokens=None):
+    """pa_mla_prefill on a device-resident MlaPrefillBatch; returns `out`."""
+    if out is None:
+        out = torch.empty((b.num_tokens, b.num_heads, b.v_head_dim), dtype=b.q.dtype,
+                          device=b.q.device)
+    pa_mla_prefill(b.q, b.kv_cache, b.w_kv, b.block_table, b.seq_lens, b.query_start_loc,
+                   b.num_heads, b.kv_lora_rank, b.qk_nope_dim, b.rope_dim, b.v_head_dim,
+                   b.block_size, b.scale, out, stream, max_seq_len=b.max_seq_len,
+                   max_total_kv=b.max_total_kv,
+                   kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None
+                   else kv_split_tokens)
     return out
 
 

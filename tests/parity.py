@@ -79,3 +79,11 @@ def sample_rows(b, n_other, seed=0, all_decode=True):
 
 def cuda_ok():
     return torch.cuda.is_available()
+
+
+def oracle_mla_prefill(b, rows=None):
+    return orc.mla_prefill(inputs.storage_array(b.q), inputs.storage_array(b.kv_cache),
+                           inputs.storage_array(b.w_kv), b.block_table.numpy(),
+                           b.seq_lens.numpy(), b.query_start_loc.numpy(), b.kv_lora_rank,
+                           b.qk_nope_dim, b.rope_dim, b.v_head_dim, b.block_size, b.scale,
+                           rows=rows)

@@ -153,3 +153,28 @@ def test_forward_ex_host_argument_checks(lib, sinks, layout, kw, want):
 def test_forward_ex_variant_checks(lib, window, slopes, use_sqrt, kw, want):
     opts = _Options(None, 0, window, slopes, use_sqrt)
     assert _forward_ex(lib, ctypes.byref(opts), **kw) == want
+
+
+def _mla_prefill(lib, **kw):
+    args = dict(q=1 << 20, c=1 << 20, w=1 << 20, bt=1 << 20, sl=1 << 20, qsl=1 << 20, H=128,
+                L=512, nope=128, R=64, dv=128, bs=64, scale=0.07, out=1 << 20, stream=None, S=1,
+                T=1, mbps=4, nb=4, msl=64, tot=64, kvs=0)
+    args.update(kw)
+    f = lib.pa_mla_prefill
+    f.restype = ctypes.c_int
+    vp, ci = ctypes.c_void_p, ctypes.c_int
+    f.argtypes = [vp] * 6 + [ci] * 6 + [ctypes.c_float, vp, vp] + [ci] * 5 + [
+        ctypes.c_longlong, ci]
+    a = args
+    return f(a["q"], a["c"], a["w"], a["bt"], a["sl"], a["qsl"], a["H"], a["L"], a["nope"],
+             a["R"], a["dv"], a["bs"], a["scale"], a["out"], a["stream"], a["S"], a["T"],
+             a["mbps"], a["nb"], a["msl"], a["tot"], a["kvs"])
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(H=0), 1), (dict(S=-1), 1), (dict(tot=-1), 1), (dict(bs=0), 1),
+    (dict(L=256), 2), (dict(R=32), 2), (dict(nope=64), 2), (dict(dv=64), 2), (dict(kvs=24), 2),
+    (dict(T=0), 0), (dict(q=0), 1), (dict(w=0), 1), (dict(out=(1 << 20) + 2), 1),
+])
+def test_mla_prefill_host_argument_checks(lib, kw, want):
+    assert _mla_prefill(lib, **kw) == want
