@@ -802,11 +802,32 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     }
     // The tile kernel's K: one 64-element (128-byte) swizzled box per half
     // and 16 slots, so the S product sees a uniform row stride.
-    CUtensorMap tm_kt;
+    // When every 64-position tile lies in one page (block_size a multiple of
+    // 64; tiles start at multiples of 64: no window, splits of a multiple of
+    // 64), the tile kernel loads a whole tile's K chunk or V rows as one box.
+    const bool page_boxes = tile_ok && c.dtype == PA_BF16 && c.block_size % 64 == 0 &&
+                            c.sliding_window == 0 && c.kv_split_tokens % 64 == 0;
+    p.tile_page_boxes = page_boxes ? 1 : 0;
+    CUtensorMap tm_kt, tm_vt;
     if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.kv_layout, c.num_blocks,
-                                     c.block_size, c.num_kv_heads, dqk, 64, 16,
+                                     c.block_size, c.num_kv_heads, dqk, 64, page_boxes ? 64 : 16,
                                      CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
+    if (page_boxes) {
+      const unsigned long long es = 2, row = (unsigned long long)c.head_dim * es;
+      const bool hnd = c.kv_layout == PA_KV_HND;
+      const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
+                                          (unsigned long long)(c.head_dim / 64),
+                                          (unsigned long long)c.num_kv_heads,
+                                          (unsigned long long)c.num_blocks};
+      const unsigned long long strides[4] = {
+          hnd ? row : (unsigned long long)c.num_kv_heads * row, 64 * es,
+          hnd ? (unsigned long long)c.block_size * row : row,
+          (unsigned long long)c.block_size * c.num_kv_heads * row};
+      const unsigned int box[5] = {64, 64, (unsigned int)(c.head_dim / 64), 1, 1};
+      if (!encode_tiled(&tm_vt, c.v_cache, c.dtype, 5, dims, strides, box, true))
+        return PA_ERR_CUDA;
+    }
     cudaError_t row_err = cudaSuccess;
     slot = timed ? prof_begin(PA_K_ROW, st) : -1;
     if (c.all_tile) {
@@ -842,7 +863,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return PA_ERR_CUDA;
       slot = timed ? prof_begin(PA_K_TILE, st) : -1;
-      const cudaError_t tile_err = launch_tile_kernel(p, tm_q, tm_kt, tm_vr, num_sms, st);
+      const cudaError_t tile_err =
+          launch_tile_kernel(p, tm_q, tm_kt, page_boxes ? tm_vt : tm_vr, num_sms, st);
       prof_end(slot, st);
       if (tile_err != cudaSuccess) return PA_ERR_CUDA;
     }

@@ -90,6 +90,9 @@ struct FwdParams {
   int head_dim_qk;          // width of q / k rows when it differs from head_dim
                             // (the value / output width); 0: the same
   int all_tile;             // 1: every row, decode included, on the tile kernel
+  int tile_page_boxes;      // 1: every 64-position tile of the tile kernel lies in
+                            // one page (block_size % 64 == 0, 64-aligned tiles):
+                            // K and V load as one 64-slot box per tile
   const float *alibi;       // [num_heads] ALiBi slopes (natural-log units) or null
   int alibi_sqrt;           // 1: the bias grows with the square root of the distance
 };

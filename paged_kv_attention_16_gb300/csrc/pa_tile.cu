@@ -131,7 +131,8 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
   return true;
 }
 
-template <int DQK, int DV>
+// PB64: every 64-position tile is one page's 64 slots (one box per tile).
+template <int DQK, int DV, bool PB64>
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
@@ -148,6 +149,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.num_heads / p.num_kv_heads;
+  constexpr bool pb64 = PB64;
   const int H = p.num_heads, bs = p.block_size;
   pdl_trigger();
   pdl_wait();  // the plan, and the row kernel before us in the stream
@@ -194,8 +196,11 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           const int jj = which == 0 ? j : j - 1;
           if (jj < 0 || jj >= it.nt) continue;
           const uint32_t g = tiles + jj;
-          const int pos = it.kv_lo + jj * kBN + lane * kBox;
-          const bool need = lane < kBN / kBox && pos < it.kv_hi;
+          // 16-slot boxes, one per lane; or, when a tile is one page's 64
+          // slots, a single 64-slot box from lane 0 (a quarter of the TMA
+          // operations: their count, not their bytes, limits the loads)
+          const int pos = it.kv_lo + jj * kBN + (pb64 ? 0 : lane * kBox);
+          const bool need = (pb64 ? lane == 0 : lane < kBN / kBox) && pos < it.kv_hi;
           const int page = (which == 0 ? kc : vc).get(need ? pos / bs : -1, lane);
           const bool ok = need && page >= 0 && page < p.num_blocks;
           if (need && !ok) atomicOr(p.status, PA_DEV_BAD_BLOCK);
@@ -219,7 +224,8 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
               mbar_wait(&bar[kVFree0 + st], ((g / kVStages) - 1) & 1, dead, p.status);
           }
           if (lane == 0)
-            mbar_arrive_expect_tx(full, __popc(mask) * (which == 0 ? C::NHQ : C::NHV) * kBox * 128);
+            mbar_arrive_expect_tx(full, __popc(mask) * (which == 0 ? C::NHQ : C::NHV) *
+                                            (pb64 ? kBN : kBox) * 128);
           __syncwarp();
           // K: one box per 64-dim half ([halves][64 rows] for the S product's
           // uniform row stride); V: one box per 16 slots with both halves
@@ -228,10 +234,12 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           if (ok) {
             if (which == 0) {
               for (int h = 0; h < C::NHQ; ++h)
-                tma_load_4d(dst + h * C::KV_HALF + lane * kBox * 128, map, h * 64, it.kvh,
-                            pos % bs, page, full);
+                tma_load_4d(dst + h * C::KV_HALF + (pb64 ? 0 : lane * kBox * 128), map, h * 64,
+                            it.kvh, pos % bs, page, full);
             } else {
-              tma_load_5d(dst + lane * C::V_BOX, map, 0, pos % bs, 0, it.kvh, page, full);
+              // V: [16-slot boxes][chunks][16 rows], or [chunks][64 rows]
+              tma_load_5d(dst + (pb64 ? 0 : lane * C::V_BOX), map, 0, pos % bs, 0, it.kvh, page,
+                          full);
             }
           }
 
@@ -279,7 +287,10 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           const uint32_t vb = sv + vs * C::V_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint64_t b = umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
+            // 16 V rows (K = 16 of the PV product); the leading byte offset
+            // steps to the next 64-wide chunk of the row
+            const uint64_t b = pb64 ? umma_desc_sw128(vb + kk * 16 * 128, kBN * 128, 1024)
+                                    : umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
             tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
@@ -434,8 +445,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
             const int h = e / ((kBN - first) * 8);
             const int rem = e % ((kBN - first) * 8);
             const int row = first + rem / 8;
-            *reinterpret_cast<uint4 *>(vs + (row / kBox) * C::V_BOX + h * (kBox * 128) +
-                                       (row % kBox) * 128 + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
+            const int off = pb64 ? h * (kBN * 128) + row * 128
+                                 : (row / kBox) * C::V_BOX + h * (kBox * 128) + (row % kBox) * 128;
+            *reinterpret_cast<uint4 *>(vs + off + (rem % 8) * 16) = make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async();
         }
@@ -506,18 +518,25 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   if (warp == 5) tc_dealloc(tmem, kTmemCols);
 }
 
+template <int DQK, int DV, bool PB64>
+cudaError_t launch_v(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                     const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
+  using C = TileCfg<DQK, DV>;
+  auto kern = tile_kernel<DQK, DV, PB64>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  return launch_dependent(kern, dim3(num_sms * kTileCtasPerSm), dim3(kTileThreads), C::SMEM,
+                          stream, tq, tk, tv, p);
+}
+
 template <int DQK, int DV>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
                      const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
-  using C = TileCfg<DQK, DV>;
-  cudaError_t e = cudaFuncSetAttribute(tile_kernel<DQK, DV>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(tile_kernel<DQK, DV>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  return launch_dependent(tile_kernel<DQK, DV>, dim3(num_sms * kTileCtasPerSm),
-                          dim3(kTileThreads), C::SMEM, stream, tq, tk, tv, p);
+  return p.tile_page_boxes ? launch_v<DQK, DV, true>(p, tq, tk, tv, num_sms, stream)
+                           : launch_v<DQK, DV, false>(p, tq, tk, tv, num_sms, stream);
 }
 
 }  // namespace
