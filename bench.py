@@ -59,6 +59,13 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _plain(o):
+    """JSON fallback for numpy scalars."""
+    if isinstance(o, np.generic):
+        return o.item()
+    raise TypeError(f"not JSON serialisable: {type(o).__name__}")
+
+
 def kv_bytes(b, window=0):
     """K and V bytes a step must read: every position some row of its request
     sees (with a sliding window, from the first row's window start on)."""
@@ -383,7 +390,7 @@ def secondary_workloads(pa, flush, peaks):
         for s_ in range(hp.num_seqs):
             ql = qsl[s_ + 1] - qsl[s_]
             pairs += ql * (ctx[s_] - ql) + ql * (ql + 1) // 2
-        att = pairs * hp.num_heads * 2 * (hp.qk_nope_dim + hp.rope_dim + hp.v_head_dim)
+        att = int(pairs) * hp.num_heads * 2 * (hp.qk_nope_dim + hp.rope_dim + hp.v_head_dim)
         up = int(ctx.sum()) * hp.num_heads * 2 * hp.kv_lora_rank * (hp.qk_nope_dim + hp.v_head_dim)
         tf = (att + up) / ms / 1e9
         res["mla_prefill"] = {"ms": ms, "tflops": tf, "tensor_frac": tf / tfl,
@@ -594,7 +601,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "peaks": {"hbm_gbs": hbm, "bf16_tflops": peaks["bf16_tflops"], "source": peak_src},
     }
-    print(json.dumps(line))
+    print(json.dumps(line, default=_plain))
 
 
 # ---------------------------------------------------------------------------

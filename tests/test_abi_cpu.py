@@ -178,3 +178,14 @@ def _mla_prefill(lib, **kw):
 ])
 def test_mla_prefill_host_argument_checks(lib, kw, want):
     assert _mla_prefill(lib, **kw) == want
+
+
+def test_mla_prefill_workspace_grows_with_the_decompression_bound(lib):
+    f = lib.pa_mla_prefill_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int]
+    small = f(8, 4096, 128, 4096, 8192, 0)
+    big = f(8, 4096, 128, 4096, 16384, 0)
+    # keys (192) and values (128) per head plus the 512-wide latent, bf16
+    assert big - small >= 8192 * (128 * (192 + 128) + 512) * 2
+    assert f(-1, 1, 128, 64, 64, 0) == 0
