@@ -41,7 +41,7 @@ from paged_kv_attention_16_gb300 import inputs  # noqa: E402
 # workload, from the ncu capture summarised in
 # profiles/row_mma_kernel_llama_decode_b64.md.  Set to None whenever the row
 # kernel changes until it is captured again.
-ROW_KERNEL_TRAFFIC = 1_193_581_000 + 7_695_104
+ROW_KERNEL_TRAFFIC = 1_193_550_000 + 7_650_816
 
 METRIC = "decode KV GB/s (% of HBM peak); mixed-batch attention TFLOPS (% of peak)"
 WORKLOAD = ("llama-3.1-8b-shaped GQA decode: batch 64, ctx uniform [500, 8192], 32 q heads, "
