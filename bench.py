@@ -240,6 +240,37 @@ def plain_and_profiled(pa, fn, steps, flush):
     return ms, {k: v[0] / v[1] for k, v in prof.items()}
 
 
+def graph_step_ms(pa, b, out, per_graph=20, reps=10):
+    """Median device time of one pa_forward step when `per_graph` steps are
+    captured in one CUDA graph and the graph is replayed (workspace reserved
+    beforehand, as capture requires)."""
+    dt = pa.PA_BF16 if b.q.dtype == torch.bfloat16 else pa.PA_F32
+    pa.pa_reserve(pa.pa_forward_workspace_bytes(dt, b.num_seqs, b.num_tokens, b.num_heads,
+                                                b.num_kv_heads, b.head_dim, b.max_seq_len,
+                                                b.kv_split_tokens))
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.forward(b, out=out, stream=s)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(per_graph):
+                pa.forward(b, out=out, stream=s)
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream()
+    times = []
+    for _ in range(reps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        g.replay()
+        e1.record(st)
+        e1.synchronize()
+        times.append(e0.elapsed_time(e1) / per_graph)
+    return statistics.median(times)
+
+
 def secondary_workloads(pa, flush, peaks):
     """Per-workload device times (median over steps, L2 flushed between)."""
     res = {}
@@ -255,6 +286,11 @@ def secondary_workloads(pa, flush, peaks):
     gbs = kv_bytes(hb) / ms / 1e6
     res["llama_decode_b1"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm,
                               "note": "2 MB of KV: launch-latency bound"}
+    try:  # the same step replayed from a CUDA graph (20 steps per graph)
+        gms = graph_step_ms(pa, b, out)
+        res["llama_decode_b1"]["graph_replay"] = {"ms": gms, "kv_gbs": kv_bytes(hb) / gms / 1e6}
+    except Exception as e:  # report, never abort the benchmark
+        res["llama_decode_b1"]["graph_replay"] = {"error": str(e)[:200]}
     del b, out
 
     # the headline decode batch with NHD and with head-major (HND) caches
