@@ -71,10 +71,12 @@ def kv_bytes(b, window=0):
     sees (with a sliding window, from the first row's window start on)."""
     es = b.k_cache.element_size()
     ctx = b.seq_lens.to(torch.int64)
+    qsl = b.query_start_loc.to(torch.int64)
+    q_len = qsl[1:] - qsl[:-1]
     if window:
-        qsl = b.query_start_loc.to(torch.int64)
-        first = (ctx - (qsl[1:] - qsl[:-1]) - window + 1).clamp(min=0)
+        first = (ctx - q_len - window + 1).clamp(min=0)
         ctx = ctx - first
+    ctx = torch.where(q_len > 0, ctx, torch.zeros_like(ctx))  # no rows, nothing read
     return int(ctx.sum()) * b.num_kv_heads * b.head_dim * es * 2
 
 
