@@ -189,3 +189,23 @@ def test_mla_prefill_workspace_grows_with_the_decompression_bound(lib):
     # keys (192) and values (128) per head plus the 512-wide latent, bf16
     assert big - small >= 8192 * (128 * (192 + 128) + 512) * 2
     assert f(-1, 1, 128, 64, 64, 0) == 0
+
+
+def test_header_compiles_as_c_and_cxx(tmp_path):
+    """include/pa.h is a plain C header (C99, pedantic) that C++ can include."""
+    import shutil
+    import subprocess
+    src = tmp_path / "use_pa.c"
+    src.write_text('#include "pa.h"\n'
+                   "int main(void) {\n"
+                   "  pa_forward_options o = {0};\n"
+                   "  (void)o;\n"
+                   "  return (int)PA_KV_HND - 1 + (int)PA_OK;\n"
+                   "}\n")
+    inc = os.path.dirname(HEADER)
+    for cmd in (["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror"],
+                ["g++", "-std=c++11", "-Wall", "-Werror", "-x", "c++"]):
+        if shutil.which(cmd[0]) is None:
+            continue
+        subprocess.run(cmd + ["-I", inc, "-c", str(src), "-o", str(tmp_path / "o.o")],
+                       check=True)
