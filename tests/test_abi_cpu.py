@@ -209,3 +209,31 @@ def test_header_compiles_as_c_and_cxx(tmp_path):
             continue
         subprocess.run(cmd + ["-I", inc, "-c", str(src), "-o", str(tmp_path / "o.o")],
                        check=True)
+
+
+def test_binding_options_struct_matches_the_header(tmp_path):
+    """ctypes' ForwardOptions has the size and field offsets the C compiler
+    gives pa_forward_options."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        return
+    from paged_kv_attention_16_gb300 import pa
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pa.h"\n'
+                   "int main(void) {\n"
+                   '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(pa_forward_options),\n'
+                   "         offsetof(pa_forward_options, sinks),\n"
+                   "         offsetof(pa_forward_options, kv_layout),\n"
+                   "         offsetof(pa_forward_options, sliding_window),\n"
+                   "         offsetof(pa_forward_options, alibi_slopes),\n"
+                   "         offsetof(pa_forward_options, alibi_sqrt));\n"
+                   "  return 0;\n}\n")
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
+                   check=True)
+    got = [int(x) for x in subprocess.run([str(exe)], check=True, capture_output=True,
+                                          text=True).stdout.split()]
+    O = pa.ForwardOptions
+    want = [ctypes.sizeof(O)] + [getattr(O, f).offset for f, _ in O._fields_]
+    assert got == want
