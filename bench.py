@@ -37,16 +37,77 @@ sys.path.insert(0, ROOT)
 
 from paged_kv_attention_16_gb300 import inputs  # noqa: E402
 
-# DRAM bytes (read + write) of one row_mma_kernel<128,4> launch on this
-# workload, from the ncu capture summarised in
-# profiles/row_mma_kernel_llama_decode_b64.md.  Set to None whenever the row
-# kernel changes until it is captured again.
-ROW_KERNEL_TRAFFIC = 1_193_550_000 + 7_650_816
+# Measured DRAM traffic per launch (ncu dram__bytes_read.sum +
+# dram__bytes_write.sum) is kept in a data file written by
+# `bench.py --record-traffic`, keyed by kernel, workload and a hash of the
+# kernel's source files: a kernel changed since its capture reads as null.
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+CSRC = os.path.join(ROOT, "paged_kv_attention_16_gb300", "csrc")
+KERNEL_SOURCES = {
+    "row_mma_kernel": ["pa_rows_mma.cu", "pa_common.cuh"],
+    "tile_kernel": ["pa_tile.cu", "pa_common.cuh"],
+    "mla_kernel": ["pa_mla.cu", "pa_common.cuh"],
+    "upproj_kernel": ["pa_upproj.cu", "pa_common.cuh"],
+}
 
 METRIC = "decode KV GB/s (% of HBM peak); mixed-batch attention TFLOPS (% of peak)"
 WORKLOAD = ("llama-3.1-8b-shaped GQA decode: batch 64, ctx uniform [500, 8192], 32 q heads, "
             "8 kv heads, head_dim 128, block_size 16, bf16, random page placement")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def source_sha(kernel):
+    import hashlib
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def read_traffic_file():
+    rows = {}
+    if os.path.exists(TRAFFIC_FILE):
+        with open(TRAFFIC_FILE) as f:
+            for line in f:
+                parts = line.split()
+                if len(parts) >= 5 and not line.startswith("#"):
+                    rows[(parts[0], parts[1])] = (parts[2], int(parts[3]), int(parts[4]))
+    return rows
+
+
+def recorded_traffic(kernel, workload):
+    """DRAM bytes read + written per launch from the last capture of this
+    kernel on this workload, or None if the kernel changed since."""
+    row = read_traffic_file().get((kernel, workload))
+    if row is None or row[0] != source_sha(kernel):
+        return None
+    return row[1] + row[2]
+
+
+def record_traffic(csv_path, kernel, workload):
+    """Write the DRAM counters of an `ncu -i REP --page raw --csv` dump (the
+    first launch of `kernel` in it) into the traffic file."""
+    import csv
+    scale = {"byte": 1, "Kbyte": 1e3, "Mbyte": 1e6, "Gbyte": 1e9, "Tbyte": 1e12}
+    with open(csv_path) as f:
+        rows = list(csv.reader(f))
+    hdr, units = rows[0], rows[1]
+    ci = {n: i for i, n in enumerate(hdr)}
+    data = [r for r in rows[2:] if kernel in r[ci["Kernel Name"]]]
+    if not data:
+        raise SystemExit(f"no launch of {kernel} in {csv_path}")
+    vals = []
+    for m in ("dram__bytes_read.sum", "dram__bytes_write.sum"):
+        vals.append(int(round(float(data[0][ci[m]].replace(",", "")) * scale[units[ci[m]]])))
+    table = read_traffic_file()
+    table[(kernel, workload)] = (source_sha(kernel), vals[0], vals[1])
+    with open(TRAFFIC_FILE, "w") as f:
+        f.write("# kernel workload source_sha16 dram_bytes_read dram_bytes_write "
+                "(per launch, ncu; written by bench.py --record-traffic)\n")
+        for (k, w), (sha, r, wr) in sorted(table.items()):
+            f.write(f"{k} {w} {sha} {r} {wr}\n")
+    print(f"{kernel} {workload}: read {vals[0]} write {vals[1]}")
 
 
 def load_peaks():
@@ -459,30 +520,44 @@ def secondary_workloads(pa, flush, peaks):
     return res
 
 
-def cpu_baseline_sample(b, budget_s=12.0):
-    """The fp64 oracle, as it stands, on a bounded sample of the workload:
-    whole requests (all heads) until about budget_s of CPU work."""
+def oracle_step_fn(host):
+    """One CPU-baseline step: the fp64 oracle, as it stands, over every row
+    of the whole decode batch (64 requests x 32 heads) in one call.  Returns
+    (step function, KV bytes per step)."""
     from oracle import oracle as orc
-    q = inputs.storage_array(b.q)
-    kc = inputs.storage_array(b.k_cache)
-    vc = inputs.storage_array(b.v_cache)
-    bt, sl, qsl = b.block_table.numpy(), b.seq_lens.numpy(), b.query_start_loc.numpy()
-    H = b.num_heads
-    done_bytes, spent, n_req = 0, 0.0, 0
-    for s in range(b.num_seqs):
-        rows = np.arange(qsl[s] * H, qsl[s + 1] * H, dtype=np.int64)
-        t0 = time.perf_counter()
-        orc.paged_attention(q, kc, vc, bt, sl, qsl, H, b.num_kv_heads, b.head_dim,
-                            b.block_size, b.scale, rows=rows)
-        spent += time.perf_counter() - t0
-        done_bytes += int(sl[s]) * b.num_kv_heads * b.head_dim * 2 * 2
-        n_req += 1
-        if spent >= budget_s:
-            break
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
-    return {"value": done_bytes / spent / 1e9, "unit": "GB/s", "cores": cores, "kind": "oracle",
-            "sample": f"{n_req} of {b.num_seqs} requests (all {H} heads each), "
-                      f"{done_bytes / 1e6:.0f} MB of KV, {spent:.1f} s"}
+    q = inputs.storage_array(host.q)
+    kc = inputs.storage_array(host.k_cache)
+    vc = inputs.storage_array(host.v_cache)
+    bt, sl, qsl = host.block_table.numpy(), host.seq_lens.numpy(), host.query_start_loc.numpy()
+
+    def step():
+        orc.paged_attention(q, kc, vc, bt, sl, qsl, host.num_heads, host.num_kv_heads,
+                            host.head_dim, host.block_size, host.scale)
+
+    return step, kv_bytes(host)
+
+
+CPU_SAMPLE = "each step: the whole batch (64 requests x 32 heads, one oracle call)"
+
+
+def cpu_baseline_subprocess(steps=4, warmup=1):
+    """The reference arm's own measurement, run as a fresh process (no CUDA
+    context, no torch thread pools beside the oracle's), on the same sample:
+    the repo arm's cpu_baseline.  Timing the oracle inside the GPU process
+    measured several times slower than the same call in a fresh process."""
+    env = dict(os.environ)
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        env.pop(k, None)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", str(steps), "--warmup", str(warmup)],
+                       capture_output=True, text=True, env=env, cwd=ROOT, timeout=900)
+    line = [x for x in r.stdout.splitlines() if x.startswith("{")]
+    if r.returncode != 0 or not line:
+        return {"error": (r.stderr or r.stdout)[-300:]}
+    ref = json.loads(line[-1])
+    cb = dict(ref["cpu_baseline"])
+    cb["sample"] += f"; {steps} timed steps in a fresh process"
+    return cb
 
 
 def run_ours(args):
@@ -599,7 +674,7 @@ def run_ours(args):
 
     if rank != 0:
         return
-    cpu = cpu_baseline_sample(host) if not args.skip_cpu else None
+    cpu = cpu_baseline_subprocess() if not args.skip_cpu else None
     clk = clocks.summary(t_wall0, t_wall1)
     line = {
         "metric": METRIC,
@@ -614,12 +689,11 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic (seeded N(0,1) values, seeded page placement; no weights needed)",
-        "config": {"workload": WORKLOAD, "batch": 64, "kv_bytes_per_step": step_kv,
-                   "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": workload_config(step_kv, world),
         "hbm_frac": value / hbm,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": ROW_KERNEL_TRAFFIC,
+                     "frac": achieved / hbm,
+                     "traffic": recorded_traffic("row_mma_kernel", "llama_decode_b64"),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "kernel": "row_mma_kernel<128,4> (bf16 decode rows, warp MMAs)",
                      "kernel_ms": row_avg, "bytes_per_launch": step_kv + step_io,
@@ -646,42 +720,36 @@ def run_ours(args):
 # reference arm: the fp64 oracle on the host cores
 # ---------------------------------------------------------------------------
 
+def workload_config(step_kv, world=1):
+    return {"workload": WORKLOAD, "batch": 64, "kv_bytes_per_step": step_kv,
+            "l2": "inputs larger than L2 (KV per step >> 129 MB); no flush",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     from oracle import oracle as orc
     host = inputs.llama_decode(64, poison=False)
-    q = inputs.storage_array(host.q)
-    kc = inputs.storage_array(host.k_cache)
-    vc = inputs.storage_array(host.v_cache)
-    bt, sl, qsl = host.block_table.numpy(), host.seq_lens.numpy(), host.query_start_loc.numpy()
-    H = host.num_heads
-
-    def step(i):
-        s = i % host.num_seqs
-        rows = np.arange(qsl[s] * H, qsl[s + 1] * H, dtype=np.int64)
-        orc.paged_attention(q, kc, vc, bt, sl, qsl, H, host.num_kv_heads, host.head_dim,
-                            host.block_size, host.scale, rows=rows)
-        return int(sl[s]) * host.num_kv_heads * host.head_dim * 2 * 2
-
-    for i in range(args.warmup):
-        step(i)
+    step, nbytes = oracle_step_fn(host)
+    for _ in range(args.warmup):
+        step()
     t0 = time.perf_counter()
-    total = 0
-    for i in range(args.steps):
-        total += step(args.warmup + i)
+    for _ in range(args.steps):
+        step()
     dt = time.perf_counter() - t0
-    value = total / dt / 1e9
-    cores = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    value = nbytes * args.steps / dt / 1e9
+    cores = orc.num_threads()
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": {"workload": WORKLOAD},
+        "data": "synthetic (seeded N(0,1) values, seeded page placement; no weights needed)",
+        "config": workload_config(nbytes),
         "cpu_baseline": {"kind": "oracle", "cores": cores, "value": value, "unit": "GB/s",
-                         "sample": "each step: one request of the batch (all 32 heads), "
-                                   "requests taken in turn"},
+                         "sample": CPU_SAMPLE,
+                         "cores_source": "omp_get_max_threads() of the oracle library"},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0}}))
 
@@ -735,8 +803,12 @@ def main():
     ap.add_argument("--only", default=None,
                     choices=sorted(list(inputs.WORKLOADS) + ["mla_decode"]),
                     help="profile helper: loop over a single workload, no JSON contract")
+    ap.add_argument("--record-traffic", nargs=3, metavar=("NCU_RAW_CSV", "KERNEL", "WORKLOAD"),
+                    help="store a capture's DRAM bytes per launch for the roofline line")
     args = ap.parse_args()
-    if args.only:
+    if args.record_traffic:
+        record_traffic(*args.record_traffic)
+    elif args.only:
         run_only(args)
     elif args.impl == "reference":
         run_reference(args)

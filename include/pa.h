@@ -24,7 +24,10 @@
  *    Calls are asynchronous on it: they never synchronise and never read
  *    device memory on the host, so pa_forward / pa_mla_decode can be captured
  *    in a CUDA graph (reserve the workspace first, see pa_reserve).
- *  - Host-side argument errors return a status and launch nothing.
+ *  - Host-side argument errors return a status and launch nothing.  A stream
+ *    that belongs to a device other than the calling thread's current device
+ *    is such an error (PA_ERR_INVALID_ARG): the library's per-device state is
+ *    that of the current device.
  *  - Bad *device* metadata never traps: it sets a bit in the device status word
  *    (read with pa_get_device_status) and the affected output rows are written
  *    as zeros:
@@ -201,17 +204,22 @@ size_t pa_forward_workspace_bytes(pa_dtype dtype, int num_seqs, int num_tokens,
  * Arguments: those of pa_forward, plus
  *   device_status  optional device pointer to one uint32 owned by the caller;
  *                  the PA_DEV_* bits of this call are OR-ed into it (clearing
- *                  it is the caller's job).  NULL: the bits land in a word
- *                  inside the static region and are not reported.
+ *                  it is the caller's job).  NULL turns error reporting off:
+ *                  the bits land in a word inside the static region that no
+ *                  call clears or reads, so bad metadata then goes unseen
+ *                  (the affected rows are still zeros).  Callers that need
+ *                  the PA_DEV_* bits pass a word of their own.
  * Returns PA_ERR_SCRATCH_LIMIT and launches nothing when the call needs more
  * scratch than the region holds, i.e. when pa_forward_workspace_bytes() for
  * the same extents exceeds PA_STATIC_SCRATCH_BYTES - 256 (a decode batch of 64
  * sequences, 32 heads, head_dim 128 and max_seq_len 8192 needs about 34 MB).
- * Otherwise the status codes of pa_forward (never PA_ERR_WORKSPACE).
+ * Otherwise the status codes of pa_forward (PA_ERR_WORKSPACE only as below).
  *
  * The first call on each device looks up the region's device address
  * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call outside any stream capture.  All calls share the one region,
+ * first call outside any stream capture.  A first call made while `stream`
+ * is capturing returns PA_ERR_WORKSPACE and launches nothing (the capture is
+ * left intact); later calls may be captured.  All calls share the one region,
  * which keeps the last call's contents (each call's planner rewrites, in
  * stream order, every table and counter the call reads): calls that overlap
  * on the GPU -- on different streams, or from host threads without ordering --
@@ -385,6 +393,20 @@ pa_status pa_debug_gather(const void *k_cache, const int32_t *block_table,
                           int max_blocks_per_seq, int num_blocks,
                           int block_size, int row_elems, int elem_bytes,
                           int max_seq_len, void *dense_out, void *stream);
+
+/*
+ * pa_debug_wait_timeout -- test-only check of the kernels' failure path: one
+ * kernel waits, with the bounded wait every kernel of this library uses, on
+ * an mbarrier that nothing arrives on.  After limit_ns nanoseconds of wall
+ * clock (1 <= limit_ns <= 1e9, the kernels' own limit) the wait gives up,
+ * sets PA_DEV_TIMEOUT in the device status word and the kernel returns, so
+ * the context stays usable: nothing traps, no copy is left in flight.
+ *   done  device pointer to one int owned by the caller; set to 2 when the
+ *         kernel has returned (its timed-out wait and a second wait that
+ *         returns at once).
+ * Asynchronous on `stream`; read the bit with pa_get_device_status.
+ */
+pa_status pa_debug_wait_timeout(uint64_t limit_ns, int *done, void *stream);
 
 /*
  * Kernel timing.  While enabled, every kernel that pa_forward, pa_mla_decode

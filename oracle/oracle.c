@@ -46,6 +46,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_OK 0
 #define OR_BAD_ARGS 1
@@ -386,4 +389,14 @@ int oracle_gather_rows(const void *k_cache, int elem_bytes, int row_elems,
     }
   }
   return OR_OK;
+}
+
+/* Threads an OpenMP parallel region of this library starts (1 without
+ * OpenMP): the host cores the timed oracle actually uses. */
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
 }

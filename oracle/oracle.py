@@ -53,6 +53,8 @@ def load(path=None):
         _VP, ctypes.c_int, ctypes.c_int, _I32P, _I32P, ctypes.c_int, ctypes.c_int,
         ctypes.c_int, ctypes.c_int, ctypes.c_longlong, _VP]
     lib.oracle_gather_rows.restype = ctypes.c_int
+    lib.oracle_num_threads.argtypes = []
+    lib.oracle_num_threads.restype = ctypes.c_int
     return lib
 
 
@@ -359,3 +361,8 @@ def mla_prefill(q, kv_cache, w_kv, block_table, seq_lens, query_start_loc, kv_lo
         keep[np.asarray(rows, np.int64)] = True
         out.reshape(T * H, v_head_dim)[~keep] = np.nan
     return out
+
+
+def num_threads(lib=None):
+    """Threads the oracle's OpenMP regions run with (its host cores)."""
+    return int((lib or _lib()).oracle_num_threads())

@@ -497,6 +497,29 @@ __global__ void gather_kernel(const uint8_t *cache, const int32_t *bt, const int
 }
 
 // ---------------------------------------------------------------------------
+// debug wait: one bounded mbarrier wait that nothing ever completes
+// ---------------------------------------------------------------------------
+
+// One warp: lane 0 initialises an mbarrier expecting one arrival that never
+// comes and waits on it through the kernels' bounded wait; the wait gives up
+// after limit_ns, sets PA_DEV_TIMEOUT and the kernel returns.  A second wait
+// of the same thread returns at once (the `dead` latch every kernel relies
+// on to end after a timeout).  No copy is issued, so nothing is in flight
+// when the kernel ends.  *done receives 1 + the number of waits that returned.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, unsigned int *status, int *done) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  fence_mbar_init();
+  bool dead = false;
+  mbar_wait_limit(&bar, 0, dead, status, limit_ns);
+  int n = dead ? 1 : 0;
+  mbar_wait_limit(&bar, 0, dead, status, limit_ns);
+  n += 1;
+  *done = 1 + n;
+}
+
+// ---------------------------------------------------------------------------
 // host state
 // ---------------------------------------------------------------------------
 
@@ -511,23 +534,46 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[64];
 
+}  // namespace
+
 bool stream_capturing(cudaStream_t stream) {
   cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &st) != cudaSuccess) return false;
   return st != cudaStreamCaptureStatusNone;
 }
 
+pa_status current_device_for(cudaStream_t stream, int *dev) {
+  if (cudaGetDevice(dev) != cudaSuccess || *dev < 0 || *dev >= 64) {
+    cudaGetLastError();
+    return PA_ERR_CUDA;
+  }
+  int sdev = *dev;
+  if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
+    cudaGetLastError();
+    return PA_ERR_INVALID_ARG;
+  }
+  return sdev == *dev ? PA_OK : PA_ERR_INVALID_ARG;
+}
+
+namespace {
+
 // Device state of the current device; initialises it outside capture.
 pa_status device_state(cudaStream_t stream, DeviceState **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  const pa_status ds = current_device_for(stream, &dev);
+  if (ds != PA_OK) return ds;
   std::lock_guard<std::mutex> lock(g_mu);
   DeviceState &d = g_dev[dev];
   if (!d.init) {
     if (stream_capturing(stream)) return PA_ERR_WORKSPACE;
-    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
       return PA_ERR_CUDA;
-    if (cudaMalloc(&d.status, 256) != cudaSuccess) return PA_ERR_CUDA;
+    }
+    if (cudaMalloc(&d.status, 256) != cudaSuccess) {
+      cudaGetLastError();
+      return PA_ERR_CUDA;
+    }
     if (cudaMemset(d.status, 0, 256) != cudaSuccess) return PA_ERR_CUDA;
     d.init = true;
   }
@@ -1042,6 +1088,16 @@ pa_status pa_debug_gather(const void *k_cache, const int32_t *block_table,
       max_blocks_per_seq, num_blocks, block_size, row_bytes, max_seq_len,
       reinterpret_cast<uint8_t *>(dense_out), d->status);
   prof_end(slot, st);
+  return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_debug_wait_timeout(uint64_t limit_ns, int *done, void *stream) {
+  if (!done || limit_ns == 0 || limit_ns > kWaitLimitNs) return PA_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  DeviceState *d = nullptr;
+  pa_status s = device_state(st, &d);
+  if (s != PA_OK) return s;
+  wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns, d->status, done);
   return cudaGetLastError() == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 

@@ -250,19 +250,25 @@ __device__ inline uint64_t global_timer_ns() {
 // thread return at once so a kernel whose copies never land still ends.
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 
-__device__ inline void mbar_wait(uint64_t *bar, uint32_t parity, bool &dead,
-                                 unsigned int *status) {
+// Bounded wait with an explicit limit (the kernels use kWaitLimitNs).
+__device__ inline void mbar_wait_limit(uint64_t *bar, uint32_t parity, bool &dead,
+                                       unsigned int *status, uint64_t limit_ns) {
   if (dead) return;
   if (mbar_try_wait(bar, parity)) return;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return;
-    if ((i & 63u) == 0 && global_timer_ns() - t0 > kWaitLimitNs) {
+    if ((i & 63u) == 0 && global_timer_ns() - t0 > limit_ns) {
       atomicOr(status, PA_DEV_TIMEOUT);
       dead = true;
       return;
     }
   }
+}
+
+__device__ inline void mbar_wait(uint64_t *bar, uint32_t parity, bool &dead,
+                                 unsigned int *status) {
+  mbar_wait_limit(bar, parity, dead, status, kWaitLimitNs);
 }
 
 // 4-D tiled TMA load global -> shared, completion counted on `bar`.

@@ -79,6 +79,13 @@ size_t fwd_workspace_bytes(const FwdCall &c);
 pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, int num_sms,
                      cudaStream_t stream, bool timed);
 
+// True while `stream` is capturing a CUDA graph.
+bool stream_capturing(cudaStream_t stream);
+// The calling thread's current device in *dev; PA_ERR_INVALID_ARG when
+// `stream` belongs to another device (kernels would get this device's
+// workspace addresses), PA_ERR_CUDA when the device cannot be queried.
+pa_status current_device_for(cudaStream_t stream, int *dev);
+
 // Library-owned per-device resources for an entry point: workspace of at
 // least ws_bytes (grown outside capture), the device status word, SM count.
 pa_status device_resources(cudaStream_t stream, size_t ws_bytes, void **ws,

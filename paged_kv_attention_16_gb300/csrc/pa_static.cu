@@ -24,19 +24,25 @@ std::mutex g_static_mu;
 StaticScratch g_static_dev[64];
 
 // Device address of the region on the current device (set up on first use).
-pa_status static_scratch(StaticScratch **out) {
+// The set-up queries the runtime, which may load the module: it is refused
+// while `stream` is capturing, so that it can never invalidate a capture.
+pa_status static_scratch(cudaStream_t stream, StaticScratch **out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return PA_ERR_CUDA;
+  const pa_status ds = pa::current_device_for(stream, &dev);
+  if (ds != PA_OK) return ds;
   std::lock_guard<std::mutex> lock(g_static_mu);
   StaticScratch &d = g_static_dev[dev];
   if (!d.ready) {
+    if (pa::stream_capturing(stream)) return PA_ERR_WORKSPACE;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || ptr == nullptr) {
       cudaGetLastError();
       return PA_ERR_CUDA;
     }
-    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
       return PA_ERR_CUDA;
+    }
     d.base = static_cast<unsigned char *>(ptr);
     d.ready = true;
   }
@@ -60,7 +66,7 @@ extern "C" pa_status pa_forward_static_scratch(
   if (pa::fwd_workspace_bytes(c) > PA_STATIC_SCRATCH_BYTES - kStatusBytes)
     return PA_ERR_SCRATCH_LIMIT;
   StaticScratch *d = nullptr;
-  s = static_scratch(&d);
+  s = static_scratch(reinterpret_cast<cudaStream_t>(stream), &d);
   if (s != PA_OK) return s;
   unsigned int *status =
       device_status ? reinterpret_cast<unsigned int *>(device_status)

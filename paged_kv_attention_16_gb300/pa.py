@@ -30,7 +30,7 @@ EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cach
            "pa_mla_decode_workspace_bytes", "pa_reserve", "pa_get_device_status",
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
            "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch", "pa_forward_ex",
-           "pa_mla_prefill", "pa_mla_prefill_workspace_bytes")
+           "pa_mla_prefill", "pa_mla_prefill_workspace_bytes", "pa_debug_wait_timeout")
 PA_K_COUNT = 8
 
 
@@ -107,6 +107,8 @@ def lib():
         L.pa_mla_prefill_workspace_bytes.argtypes = [c_int, c_int, c_int, c_int,
                                                      ctypes.c_longlong, c_int]
         L.pa_mla_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.pa_debug_wait_timeout.argtypes = [ctypes.c_uint64, vp, vp]
+        L.pa_debug_wait_timeout.restype = c_int
         L.pa_kernel_name.argtypes = [c_int]
         L.pa_kernel_name.restype = ctypes.c_char_p
         _lib = L
@@ -285,6 +287,16 @@ def pa_debug_gather(k_cache, block_table, seq_lens, block_size, max_seq_len, den
                                int(k_cache.element_size()), int(max_seq_len), _ptr(dense_out),
                                _stream_ptr(stream))
     _check(st, "pa_debug_gather")
+
+
+def pa_debug_wait_timeout(limit_ns, done, stream=None, check=True):
+    """Test-only: one kernel whose bounded mbarrier wait runs out after
+    limit_ns (see include/pa.h); `done` is an int32 device tensor of one
+    element that the kernel sets to 2 when it returns."""
+    st = lib().pa_debug_wait_timeout(int(limit_ns), _ptr(done), _stream_ptr(stream))
+    if check:
+        _check(st, "pa_debug_wait_timeout")
+    return st
 
 
 # ---------------------------------------------------------------------------
