@@ -290,17 +290,19 @@ size_t pa_mla_decode_workspace_bytes(int num_seqs, int num_heads,
  *  A bad block id in a request's context sets PA_DEV_BAD_BLOCK and zeroes
  *  that request's rows.
  *  Supported: kv_lora_rank 512, rope_dim 64, qk_nope_dim 128, v_head_dim
- *  128, any num_heads and block_size >= 1; kv_split_tokens as for pa_forward.
+ *  128, any num_heads, block_size a multiple of 16 (at most 256: a run of
+ *  16 positions never crosses a page); kv_split_tokens as for pa_forward.
  *  max_seq_len    host-known bound on seq_lens
  *  max_total_kv   host-known bound on the sum of seq_lens (sizes the
  *                 decompressed keys and values: about 81 KB per position at
  *                 128 heads); a batch beyond it sets PA_DEV_OVERFLOW and
  *                 writes zeros
- * The up-projection runs as two cuBLAS GEMMs (bf16 in, fp32 accumulation,
- * bf16 keys and values), loaded at run time; without cuBLAS the call returns
- * PA_ERR_UNSUPPORTED.  The attention is pa_forward's tensor-core tile kernel
- * with q and k rows of 192 and v rows of 128.  Status bits and errors as for
- * pa_forward; PA_ERR_UNSUPPORTED for other dimensions.
+ * The up-projection is this library's tensor-core GEMM (bf16 in, fp32
+ * accumulation, bf16 keys and values), whose A operand is read from the
+ * pages the block table names; the 64 rotary columns are stored once per
+ * position, not per head.  The attention is pa_forward's tensor-core tile
+ * kernel with q and k rows of 192 and v rows of 128.  Status bits and errors
+ * as for pa_forward; PA_ERR_UNSUPPORTED for other dimensions.
  */
 pa_status pa_mla_prefill(const void *q, const void *kv_cache, const void *w_kv,
                          const int32_t *block_table, const int32_t *seq_lens,
@@ -425,7 +427,9 @@ enum {
   PA_K_MLA = 4,       /* absorbed-MLA decode kernel                 */
   PA_K_MLA_MERGE = 5, /* MLA log-sum-exp merge                      */
   PA_K_GATHER = 6,    /* debug gather                               */
-  PA_K_COUNT = 8
+  PA_K_UPPROJ = 7,    /* MLA prefill up-projection (tensor cores)   */
+  PA_K_MLA_ROPE = 8,  /* MLA prefill rotary-key copy                */
+  PA_K_COUNT = 10
 };
 pa_status pa_profile_enable(int on);
 pa_status pa_profile_read(double *total_ms, int *launches);

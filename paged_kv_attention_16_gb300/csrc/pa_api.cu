@@ -505,18 +505,18 @@ __global__ void gather_kernel(const uint8_t *cache, const int32_t *bt, const int
 // after limit_ns, sets PA_DEV_TIMEOUT and the kernel returns.  A second wait
 // of the same thread returns at once (the `dead` latch every kernel relies
 // on to end after a timeout).  No copy is issued, so nothing is in flight
-// when the kernel ends.  *done receives 1 + the number of waits that returned.
+// when the kernel ends.  *done receives 2 when the first wait ran out and the
+// second returned.
 __global__ void wait_timeout_kernel(uint64_t limit_ns, unsigned int *status, int *done) {
   __shared__ uint64_t bar;
   if (threadIdx.x != 0) return;
   mbar_init(&bar, 1);
   fence_mbar_init();
   bool dead = false;
-  mbar_wait_limit(&bar, 0, dead, status, limit_ns);
-  int n = dead ? 1 : 0;
-  mbar_wait_limit(&bar, 0, dead, status, limit_ns);
-  n += 1;
-  *done = 1 + n;
+  mbar_wait_limit(&bar, 0, dead, status, limit_ns);  // runs out: dead
+  const int timed_out = dead ? 1 : 0;
+  mbar_wait_limit(&bar, 0, dead, status, limit_ns);  // returns at once
+  *done = timed_out + 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -854,11 +854,19 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     const bool page_boxes = tile_ok && c.dtype == PA_BF16 && c.block_size % 64 == 0 &&
                             c.sliding_window == 0 && c.kv_split_tokens % 64 == 0;
     p.tile_page_boxes = page_boxes ? 1 : 0;
-    CUtensorMap tm_kt, tm_vt;
+    // Split keys (MLA prefill): the key tensor holds dqk - 64 columns per
+    // (position, head) and the last 64 come from one row per position.
+    CUtensorMap tm_kt, tm_vt, tm_krope;
+    p.k_rope_split = c.k_rope ? 1 : 0;
     if (tile_ok && !encode_cache_map(&tm_kt, c.k_cache, c.dtype, c.kv_layout, c.num_blocks,
-                                     c.block_size, c.num_kv_heads, dqk, 64, page_boxes ? 64 : 16,
-                                     CU_TENSOR_MAP_SWIZZLE_128B))
+                                     c.block_size, c.num_kv_heads, c.k_rope ? dqk - 64 : dqk, 64,
+                                     page_boxes ? 64 : 16, CU_TENSOR_MAP_SWIZZLE_128B))
       return PA_ERR_CUDA;
+    if (c.k_rope && !encode_cache_map(&tm_krope, c.k_rope, c.dtype, PA_KV_NHD, c.num_blocks,
+                                      c.block_size, 1, 64, 64, page_boxes ? 64 : 16,
+                                      CU_TENSOR_MAP_SWIZZLE_128B))
+      return PA_ERR_CUDA;
+    if (!c.k_rope) tm_krope = tm_kt;
     if (page_boxes) {
       const unsigned long long es = 2, row = (unsigned long long)c.head_dim * es;
       const bool hnd = c.kv_layout == PA_KV_HND;
@@ -910,7 +918,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
         return PA_ERR_CUDA;
       slot = timed ? prof_begin(PA_K_TILE, st) : -1;
       const cudaError_t tile_err =
-          launch_tile_kernel(p, tm_q, tm_kt, page_boxes ? tm_vt : tm_vr, num_sms, st);
+          launch_tile_kernel(p, tm_q, tm_kt, page_boxes ? tm_vt : tm_vr, tm_krope, num_sms, st);
       prof_end(slot, st);
       if (tile_err != cudaSuccess) return PA_ERR_CUDA;
     }

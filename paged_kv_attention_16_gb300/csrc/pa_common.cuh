@@ -95,6 +95,8 @@ struct FwdParams {
                             // K and V load as one 64-slot box per tile
   const float *alibi;       // [num_heads] ALiBi slopes (natural-log units) or null
   int alibi_sqrt;           // 1: the bias grows with the square root of the distance
+  int k_rope_split;         // 1: the last 64 key columns come from a separate
+                            // [pages, slots, 1, 64] tensor shared by all heads
 };
 
 // First KV position the query at position `pos` sees: with a sliding window
@@ -290,6 +292,15 @@ __device__ inline void tma_load_5d(void *dst, const CUtensorMap *map, int c0, in
       " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4),
       "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ inline void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1,
+                                   uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
       : "memory");
 }
 
@@ -628,6 +639,18 @@ __device__ inline void mbar_wait_cluster(uint64_t *bar, uint32_t parity, bool &d
       return;
     }
   }
+}
+
+// Asynchronous 16-byte store into another CTA's shared memory (a cluster
+// address); its bytes complete as transaction bytes on that CTA's mbarrier
+// `mbar_cluster`, which the receiver waits on (no release fence needed).
+__device__ inline void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
+                                   uint32_t mbar_cluster) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
+          "r"(cluster_addr),
+      "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar_cluster)
+      : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to

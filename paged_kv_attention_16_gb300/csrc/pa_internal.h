@@ -47,9 +47,26 @@ cudaError_t launch_row_mma_kernel(const FwdParams &p, const CUtensorMap &tm_k,
 
 // Tensor-core (tcgen05) tile kernel for bf16 extend/prefill rows.
 bool tile_kernel_supported(int dtype, int head_dim, int group);
+// tm_kr: the shared rotary-key columns when p.k_rope_split (else unused).
 cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_k, const CUtensorMap &tm_v, int grid,
-                               cudaStream_t stream);
+                               const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                               const CUtensorMap &tm_kr, int grid, cudaStream_t stream);
+
+// Up-projection of the non-absorbed MLA prefill (tensor cores): the latent
+// rows of every dense row (request s's positions from seg[s] on, 16-aligned
+// runs) are read through the block table and multiplied by each head's
+// w_kv rows into key and value rows.
+struct UpprojArgs {
+  const int32_t *block_table;
+  int num_seqs, num_heads, block_size, max_blocks_per_seq, num_blocks;
+  const long long *total;  // dense rows in use (device)
+  const long long *seg;    // [num_seqs] first dense row of each request
+  __nv_bfloat16 *k_nope;   // [rows, num_heads, 128]
+  __nv_bfloat16 *v;        // [rows, num_heads, 128]
+  unsigned int *status;
+};
+cudaError_t launch_upproj(const UpprojArgs &a, const void *kv_cache, const void *w_kv,
+                          int num_sms, cudaStream_t stream);
 
 // One pa_forward call's host-side arguments.
 struct FwdCall {
@@ -69,6 +86,10 @@ struct FwdCall {
   // elements, v and out rows of head_dim, every row on the tile kernel.
   int head_dim_qk = 0;
   bool all_tile = false;
+  // Keys split in two tensors: k_cache holds the first head_dim_qk - 64
+  // columns of every (position, head) key row, k_rope the last 64 columns,
+  // shared by all heads: [num_blocks, block_size, 64].  Null: keys whole.
+  const void *k_rope = nullptr;
 };
 // Host-side argument checks of pa_forward (PA_OK also when num_tokens == 0).
 pa_status fwd_check(const FwdCall &c);

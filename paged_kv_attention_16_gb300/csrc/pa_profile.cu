@@ -104,6 +104,8 @@ const char *pa_kernel_name(int kernel_id) {
     case PA_K_MLA: return "mla";
     case PA_K_MLA_MERGE: return "mla_merge";
     case PA_K_GATHER: return "gather";
+    case PA_K_UPPROJ: return "upproj";
+    case PA_K_MLA_ROPE: return "mla_rope";
   }
   return "unknown";
 }

@@ -135,7 +135,8 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
 template <int DQK, int DV, bool PB64>
 __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                const __grid_constant__ CUtensorMap tm_v, const FwdParams p) {
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kr,
+                const FwdParams p) {
   using C = TileCfg<DQK, DV>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled operand tiles need 1024-byte alignment.
@@ -160,6 +161,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     prefetch_tensor_map(&tm_q);
     prefetch_tensor_map(&tm_k);
     prefetch_tensor_map(&tm_v);
+    if (p.k_rope_split) prefetch_tensor_map(&tm_kr);
     for (int b = 0; b < kNumBars; ++b) {
       const bool per_warp = b == kPFull0 || b == kPFull1 || b == kOFree;
       mbar_init(&bar[b], per_warp ? 4 : 1);
@@ -233,9 +235,13 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           // box), half as many TMA boxes.
           if (ok) {
             if (which == 0) {
-              for (int h = 0; h < C::NHQ; ++h)
-                tma_load_4d(dst + h * C::KV_HALF + (pb64 ? 0 : lane * kBox * 128), map, h * 64,
-                            it.kvh, pos % bs, page, full);
+              for (int h = 0; h < C::NHQ; ++h) {
+                // split keys: the last 64 columns are the shared rotary key
+                const bool rope = p.k_rope_split && h == C::NHQ - 1;
+                tma_load_4d(dst + h * C::KV_HALF + (pb64 ? 0 : lane * kBox * 128),
+                            rope ? &tm_kr : map, rope ? 0 : h * 64, rope ? 0 : it.kvh, pos % bs,
+                            page, full);
+              }
             } else {
               // V: [16-slot boxes][chunks][16 rows], or [chunks][64 rows]
               tma_load_5d(dst + (pb64 ? 0 : lane * C::V_BOX), map, 0, pos % bs, 0, it.kvh, page,
@@ -520,7 +526,8 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
 
 template <int DQK, int DV, bool PB64>
 cudaError_t launch_v(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
+                     const CUtensorMap &tv, const CUtensorMap &tkr, int num_sms,
+                     cudaStream_t stream) {
   using C = TileCfg<DQK, DV>;
   auto kern = tile_kernel<DQK, DV, PB64>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
@@ -529,14 +536,15 @@ cudaError_t launch_v(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms * kTileCtasPerSm), dim3(kTileThreads), C::SMEM,
-                          stream, tq, tk, tv, p);
+                          stream, tq, tk, tv, tkr, p);
 }
 
 template <int DQK, int DV>
 cudaError_t launch_d(const FwdParams &p, const CUtensorMap &tq, const CUtensorMap &tk,
-                     const CUtensorMap &tv, int num_sms, cudaStream_t stream) {
-  return p.tile_page_boxes ? launch_v<DQK, DV, true>(p, tq, tk, tv, num_sms, stream)
-                           : launch_v<DQK, DV, false>(p, tq, tk, tv, num_sms, stream);
+                     const CUtensorMap &tv, const CUtensorMap &tkr, int num_sms,
+                     cudaStream_t stream) {
+  return p.tile_page_boxes ? launch_v<DQK, DV, true>(p, tq, tk, tv, tkr, num_sms, stream)
+                           : launch_v<DQK, DV, false>(p, tq, tk, tv, tkr, num_sms, stream);
 }
 
 }  // namespace
@@ -547,12 +555,15 @@ bool tile_kernel_supported(int dtype, int head_dim, int group) {
 }
 
 cudaError_t launch_tile_kernel(const FwdParams &p, const CUtensorMap &tm_q,
-                               const CUtensorMap &tm_k, const CUtensorMap &tm_v, int num_sms,
-                               cudaStream_t stream) {
+                               const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                               const CUtensorMap &tm_kr, int num_sms, cudaStream_t stream) {
   const int dqk = p.head_dim_qk > 0 ? p.head_dim_qk : p.head_dim;
-  if (dqk == 128 && p.head_dim == 128) return launch_d<128, 128>(p, tm_q, tm_k, tm_v, num_sms, stream);
-  if (dqk == 64 && p.head_dim == 64) return launch_d<64, 64>(p, tm_q, tm_k, tm_v, num_sms, stream);
-  if (dqk == 192 && p.head_dim == 128) return launch_d<192, 128>(p, tm_q, tm_k, tm_v, num_sms, stream);
+  if (dqk == 128 && p.head_dim == 128)
+    return launch_d<128, 128>(p, tm_q, tm_k, tm_v, tm_kr, num_sms, stream);
+  if (dqk == 64 && p.head_dim == 64)
+    return launch_d<64, 64>(p, tm_q, tm_k, tm_v, tm_kr, num_sms, stream);
+  if (dqk == 192 && p.head_dim == 128)
+    return launch_d<192, 128>(p, tm_q, tm_k, tm_v, tm_kr, num_sms, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -31,7 +31,7 @@ EXPORTS = ("pa_forward", "pa_forward_workspace_bytes", "pa_mla_decode", "pa_cach
            "pa_status_string", "pa_num_sms", "pa_debug_gather", "pa_profile_enable",
            "pa_profile_read", "pa_kernel_name", "pa_forward_static_scratch", "pa_forward_ex",
            "pa_mla_prefill", "pa_mla_prefill_workspace_bytes", "pa_debug_wait_timeout")
-PA_K_COUNT = 8
+PA_K_COUNT = 10
 
 
 class ForwardOptions(ctypes.Structure):

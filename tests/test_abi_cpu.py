@@ -186,8 +186,9 @@ def test_mla_prefill_workspace_grows_with_the_decompression_bound(lib):
     f.argtypes = [ctypes.c_int] * 4 + [ctypes.c_longlong, ctypes.c_int]
     small = f(8, 4096, 128, 4096, 8192, 0)
     big = f(8, 4096, 128, 4096, 16384, 0)
-    # keys (192) and values (128) per head plus the 512-wide latent, bf16
-    assert big - small >= 8192 * (128 * (192 + 128) + 512) * 2
+    # per position: 128 key and 128 value entries per head, plus the 64-wide
+    # rotary key stored once, bf16
+    assert big - small >= 8192 * (128 * (128 + 128) + 64) * 2
     assert f(-1, 1, 128, 64, 64, 0) == 0
 
 
