@@ -27,7 +27,8 @@
  *  - Host-side argument errors return a status and launch nothing.  A stream
  *    that belongs to a device other than the calling thread's current device
  *    is such an error (PA_ERR_INVALID_ARG): the library's per-device state is
- *    that of the current device.
+ *    that of the current device.  (A stream that is capturing a graph is not
+ *    queried for its device: the query would invalidate the capture.)
  *  - Bad *device* metadata never traps: it sets a bit in the device status word
  *    (read with pa_get_device_status) and the affected output rows are written
  *    as zeros:

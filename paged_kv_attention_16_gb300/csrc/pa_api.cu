@@ -106,13 +106,15 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   const long long mask21 = (1ll << 21) - 1;
   const long long n_dec = class_tot & mask21, n_ext = (class_tot >> 21) & mask21;
 
-  // Decode split: the smallest power of two >= kRowMinSplit that keeps the
-  // item count near 8 items per resident CTA
-  // (4 per CTA from G = 8 on: their items carry more work per KV byte)
+  // Decode split: the multiple of 64 positions that makes the item count
+  // about 8 items per resident CTA (4 per CTA from G = 8 on: their items
+  // carry more work per KV byte), within [kRowMinSplit, kRowMaxSplit].  Not
+  // rounded to a power of two: that could leave the last wave of items
+  // covering only part of the grid.
   const long long target = (G >= 8 ? 4ll : 8ll) * (p.row_ctas > 0 ? p.row_ctas : 1);
   const long long kv_work = work_tot * Hk;
-  int L = kRowMinSplit;
-  while (L < kRowMaxSplit && kv_work > (long long)L * target) L <<= 1;
+  const long long Lw = ceil_div_ll(ceil_div_ll(kv_work, target), 64) * 64;
+  int L = (int)(Lw < kRowMinSplit ? kRowMinSplit : (Lw > kRowMaxSplit ? kRowMaxSplit : Lw));
   if (p.kv_split_tokens > 0 && p.kv_split_tokens < L) L = p.kv_split_tokens;
   // Extend/prefill rows on the row path: at most ~4 splits per row.
   int Lr = (int)ceil_div_ll(ceil_div_ll(p.max_seq_len, 4), 16) * 16;
@@ -547,6 +549,9 @@ pa_status current_device_for(cudaStream_t stream, int *dev) {
     cudaGetLastError();
     return PA_ERR_CUDA;
   }
+  // A stream that is capturing is not queried (the query would invalidate a
+  // global-mode capture); the check applies to calls made outside capture.
+  if (stream_capturing(stream)) return PA_OK;
   int sdev = *dev;
   if (cudaStreamGetDevice(stream, &sdev) != cudaSuccess) {
     cudaGetLastError();

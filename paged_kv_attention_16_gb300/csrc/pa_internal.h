@@ -104,7 +104,8 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
 bool stream_capturing(cudaStream_t stream);
 // The calling thread's current device in *dev; PA_ERR_INVALID_ARG when
 // `stream` belongs to another device (kernels would get this device's
-// workspace addresses), PA_ERR_CUDA when the device cannot be queried.
+// workspace addresses), PA_ERR_CUDA when the device cannot be queried.  A
+// capturing stream is not checked.
 pa_status current_device_for(cudaStream_t stream, int *dev);
 
 // Library-owned per-device resources for an entry point: workspace of at

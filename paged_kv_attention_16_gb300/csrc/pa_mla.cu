@@ -14,14 +14,20 @@
 //   CTA 0 owns latent columns 0..255 plus the 64 rope columns,
 //   CTA 1 owns latent columns 256..511.
 // Each CTA loads only its own columns of every cached row (TMA, 128-byte
-// swizzled boxes of 64 columns x 32 slots), so the cache is read from HBM
-// exactly once and no FLOP is duplicated.  Per 32-position tile each CTA
-// forms its partial scores S_c = Q[:, own] K[:, own]^T in TMEM, stages them in
-// its own shared memory and pushes them to its peer with one bulk DSMEM copy
-// (completion counted on the peer's mbarrier), adds the peer's partial, runs
-// the same online softmax (base 2, lazy rescaling), stores P as packed bf16
-// in TMEM and accumulates O[:, own] += P V[:, own] (N = 256, P read from TMEM,
-// V read MN-major from the staged rows).
+// swizzled boxes of 64 columns x 32 slots into a 4-stage ring of 64-position
+// tiles), so the cache is read from HBM exactly once and no FLOP is
+// duplicated.  Tensor memory per CTA: O (128 x 256 fp32), the item's query
+// columns (bf16 pairs, the A operand of the score product), one S tile
+// (128 x 64 fp32) and P (128 x 64 bf16).  Per tile each CTA forms its partial
+// scores S_c = Q[:, own] K[:, own]^T, and its softmax warps push them from
+// registers straight into the peer's shared memory with asynchronous remote
+// stores that complete on the peer's mbarrier -- for tile j + 1 while tile j
+// is being finished, so the exchange latency hides behind a softmax.  Each
+// CTA adds the peer's partial to its own (the same sum in both), runs the
+// same online softmax (base 2, lazy rescaling), stores P as packed bf16 in
+// TMEM and accumulates O[:, own] += P V[:, own] (N = 256, P read from TMEM,
+// V read MN-major from the staged rows).  The score product runs two tiles
+// ahead of the value product.
 // Splits of a long context are merged by log-sum-exp in a second kernel.
 #include "pa_internal.h"
 
@@ -29,35 +35,35 @@ namespace pa {
 namespace {
 
 constexpr int kMlaL = 512, kMlaR = 64, kMlaW = 576, kMlaH = 128;
-constexpr int kMN = 32;             // KV positions per tile
+constexpr int kMN = 64;             // KV positions per tile
+constexpr int kMHalf = 32;          // slots per TMA box (a box never crosses a page)
 constexpr int kMlaThreads = 192;    // 4 softmax warps, producer warp, MMA warp
-constexpr int kMlaStages = 4;
-constexpr int kChunkQ = 128 * 128;  // Q: 128 heads x 64 columns, bf16
-constexpr int kChunkKV = kMN * 128; // KV: 32 rows x 64 columns, bf16
+constexpr int kMlaStages = 3;
+constexpr int kChunkKV = kMN * 128; // one 64-column chunk of a tile: 64 rows x 128 B
 constexpr int kMaxChunks = 5;
 constexpr int kVHalf = 256;         // value columns per CTA
 constexpr float kTau = 8.0f;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 0;      // O: columns [0, 256)
-constexpr uint32_t kTmemS = 256;    // S: two buffers of 32 columns
-constexpr uint32_t kTmemP = 320;    // P: two buffers of 16 columns (32 bf16 per row)
+constexpr uint32_t kTmemQ = 256;    // query columns: 160 (CTA 0) or 128 (CTA 1)
+constexpr uint32_t kTmemS = 416;    // S: 64 columns
+constexpr uint32_t kTmemP = 480;    // P: 32 columns (64 bf16 per row)
 constexpr int kMinSplit = 512;
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + kMaxChunks * kChunkQ;
 constexpr int STAGE_BYTES = kMaxChunks * kChunkKV;
 constexpr int X_BYTES = 128 * kMN * 4;               // one tile of partial scores
-constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;  // peer's partials, 2 buffers
-constexpr int OFF_XS = OFF_X + 2 * X_BYTES;               // own partials staged, 2 buffers
-constexpr int OFF_BAR = OFF_XS + 2 * X_BYTES;
+constexpr int OFF_KV = 0;
+constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;  // the peer's partials, 2 buffers
+constexpr int OFF_XS = OFF_X + 2 * X_BYTES;               // own partials staged for the copy
+constexpr int OFF_BAR = OFF_XS + X_BYTES;
 
 enum MBar {
-  kQFull = 0, kQFree, kKVFull0, kKVFree0 = kKVFull0 + kMlaStages, kSFull0 = kKVFree0 + kMlaStages,
-  kSFree0 = kSFull0 + 2, kXFull0 = kSFree0 + 2, kXFree0 = kXFull0 + 2, kPFull0 = kXFree0 + 2,
-  kODone0 = kPFull0 + 2, kOFree = kODone0 + 2, kNumMBars
+  kQFull = 0, kQFree, kKVFull0, kKVFree0 = kKVFull0 + kMlaStages, kSFull = kKVFree0 + kMlaStages,
+  kSFree, kPFull, kODone, kOFree, kXFull0, kXFree0 = kXFull0 + 2, kNumMBars = kXFree0 + 2
 };
 constexpr int OFF_MISC = OFF_BAR + kNumMBars * 8;
 constexpr int MLA_SMEM = OFF_MISC + 64 + 1024;
+static_assert(MLA_SMEM <= 232448, "shared memory budget");
 
 constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kMN, 0);
 constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, kVHalf, 1);
@@ -70,9 +76,13 @@ struct MlaArgs {
   int num_seqs, block_size, max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
   float scale_log2;
   int max_splits, num_clusters;
-  long long *plan;      // [0] work items, [1] split length
-  long long *item_end;  // [num_seqs] inclusive prefix of splits
-  int *nsplit;          // [num_seqs]; 0 marks a sequence whose metadata failed
+  // plan[2] = 0 (fixed split length): [0] work items, [1] split length,
+  //   item_end = inclusive prefix of each sequence's splits;
+  // plan[2] = 1 (balanced): [0] 64-position tiles in all, [1] tiles per
+  //   cluster, item_end = inclusive prefix of each sequence's tiles
+  long long *plan;
+  long long *item_end;  // [num_seqs]
+  int *nsplit;          // [num_seqs] pieces (partials); 0 marks a sequence whose metadata failed
   float *part_o;        // [(s * 128 + h) * max_splits + split][512]
   float *part_lse;      // same rows; base-2 log-sum-exp, NaN = bad split
   unsigned int *status;
@@ -84,65 +94,120 @@ __device__ inline int chunk_of(uint32_t rank, int i) {
 }
 
 // ---------------------------------------------------------------------------
-// planner: validity, split length, prefix sums of splits (one block)
+// planner: validity, work split, prefix sums (one block)
+//
+// Automatic split (kv_split_tokens == 0): the batch's 64-position tiles, in
+// sequence order, are cut into one contiguous run per cluster of
+// ceil(tiles / clusters) tiles (at least kMinSplit / 64): every cluster gets
+// the same work whatever the mix of lengths, and a sequence is split only
+// where a run boundary falls inside it, so at most one partial per cluster
+// boundary is written.  A fixed kv_split_tokens cuts every sequence into
+// splits of that length, dealt to the clusters in turn.
 // ---------------------------------------------------------------------------
+constexpr int kMinRunTiles = kMinSplit / kMN;
+
+__device__ inline bool mla_seq_ok(const MlaArgs &a, int ctx) {
+  return ctx >= 1 && ctx <= a.max_seq_len &&
+         ceil_div_ll(ctx, a.block_size) <= (long long)a.max_blocks_per_seq;
+}
+
 __global__ void __launch_bounds__(1024) mla_plan_kernel(const MlaArgs a) {
   __shared__ long long scratch[33];
   const int S = a.num_seqs, tid = threadIdx.x;
   pdl_wait();     // whatever preceded this call in the stream
   pdl_trigger();  // the decode kernel may start its prologue meanwhile
-  long long tot = 0;
-  int bad = 0;
-  for (int s = tid; s < S; s += 1024) {
-    const int ctx = a.seq_lens[s];
-    const bool ok = ctx >= 1 && ctx <= a.max_seq_len &&
-                    ceil_div_ll(ctx, a.block_size) <= (long long)a.max_blocks_per_seq;
-    if (ok) tot += ctx; else bad = 1;
-  }
-  if (bad) atomicOr(a.status, PA_DEV_BAD_SEQLEN);
-  long long total;
-  block_inclusive_scan(tot, scratch, &total);
-  long long L;
-  if (a.kv_split_tokens > 0) {
-    L = a.kv_split_tokens;
-  } else {
-    L = kMinSplit;
-    while (L < 8192 && total > L * 6ll * a.num_clusters) L <<= 1;
-  }
+  const bool fixed = a.kv_split_tokens > 0;
+  const long long L = fixed ? a.kv_split_tokens : kMN;
+  // per sequence: splits (fixed) or tiles (balanced)
   long long run = 0;
+  int bad = 0;
   for (int base = 0; base < S; base += 1024) {
     const int s = base + tid;
-    int ns = 0;
+    long long n = 0;
     if (s < S) {
       const int ctx = a.seq_lens[s];
-      const bool ok = ctx >= 1 && ctx <= a.max_seq_len &&
-                      ceil_div_ll(ctx, a.block_size) <= (long long)a.max_blocks_per_seq;
-      ns = ok ? (int)ceil_div_ll(ctx, L) : 0;
-      if (ns > a.max_splits) ns = 0;  // cannot happen when seq_lens <= max_seq_len
+      if (mla_seq_ok(a, ctx)) n = ceil_div_ll(ctx, L); else bad = 1;
     }
     long long ctot;
-    const long long incl = block_inclusive_scan(ns, scratch, &ctot) + run;
-    if (s < S) {
-      a.item_end[s] = incl;
-      a.nsplit[s] = ns;
-    }
+    const long long incl = block_inclusive_scan(n, scratch, &ctot) + run;
+    if (s < S) a.item_end[s] = incl;
     run += ctot;
+  }
+  if (bad) atomicOr(a.status, PA_DEV_BAD_SEQLEN);
+  __syncthreads();
+  long long per = L;
+  if (!fixed) {
+    per = ceil_div_ll(run, a.num_clusters > 0 ? a.num_clusters : 1);
+    if (per < kMinRunTiles) per = kMinRunTiles;
+  }
+  for (int s = tid; s < S; s += 1024) {
+    const long long t1 = a.item_end[s], t0 = s ? a.item_end[s - 1] : 0;
+    int ns = (int)(t1 - t0);
+    if (!fixed && t1 > t0) ns = (int)((t1 - 1) / per - t0 / per + 1);  // run boundaries inside
+    if (ns > a.max_splits) ns = 0;  // cannot happen when seq_lens <= max_seq_len
+    a.nsplit[s] = ns;
   }
   if (tid == 0) {
     a.plan[0] = run;
-    a.plan[1] = L;
+    a.plan[1] = per;
+    a.plan[2] = fixed ? 0 : 1;
   }
 }
+
+// One work piece: positions [kv_lo, kv_hi) of sequence s, its split `split`.
+struct MlaPiece {
+  int s, split, kv_lo, kv_hi;
+};
+
+// Walks a cluster's pieces in order; every warp role keeps its own walker.
+struct PieceWalk {
+  long long pos, end, step;
+  bool balanced;
+
+  __device__ void start(const MlaArgs &a, long long cluster, long long nclusters) {
+    balanced = a.plan[2] != 0;
+    if (balanced) {
+      pos = cluster * a.plan[1];
+      end = min(pos + a.plan[1], a.plan[0]);
+      step = 0;
+    } else {
+      pos = cluster;
+      end = a.plan[0];
+      step = nclusters;
+    }
+  }
+
+  __device__ bool next(const MlaArgs &a, MlaPiece &p) {
+    if (pos >= end) return false;
+    const int s = list_find(a.item_end, a.num_seqs, pos);
+    const long long first = s ? a.item_end[s - 1] : 0;
+    const int ctx = a.seq_lens[s];
+    p.s = s;
+    if (balanced) {
+      const long long per = a.plan[1];
+      const long long stop = min(end, a.item_end[s]);
+      p.split = (int)(pos / per - first / per);
+      p.kv_lo = (int)((pos - first) * kMN);
+      p.kv_hi = (int)min((stop - first) * kMN, (long long)ctx);
+      pos = stop;
+    } else {
+      const int L = (int)a.plan[1];
+      p.split = (int)(pos - first);
+      p.kv_lo = p.split * L;
+      p.kv_hi = min(p.kv_lo + L, ctx);
+      pos += step;
+    }
+    return true;
+  }
+};
 
 // ---------------------------------------------------------------------------
 // the cluster kernel
 // ---------------------------------------------------------------------------
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-               const MlaArgs a) {
+    mla_kernel(const __grid_constant__ CUtensorMap tm_kv, const MlaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  uint8_t *sQ = smem + OFF_Q;
   uint8_t *sKV = smem + OFF_KV;
   uint8_t *sX = smem + OFF_X;
   uint8_t *sXS = smem + OFF_XS;
@@ -156,16 +221,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const long long cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
   pdl_trigger();
   pdl_wait();  // the plan
-  const long long n_items = a.plan[0];
-  const int L = (int)a.plan[1];
-  const int S = a.num_seqs, bs = a.block_size;
+  const int bs = a.block_size;
 
   if (tid == 0) {
-    prefetch_tensor_map(&tm_q);
     prefetch_tensor_map(&tm_kv);
     for (int b = 0; b < kNumMBars; ++b) {
-      const bool per_warp = b == kSFree0 || b == kSFree0 + 1 || b == kPFull0 ||
-                            b == kPFull0 + 1 || b == kOFree;
+      const bool per_warp = b == kQFull || b == kSFree || b == kPFull || b == kOFree;
       mbar_init(&bar[b], per_warp ? 4u : 1u);
     }
     fence_mbar_init();
@@ -178,97 +239,100 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t tmem = *s_tmem;
   bool dead = false;
 
-  auto decode = [&](long long item, int &s, int &split, int &kv_lo, int &kv_hi) {
-    s = list_find(a.item_end, S, item);
-    split = (int)(item - (s ? a.item_end[s - 1] : 0));
-    kv_lo = split * L;
-    kv_hi = min(kv_lo + L, a.seq_lens[s]);
-  };
-
   if (warp == 4) {
     // ------------------------------------------------------------- producer
-    // The whole warp walks the items (the page cache is warp-wide); lane 0
-    // waits on the barriers and issues the copies.
-    uint32_t tiles = 0, items = 0;
-    for (long long item = cluster; item < n_items; item += nclusters) {
-      int s, split, kv_lo, kv_hi;
-      decode(item, s, split, kv_lo, kv_hi);
+    // The whole warp walks the items (the page cache is warp-wide); lanes 0
+    // and 1 load the two 32-slot halves of each tile, lane 0 waits.
+    uint32_t tiles = 0;
+    PieceWalk walk;
+    walk.start(a, cluster, nclusters);
+    MlaPiece pc_;
+    while (walk.next(a, pc_)) {
+      const int s = pc_.s, kv_lo = pc_.kv_lo, kv_hi = pc_.kv_hi;
       const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
-      if (lane == 0) {
-        if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, a.status);
-        mbar_arrive_expect_tx(&bar[kQFull], nch * kChunkQ);
-        for (int i = 0; i < nch; ++i)
-          tma_load_3d(sQ + i * kChunkQ, &tm_q, chunk_of(rank, i) * 64, 0, s, &bar[kQFull]);
-      }
       const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
       PageCache pc;
       pc.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
       for (int j = 0; j < nt; ++j) {
         const uint32_t g = tiles + j;
         const int st = g % kMlaStages;
-        const int pos = kv_lo + j * kMN;
-        const int page = pc.get(pos / bs, lane);
-        const bool ok = page >= 0 && page < a.num_blocks;
+        const int pos = kv_lo + j * kMN + lane * kMHalf;
+        const bool need = lane < 2 && pos < kv_hi;
+        const int page = pc.get(need ? pos / bs : -1, lane);
+        const bool ok = need && page >= 0 && page < a.num_blocks;
+        if (need && !ok) atomicOr(a.status, PA_DEV_BAD_BLOCK);
+        const unsigned mask = __ballot_sync(0xffffffffu, ok);
+        // into L2 now, into the ring once the stage is free: the wait for the
+        // stage then hides the HBM latency
+        if (ok)
+          for (int i = 0; i < nch; ++i)
+            tma_prefetch_3d(&tm_kv, chunk_of(rank, i) * 64, pos % bs, page);
         if (lane == 0) {
-          if (!ok) atomicOr(a.status, PA_DEV_BAD_BLOCK);
           if (g >= kMlaStages)
             mbar_wait(&bar[kKVFree0 + st], ((g / kMlaStages) - 1) & 1, dead, a.status);
-          mbar_arrive_expect_tx(&bar[kKVFull0 + st], ok ? nch * kChunkKV : 0);
-          if (ok)
-            for (int i = 0; i < nch; ++i)
-              tma_load_3d(sKV + st * STAGE_BYTES + i * kChunkKV, &tm_kv, chunk_of(rank, i) * 64,
-                          pos % bs, page, &bar[kKVFull0 + st]);
+          mbar_arrive_expect_tx(&bar[kKVFull0 + st], __popc(mask) * nch * kMHalf * 128);
         }
+        __syncwarp();
+        if (ok)
+          for (int i = 0; i < nch; ++i)
+            tma_load_3d(sKV + st * STAGE_BYTES + i * kChunkKV + lane * kMHalf * 128, &tm_kv,
+                        chunk_of(rank, i) * 64, pos % bs, page, &bar[kKVFull0 + st]);
         __syncwarp();
       }
       tiles += nt;
-      ++items;
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t tiles = 0, items = 0;
-      const uint32_t sq = smem_u32(sQ), skv = smem_u32(sKV);
-      auto issue_s = [&](uint32_t g) {
-        const int st = g % kMlaStages, b = g & 1;
-        mbar_wait(&bar[kKVFull0 + st], (g / kMlaStages) & 1, dead, a.status);
-        if (g >= 2) mbar_wait(&bar[kSFree0 + b], ((g >> 1) - 1) & 1, dead, a.status);
+      uint32_t g = 0, items = 0;
+      const uint32_t skv = smem_u32(sKV);
+      // S of tile t (global count) once its K rows have landed and the
+      // softmax has read S of tile t - 1 out of the single S buffer.
+      auto issue_s = [&](uint32_t t) {
+        const int st = t % kMlaStages;
+        mbar_wait(&bar[kKVFull0 + st], (t / kMlaStages) & 1, dead, a.status);
+        if (t > 0) mbar_wait(&bar[kSFree], (t - 1) & 1, dead, a.status);
         tc_fence_after();
         const uint32_t kb = skv + st * STAGE_BYTES;
-        for (int i = 0; i < nch; ++i)
-#pragma unroll
-          for (int sub = 0; sub < 4; ++sub) {
-            const uint64_t ad = umma_desc_sw128(sq + i * kChunkQ + sub * 32, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(kb + i * kChunkKV + sub * 32, 16, 1024);
-            tc_mma_bf16(tmem + kTmemS + b * kMN, ad, bd, IDESC_S, (i > 0 || sub > 0) ? 1u : 0u);
-          }
-        tc_commit(&bar[kSFull0 + b]);
+        for (int kk = 0; kk < nch * 4; ++kk) {
+          const uint64_t bd = umma_desc_sw128(kb + (kk >> 2) * kChunkKV + (kk & 3) * 32, 16, 1024);
+          tc_mma_bf16_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&bar[kSFull]);
       };
-      for (long long item = cluster; item < n_items; item += nclusters) {
-        int s, split, kv_lo, kv_hi;
-        decode(item, s, split, kv_lo, kv_hi);
-        const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
+      PieceWalk walk;
+      walk.start(a, cluster, nclusters);
+      MlaPiece pc_;
+      while (walk.next(a, pc_)) {
+        const int nt = (pc_.kv_hi - pc_.kv_lo + kMN - 1) / kMN;
         mbar_wait(&bar[kQFull], items & 1, dead, a.status);
-        issue_s(tiles);
+        tc_fence_after();
+        issue_s(g);
+        if (nt == 1) tc_commit(&bar[kQFree]);
+        if (nt > 1) {
+          issue_s(g + 1);
+          if (nt == 2) tc_commit(&bar[kQFree]);
+        }
         for (int j = 0; j < nt; ++j) {
-          const uint32_t g = tiles + j;
-          if (j + 1 < nt) issue_s(g + 1);
-          const int pb = g & 1;
-          mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, a.status);
+          const uint32_t t = g + j;
+          if (j + 2 < nt) {
+            issue_s(t + 2);
+            if (j + 2 == nt - 1) tc_commit(&bar[kQFree]);
+          }
+          mbar_wait(&bar[kPFull], t & 1, dead, a.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, a.status);
           tc_fence_after();
-          const uint32_t vb = skv + (g % kMlaStages) * STAGE_BYTES;
+          const uint32_t vb = skv + (t % kMlaStages) * STAGE_BYTES;
 #pragma unroll
           for (int kk = 0; kk < kMN / 16; ++kk) {
             const uint64_t bd = umma_desc_sw128(vb + kk * 16 * 128, kChunkKV, 1024);
-            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + pb * 16 + kk * 8, bd, IDESC_PV,
+            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemP + kk * 8, bd, IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&bar[kKVFree0 + g % kMlaStages]);
-          tc_commit(&bar[kODone0 + pb]);
+          tc_commit(&bar[kKVFree0 + t % kMlaStages]);
+          tc_commit(&bar[kODone]);
         }
-        tc_commit(&bar[kQFree]);
-        tiles += nt;
+        g += nt;
         ++items;
       }
     }
@@ -283,10 +347,76 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       xfull_peer[b] = cluster_map(smem_u32(&bar[kXFull0 + b]), peer);
       xfree_peer[b] = cluster_map(smem_u32(&bar[kXFree0 + b]), peer);
     }
-    uint32_t tiles = 0, items = 0;
-    for (long long item = cluster; item < n_items; item += nclusters) {
-      int s, split, kv_lo, kv_hi;
-      decode(item, s, split, kv_lo, kv_hi);
+    // This CTA's query columns of item `it` into TMEM (bf16 pairs, the A
+    // operand of the score product): 64-column chunks in contraction order.
+    auto load_q = [&](int s) {
+      const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q) + ((size_t)s * kMlaH + r) * (kMlaW / 8);
+      // two rounds of at most three 64-column chunks (the rows were
+      // prefetched into L2 while the previous item ran)
+#pragma unroll
+      for (int i0 = 0; i0 < kMaxChunks; i0 += 3) {
+        uint4 qv[3][8];
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+          if (i0 + i < nch) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x) qv[i][x] = __ldg(qrow + chunk_of(rank, i0 + i) * 8 + x);
+          }
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+          if (i0 + i < nch)
+            tc_st32(tmem + lane_off + kTmemQ + (i0 + i) * 32,
+                    *reinterpret_cast<const uint32_t(*)[32]>(qv[i]));
+      }
+      tc_wait_st();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kQFull]);
+    };
+    // Read S of tile t out of TMEM, free the buffer, stage the values and
+    // push them into the peer's exchange buffer t & 1 with one bulk copy
+    // (completion counted on the peer's mbarrier).  Row r: 16 float4 slots,
+    // slot v stored at v ^ (r % 8), so the rows a quarter-warp touches fall
+    // in different banks.  The single staging buffer is reused once the
+    // previous copy has read it.
+    auto fetch_send = [&](uint32_t t, float (&v)[kMN]) {
+      mbar_wait(&bar[kSFull], t & 1, dead, a.status);
+      tc_fence_after();
+      uint32_t raw[kMN];
+      tc_ld32(tmem + lane_off + kTmemS, *reinterpret_cast<uint32_t(*)[32]>(raw));
+      tc_ld32(tmem + lane_off + kTmemS + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+      tc_wait_ld();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kSFree]);
+#pragma unroll
+      for (int x = 0; x < kMN; ++x) v[x] = __uint_as_float(raw[x]);
+      const int b = t & 1;
+      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      named_sync(1, 128);
+      float4 *st4 = reinterpret_cast<float4 *>(sXS + r * kMN * 4);
+#pragma unroll
+      for (int x = 0; x < kMN / 4; ++x)
+        st4[x ^ (r & 7)] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+      fence_proxy_async();
+      named_sync(1, 128);
+      if (r == 0) {
+        // the peer's buffer b is free once it has consumed tile t - 2
+        if (t >= 2) mbar_wait_cluster(&bar[kXFree0 + b], ((t >> 1) - 1) & 1, dead, a.status);
+        bulk_copy_to_peer(x_peer[b], sXS, X_BYTES, xfull_peer[b]);
+        asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      }
+    };
+
+    uint32_t g = 0, items = 0;
+    PieceWalk walk;
+    walk.start(a, cluster, nclusters);
+    MlaPiece piece, next_piece;
+    bool have = walk.next(a, piece);
+    if (have) load_q(piece.s);
+    while (have) {
+      const bool have_next = walk.next(a, next_piece);
+      const int s = piece.s, split = piece.split, kv_lo = piece.kv_lo, kv_hi = piece.kv_hi;
       const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
       {
         const int pfirst = kv_lo / bs, plast = (kv_hi - 1) / bs;
@@ -303,62 +433,46 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         named_sync(1, 128);
       }
       const bool item_bad = s_bad[items & 1] != 0;
+      // the next piece's queries reach L2 while this one runs
+      if (have_next) {
+        const char *qn =
+            reinterpret_cast<const char *>(a.q) + ((size_t)next_piece.s * kMlaH + r) * kMlaW * 2;
+        for (int i = 0; i < nch; ++i)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + chunk_of(rank, i) * 128) : "memory");
+      }
+      float cur[kMN], nxt[kMN];
+      fetch_send(g, cur);
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nt; ++j) {
-        const uint32_t g = tiles + j;
-        const int b = g & 1;
+        const uint32_t t = g + j;
+        const int b = t & 1;
         const int base = kv_lo + j * kMN;
-        mbar_wait(&bar[kSFull0 + b], (g >> 1) & 1, dead, a.status);
-        tc_fence_after();
-        uint32_t raw[32];
-        tc_ld32(tmem + lane_off + kTmemS + b * kMN, raw);
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kSFree0 + b]);
-        // stage the partial scores, then one bulk copy to the peer: the staging
-        // and the peer's buffer b are free once the peer has consumed tile g - 2
-        if (g >= 2) mbar_wait_cluster(&bar[kXFree0 + b], ((g >> 1) - 1) & 1, dead, a.status);
-        // Row r of the partial scores is 8 float4s; float4 v sits in slot
-        // v ^ (r % 8), so the 8 rows a quarter-warp touches hit 8 different
-        // bank groups (plain rows of 128 bytes all start in the same banks).
-        float4 *st4 = reinterpret_cast<float4 *>(sXS + b * X_BYTES + r * kMN * 4);
-#pragma unroll
-        for (int v = 0; v < kMN / 4; ++v)
-          st4[v ^ (r & 7)] = make_float4(__uint_as_float(raw[4 * v]), __uint_as_float(raw[4 * v + 1]),
-                                         __uint_as_float(raw[4 * v + 2]), __uint_as_float(raw[4 * v + 3]));
-        fence_proxy_async();
-        named_sync(1, 128);
-        if (r == 0) {
-          mbar_arrive_expect_tx(&bar[kXFull0 + b], X_BYTES);  // the peer's tile g lands here
-          bulk_copy_to_peer(x_peer[b], sXS + b * X_BYTES, X_BYTES, xfull_peer[b]);
-        }
-        mbar_wait_cluster(&bar[kXFull0 + b], (g >> 1) & 1, dead, a.status);
-        float sc[kMN];
+        if (j + 1 < nt) fetch_send(t + 1, nxt);
+        // the peer's partial scores of tile t
+        if (r == 0) mbar_arrive_expect_tx(&bar[kXFull0 + b], X_BYTES);
+        mbar_wait_cluster(&bar[kXFull0 + b], (t >> 1) & 1, dead, a.status);
         const float4 *xr = reinterpret_cast<const float4 *>(sX + b * X_BYTES + r * kMN * 4);
 #pragma unroll
-        for (int v = 0; v < kMN / 4; ++v) {
-          const float4 o4 = xr[v ^ (r & 7)];
-          sc[4 * v] = __uint_as_float(raw[4 * v]) + o4.x;
-          sc[4 * v + 1] = __uint_as_float(raw[4 * v + 1]) + o4.y;
-          sc[4 * v + 2] = __uint_as_float(raw[4 * v + 2]) + o4.z;
-          sc[4 * v + 3] = __uint_as_float(raw[4 * v + 3]) + o4.w;
+        for (int x = 0; x < kMN / 4; ++x) {
+          const float4 o4 = xr[x ^ (r & 7)];
+          cur[4 * x] += o4.x;
+          cur[4 * x + 1] += o4.y;
+          cur[4 * x + 2] += o4.z;
+          cur[4 * x + 3] += o4.w;
         }
         named_sync(1, 128);
-        // Hand our buffer b back to the peer.  Every thread's reads of it have
-        // returned (their sums are in registers) and the CTA barrier above
-        // orders them before this arrive, so a relaxed arrive suffices; a
-        // cluster-scope release arrive cost about 1.8k cycles a tile.
+        // Hand buffer b back to the peer: every read of it has returned and
+        // the barrier above orders them before this arrive.
         if (r == 0) mbar_arrive_remote_relaxed(xfree_peer[b]);
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int c = 0; c < kMN; ++c) {
-          sc[c] = (base + c < kv_hi) ? sc[c] * a.scale_log2 : -INFINITY;
-          mxa[c & 3] = fmaxf(mxa[c & 3], sc[c]);
+          cur[c] = (base + c < kv_hi) ? cur[c] * a.scale_log2 : -INFINITY;
+          mxa[c & 3] = fmaxf(mxa[c & 3], cur[c]);
         }
         const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-        // P buffer b was last read by the PV product of tile g - 2
-        if (g >= 2) mbar_wait(&bar[kODone0 + b], ((g >> 1) - 1) & 1, dead, a.status);
+        // P and O were last touched by the value product of tile t - 1
+        if (t > 0) mbar_wait(&bar[kODone], (t - 1) & 1, dead, a.status);
         tc_fence_after();
         float alpha = 1.f;
         bool rescale = false;
@@ -369,8 +483,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
           rescale = j > 0;
         }
         if (__any_sync(0xffffffffu, rescale)) {
-          mbar_wait(&bar[kODone0 + (b ^ 1)], ((g - 1) >> 1) & 1, dead, a.status);
-          tc_fence_after();
           const float al = rescale ? alpha : 1.f;
           for (int c0 = 0; c0 < kVHalf; c0 += 32) {
             uint32_t o[32];
@@ -387,20 +499,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         uint32_t pw[kMN / 2];
 #pragma unroll
         for (int x = 0; x < kMN / 2; ++x) {
-          const float p0 = fast_exp2(sc[2 * x] - mu);
-          const float p1 = fast_exp2(sc[2 * x + 1] - mu);
+          const float p0 = fast_exp2(cur[2 * x] - mu);
+          const float p1 = fast_exp2(cur[2 * x + 1] - mu);
           suma[x & 3] += p0 + p1;
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
         }
-        tc_st16(tmem + lane_off + kTmemP + b * 16, pw);
+        tc_st32(tmem + lane_off + kTmemP, pw);
         tc_wait_st();
         l += (suma[0] + suma[1]) + (suma[2] + suma[3]);
         if (j == nt - 1 && kv_hi - base < kMN) {
-          // slots past the sequence end may hold anything; 0 * NaN is NaN
-          mbar_wait(&bar[kKVFull0 + g % kMlaStages], (g / kMlaStages) & 1, dead, a.status);
+          // slots past the sequence end may hold anything; 0 * NaN is NaN.
+          // S of this tile is done, so its K rows may be overwritten too.
+          mbar_wait(&bar[kKVFull0 + t % kMlaStages], (t / kMlaStages) & 1, dead, a.status);
           const int first = kv_hi - base;
-          uint8_t *vb = sKV + (g % kMlaStages) * STAGE_BYTES;
+          uint8_t *vb = sKV + (t % kMlaStages) * STAGE_BYTES;
           const int per_chunk = (kMN - first) * 8;
           for (int e = r; e < 4 * per_chunk; e += 128) {
             const int ci = e / per_chunk, rem = e % per_chunk;
@@ -411,11 +524,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bar[kPFull0 + b]);
+        if (lane == 0) mbar_arrive(&bar[kPFull]);
+        if (j + 1 < nt) {
+#pragma unroll
+          for (int x = 0; x < kMN; ++x) cur[x] = nxt[x];
+        }
+      }
+      // the next piece's queries, once the last score product of this one is done
+      if (have_next) {
+        mbar_wait(&bar[kQFree], items & 1, dead, a.status);
+        tc_fence_after();
+        load_q(next_piece.s);
       }
       // ---- epilogue
-      const uint32_t glast = tiles + nt - 1;
-      mbar_wait(&bar[kODone0 + (glast & 1)], (glast >> 1) & 1, dead, a.status);
+      const uint32_t glast = g + nt - 1;
+      mbar_wait(&bar[kODone], glast & 1, dead, a.status);
       tc_fence_after();
       const int ns = a.nsplit[s];
       const bool direct = ns == 1;
@@ -458,9 +581,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kOFree]);
-      tiles += nt;
+      g += nt;
       ++items;
+      piece = next_piece;
+      have = have_next;
     }
+    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
@@ -472,40 +598,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 // ---------------------------------------------------------------------------
 // merge of split partials: one block per (sequence, head) row
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) mla_merge_kernel(const MlaArgs a) {
-  const int tid = threadIdx.x;
+// One warp per (sequence, head) row: lane q < 32 holds split q's
+// log-sum-exp (more splits loop), every lane 16 of the 512 columns.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(32 * kMergeWarps) mla_merge_kernel(const MlaArgs a) {
+  const int lane = threadIdx.x & 31;
   const long long rows = (long long)a.num_seqs * kMlaH;
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
   pdl_trigger();
   pdl_wait();  // the split partials
   __nv_bfloat16 *out = reinterpret_cast<__nv_bfloat16 *>(a.out);
-  for (long long row = blockIdx.x; row < rows; row += gridDim.x) {
+  for (long long row = gw; row < rows; row += nw) {
     const int s = (int)(row / kMlaH);
     const int ns = a.nsplit[s];
     if (ns == 1) continue;
-    __nv_bfloat162 *dst = reinterpret_cast<__nv_bfloat162 *>(out + row * kMlaL) + tid;
+    uint4 *dst = reinterpret_cast<uint4 *>(out + row * kMlaL) + lane * 2;
     if (ns == 0) {
-      *dst = __floats2bfloat162_rn(0.f, 0.f);
+      dst[0] = make_uint4(0u, 0u, 0u, 0u);
+      dst[1] = make_uint4(0u, 0u, 0u, 0u);
       continue;
     }
     const long long base = row * a.max_splits;
     float M = -INFINITY;
-    bool bad = false;
-    for (int q = 0; q < ns; ++q) {
+    int bad = 0;
+    for (int q = lane; q < ns; q += 32) {
       const float v = a.part_lse[base + q];
-      if (isnan(v)) bad = true; else M = fmaxf(M, v);
+      if (isnan(v)) bad = 1; else M = fmaxf(M, v);
     }
-    float L = 0.f, x = 0.f, y = 0.f;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+      M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      bad |= __shfl_xor_sync(0xffffffffu, bad, o);
+    }
+    float acc[16];
+#pragma unroll
+    for (int x = 0; x < 16; ++x) acc[x] = 0.f;
+    float L = 0.f;
     if (!bad && M != -INFINITY) {
       for (int q = 0; q < ns; ++q) {
         const float w = fast_exp2(a.part_lse[base + q] - M);
-        const float2 v = reinterpret_cast<const float2 *>(a.part_o + (base + q) * kMlaL)[tid];
+        const float4 *src = reinterpret_cast<const float4 *>(a.part_o + (base + q) * kMlaL) + lane * 4;
         L += w;
-        x = fmaf(w, v.x, x);
-        y = fmaf(w, v.y, y);
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const float4 x4 = __ldg(src + v);
+          acc[4 * v] = fmaf(w, x4.x, acc[4 * v]);
+          acc[4 * v + 1] = fmaf(w, x4.y, acc[4 * v + 1]);
+          acc[4 * v + 2] = fmaf(w, x4.z, acc[4 * v + 2]);
+          acc[4 * v + 3] = fmaf(w, x4.w, acc[4 * v + 3]);
+        }
       }
     }
     const float inv = (bad || !(L > 0.f)) ? 0.f : 1.f / L;
-    *dst = __floats2bfloat162_rn(x * inv, y * inv);
+    uint32_t w[8];
+#pragma unroll
+    for (int x = 0; x < 8; ++x) {
+      const __nv_bfloat162 h2 = __floats2bfloat162_rn(acc[2 * x] * inv, acc[2 * x + 1] * inv);
+      w[x] = *reinterpret_cast<const uint32_t *>(&h2);
+    }
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -518,8 +671,10 @@ size_t al256(size_t x) { return (x + 255) & ~size_t(255); }
 
 MlaLayout mla_layout(int num_seqs, int max_seq_len, int kvs) {
   MlaLayout l{};
-  const long long lmin = kvs > 0 ? kvs : kMinSplit;
-  l.max_splits = (int)ceil_div_ll(max_seq_len > 0 ? max_seq_len : 1, lmin);
+  // fixed splits: ceil(len / kvs); automatic runs of at least kMinSplit
+  // positions: a sequence meets at most ceil(len / kMinSplit) + 1 of them
+  l.max_splits = kvs > 0 ? (int)ceil_div_ll(max_seq_len > 0 ? max_seq_len : 1, kvs)
+                         : (int)ceil_div_ll(max_seq_len > 0 ? max_seq_len : 1, kMinSplit) + 1;
   const size_t S = num_seqs > 0 ? num_seqs : 1;
   const size_t rows = (size_t)S * kMlaH * l.max_splits;
   size_t off = 0;
@@ -624,29 +779,27 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
   a.part_lse = reinterpret_cast<float *>(w + lay.part_lse);
   a.status = status;
 
-  CUtensorMap tm_q, tm_kv;
-  const unsigned long long qd[3] = {kMlaW, kMlaH, (unsigned long long)num_seqs};
-  const unsigned long long qs[2] = {kMlaW * 2, (unsigned long long)kMlaH * kMlaW * 2};
-  const unsigned int qb[3] = {64, 128, 1};
+  CUtensorMap tm_kv;
   const unsigned long long kd[3] = {kMlaW, (unsigned long long)block_size,
                                     (unsigned long long)num_blocks};
   const unsigned long long ks[2] = {kMlaW * 2, (unsigned long long)block_size * kMlaW * 2};
-  const unsigned int kb[3] = {64, kMN, 1};
-  if (!encode_tiled(&tm_q, q, PA_BF16, 3, qd, qs, qb, true) ||
-      !encode_tiled(&tm_kv, kv_cache, PA_BF16, 3, kd, ks, kb, true))
-    return PA_ERR_CUDA;
+  const unsigned int kb[3] = {64, kMHalf, 1};
+  if (!encode_tiled(&tm_kv, kv_cache, PA_BF16, 3, kd, ks, kb, true)) return PA_ERR_CUDA;
 
   int slot = prof_begin(PA_K_PLAN, st);
   cudaError_t err = launch_dependent(mla_plan_kernel, dim3(1), dim3(1024), 0, st, a);
   prof_end(slot, st);
   if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA, st);
-  err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads),
-                                     MLA_SMEM, st, tm_q, tm_kv, a);
+  err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads), MLA_SMEM, st,
+                         tm_kv, a);
   prof_end(slot, st);
   if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA_MERGE, st);
-  err = launch_dependent(mla_merge_kernel, dim3(num_sms * 4), dim3(256), 0, st, a);
+  long long mblocks = ((long long)num_seqs * kMlaH + kMergeWarps - 1) / kMergeWarps;
+  if (mblocks > (long long)num_sms * 16) mblocks = (long long)num_sms * 16;
+  err = launch_dependent(mla_merge_kernel, dim3((unsigned)mblocks), dim3(32 * kMergeWarps), 0, st,
+                         a);
   prof_end(slot, st);
   if (err != cudaSuccess) return PA_ERR_CUDA;
   return PA_OK;

@@ -87,3 +87,39 @@ def oracle_mla_prefill(b, rows=None):
                            b.seq_lens.numpy(), b.query_start_loc.numpy(), b.kv_lora_rank,
                            b.qk_nope_dim, b.rope_dim, b.v_head_dim, b.block_size, b.scale,
                            rows=rows)
+
+
+def tile_edge_rows(b, requests, tile_rows=128):
+    """Flat (token * H + head) rows at the first and the last row of every
+    tensor-core tile of the listed requests: a tile packs tile_rows / G
+    tokens x the G query heads of one KV head, so its first row is (first
+    token, first head of the group) and its last (last token, last head)."""
+    H, Hk = b.num_heads, b.num_kv_heads
+    G = H // Hk
+    TQ = tile_rows // G
+    qsl = b.query_start_loc.numpy()
+    rows = []
+    for s in requests:
+        q0, q1 = int(qsl[s]), int(qsl[s + 1])
+        for t0 in range(0, q1 - q0, TQ):
+            t_last = min(t0 + TQ, q1 - q0) - 1
+            for k in range(Hk):
+                rows.append((q0 + t0) * H + k * G)
+                rows.append((q0 + t_last) * H + k * G + G - 1)
+    return np.asarray(rows, dtype=np.int64)
+
+
+def longest_requests(b, kind):
+    """Index of the longest prefill ("prefill": no cached prefix) or extend
+    ("extend") request of a batch, by new tokens."""
+    qsl = b.query_start_loc.numpy()
+    ctx = b.seq_lens.numpy()
+    best, best_len = None, 0
+    for s in range(b.num_seqs):
+        ql = int(qsl[s + 1] - qsl[s])
+        is_prefill = ql == int(ctx[s]) and ql > 1
+        is_extend = 1 < ql < int(ctx[s])
+        if ((kind == "prefill" and is_prefill) or (kind == "extend" and is_extend)) and ql > best_len:
+            best, best_len = s, ql
+    return best
+

@@ -46,15 +46,22 @@ def test_llama_decode_b64_full():
 
 
 def test_mixed_qwen3_sampled():
+    """Every decode row, 1536 random extend / prefill rows, and the first and
+    last row of every 128-row tile of the longest prefill and extend."""
     b = inputs.mixed_qwen3()
-    rows = parity.sample_rows(b, 1536, seed=1)
+    edges = parity.tile_edge_rows(b, [parity.longest_requests(b, "prefill"),
+                                      parity.longest_requests(b, "extend")])
+    rows = np.unique(np.concatenate([parity.sample_rows(b, 1536, seed=1), edges]))
     got = parity.gpu_forward(b)
     parity.compare(got, parity.oracle_forward(b, rows=rows), "bf16", rows=rows, what="mixed")
 
 
 def test_long_chunked_sampled():
+    """Every decode row, 96 random extend rows, and the first and last row of
+    every 128-row tile of one 2048-token extend on its 96K prefix."""
     b = inputs.long_chunked()
-    rows = parity.sample_rows(b, 96, seed=2)
+    edges = parity.tile_edge_rows(b, [parity.longest_requests(b, "extend")])
+    rows = np.unique(np.concatenate([parity.sample_rows(b, 96, seed=2), edges]))
     got = parity.gpu_forward(b)
     parity.compare(got, parity.oracle_forward(b, rows=rows), "bf16", rows=rows, what="long")
 
