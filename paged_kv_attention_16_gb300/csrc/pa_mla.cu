@@ -37,8 +37,12 @@ namespace {
 constexpr int kMlaL = 512, kMlaR = 64, kMlaW = 576, kMlaH = 128;
 constexpr int kMN = 64;             // KV positions per tile
 constexpr int kMHalf = 32;          // slots per TMA box (a box never crosses a page)
-constexpr int kMlaThreads = 192;    // 4 softmax warps, producer warp, MMA warp
-constexpr int kMlaStages = 3;
+constexpr int kSoftWarps = 8;       // two per TMEM lane quarter: each thread half a row
+constexpr int kSoftThreads = 32 * kSoftWarps;
+constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
+constexpr int kMlaThreads = 32 * (kSoftWarps + 2);
+constexpr int kPrefetchTiles = 4;   // KV tiles brought into L2 ahead of the ring
+constexpr int kMlaStages = 4;
 constexpr int kChunkKV = kMN * 128; // one 64-column chunk of a tile: 64 rows x 128 B
 constexpr int kMaxChunks = 5;
 constexpr int kVHalf = 256;         // value columns per CTA
@@ -53,15 +57,16 @@ constexpr int kMinSplit = 512;
 constexpr int STAGE_BYTES = kMaxChunks * kChunkKV;
 constexpr int X_BYTES = 128 * kMN * 4;               // one tile of partial scores
 constexpr int OFF_KV = 0;
-constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;  // the peer's partials, 2 buffers
-constexpr int OFF_XS = OFF_X + 2 * X_BYTES;               // own partials staged for the copy
+constexpr int OFF_X = OFF_KV + kMlaStages * STAGE_BYTES;  // the peer's partials of a tile
+constexpr int OFF_XS = OFF_X + X_BYTES;                   // own partials staged for the copy
 constexpr int OFF_BAR = OFF_XS + X_BYTES;
 
 enum MBar {
   kQFull = 0, kQFree, kKVFull0, kKVFree0 = kKVFull0 + kMlaStages, kSFull = kKVFree0 + kMlaStages,
-  kSFree, kPFull, kODone, kOFree, kXFull0, kXFree0 = kXFull0 + 2, kNumMBars = kXFree0 + 2
+  kSFree, kPFull, kODone, kOFree, kXFull, kXFree, kNumMBars
 };
-constexpr int OFF_MISC = OFF_BAR + kNumMBars * 8;
+constexpr int OFF_RED = OFF_BAR + kNumMBars * 8;          // 256 floats: row halves' maxima
+constexpr int OFF_MISC = OFF_RED + kSoftThreads * 4;
 constexpr int MLA_SMEM = OFF_MISC + 64 + 1024;
 static_assert(MLA_SMEM <= 232448, "shared memory budget");
 
@@ -76,6 +81,8 @@ struct MlaArgs {
   int num_seqs, block_size, max_blocks_per_seq, num_blocks, max_seq_len, kv_split_tokens;
   float scale_log2;
   int max_splits, num_clusters;
+  int page_tiles;       // 1: every 64-position tile lies in one page (block_size % 64 == 0
+                        // and tiles start at multiples of 64): one box per 4 chunks
   // plan[2] = 0 (fixed split length): [0] work items, [1] split length,
   //   item_end = inclusive prefix of each sequence's splits;
   // plan[2] = 1 (balanced): [0] 64-position tiles in all, [1] tiles per
@@ -205,13 +212,15 @@ struct PieceWalk {
 // the cluster kernel
 // ---------------------------------------------------------------------------
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
-    mla_kernel(const __grid_constant__ CUtensorMap tm_kv, const MlaArgs a) {
+    mla_kernel(const __grid_constant__ CUtensorMap tm_kv, const __grid_constant__ CUtensorMap tm_kv4,
+               const MlaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t *sKV = smem + OFF_KV;
   uint8_t *sX = smem + OFF_X;
   uint8_t *sXS = smem + OFF_XS;
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + OFF_BAR);
+  float *s_red = reinterpret_cast<float *>(smem + OFF_RED);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + OFF_MISC);
   int *s_bad = reinterpret_cast<int *>(smem + OFF_MISC + 16);
 
@@ -225,13 +234,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
 
   if (tid == 0) {
     prefetch_tensor_map(&tm_kv);
+    prefetch_tensor_map(&tm_kv4);
     for (int b = 0; b < kNumMBars; ++b) {
       const bool per_warp = b == kQFull || b == kSFree || b == kPFull || b == kOFree;
-      mbar_init(&bar[b], per_warp ? 4u : 1u);
+      mbar_init(&bar[b], per_warp ? (uint32_t)kSoftWarps : 1u);
     }
     fence_mbar_init();
   }
-  if (warp == 5) tc_alloc(s_tmem, kTmemCols);
+  if (warp == kMmaWarp) tc_alloc(s_tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // the peer's barriers exist before anyone arrives remotely
@@ -239,10 +249,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   const uint32_t tmem = *s_tmem;
   bool dead = false;
 
-  if (warp == 4) {
+  if (warp == kProducerWarp) {
     // ------------------------------------------------------------- producer
-    // The whole warp walks the items (the page cache is warp-wide); lanes 0
-    // and 1 load the two 32-slot halves of each tile, lane 0 waits.
+    // The whole warp walks the pieces (the page caches are warp-wide); lanes
+    // 0 and 1 handle the two 32-slot halves of each tile, lane 0 waits.  A
+    // second cursor brings the tile kPrefetchTiles ahead into L2, so that a
+    // ring load, issued once its stage is free, is served from L2.
     uint32_t tiles = 0;
     PieceWalk walk;
     walk.start(a, cluster, nclusters);
@@ -251,37 +263,64 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       const int s = pc_.s, kv_lo = pc_.kv_lo, kv_hi = pc_.kv_hi;
       const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
       const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
-      PageCache pc;
+      PageCache pc, pf;
       pc.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
+      pf.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
+      // A tile's rows: with page_tiles, one box of 4 latent chunks x 64 slots
+      // (whole 512-byte row spans, so the copy engine moves few large pieces)
+      // plus, on CTA 0, one box for the rope chunk; otherwise one 64-column x
+      // 32-slot box per chunk and half tile (lanes 0 and 1).
+      const bool big = a.page_tiles != 0;
+      const int c4 = rank == 0 ? 0 : 4;  // first latent chunk of this CTA
+      auto prefetch = [&](int j) {
+        const int pos = kv_lo + j * kMN + lane * kMHalf;
+        const bool need = (big ? lane == 0 : lane < 2) && j < nt && pos < kv_hi;
+        const int page = pf.get(need ? pos / bs : -1, lane);
+        if (need && page >= 0 && page < a.num_blocks) {
+          if (big) {
+            tma_prefetch_4d(&tm_kv4, 0, pos % bs, c4, page);
+            if (rank == 0) tma_prefetch_3d(&tm_kv, 8 * 64, pos % bs, page);
+          } else {
+            for (int i = 0; i < nch; ++i)
+              tma_prefetch_3d(&tm_kv, chunk_of(rank, i) * 64, pos % bs, page);
+          }
+        }
+      };
+      for (int j = 0; j < kPrefetchTiles; ++j) prefetch(j);
       for (int j = 0; j < nt; ++j) {
+        prefetch(j + kPrefetchTiles);
         const uint32_t g = tiles + j;
         const int st = g % kMlaStages;
         const int pos = kv_lo + j * kMN + lane * kMHalf;
-        const bool need = lane < 2 && pos < kv_hi;
+        const bool need = (big ? lane == 0 : lane < 2) && pos < kv_hi;
         const int page = pc.get(need ? pos / bs : -1, lane);
         const bool ok = need && page >= 0 && page < a.num_blocks;
         if (need && !ok) atomicOr(a.status, PA_DEV_BAD_BLOCK);
         const unsigned mask = __ballot_sync(0xffffffffu, ok);
-        // into L2 now, into the ring once the stage is free: the wait for the
-        // stage then hides the HBM latency
-        if (ok)
-          for (int i = 0; i < nch; ++i)
-            tma_prefetch_3d(&tm_kv, chunk_of(rank, i) * 64, pos % bs, page);
         if (lane == 0) {
           if (g >= kMlaStages)
             mbar_wait(&bar[kKVFree0 + st], ((g / kMlaStages) - 1) & 1, dead, a.status);
-          mbar_arrive_expect_tx(&bar[kKVFull0 + st], __popc(mask) * nch * kMHalf * 128);
+          mbar_arrive_expect_tx(&bar[kKVFull0 + st],
+                                __popc(mask) * nch * (big ? kMN : kMHalf) * 128);
         }
         __syncwarp();
-        if (ok)
-          for (int i = 0; i < nch; ++i)
-            tma_load_3d(sKV + st * STAGE_BYTES + i * kChunkKV + lane * kMHalf * 128, &tm_kv,
-                        chunk_of(rank, i) * 64, pos % bs, page, &bar[kKVFull0 + st]);
+        if (ok) {
+          uint8_t *dst = sKV + st * STAGE_BYTES;
+          if (big) {
+            tma_load_4d(dst, &tm_kv4, 0, pos % bs, c4, page, &bar[kKVFull0 + st]);
+            if (rank == 0)
+              tma_load_3d(dst + 4 * kChunkKV, &tm_kv, 8 * 64, pos % bs, page, &bar[kKVFull0 + st]);
+          } else {
+            for (int i = 0; i < nch; ++i)
+              tma_load_3d(dst + i * kChunkKV + lane * kMHalf * 128, &tm_kv, chunk_of(rank, i) * 64,
+                          pos % bs, page, &bar[kKVFull0 + st]);
+          }
+        }
         __syncwarp();
       }
       tiles += nt;
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t g = 0, items = 0;
@@ -339,71 +378,62 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int r = tid;  // head == TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    uint32_t x_peer[2], xfull_peer[2], xfree_peer[2];
-    for (int b = 0; b < 2; ++b) {
-      x_peer[b] = cluster_map(smem_u32(sX + b * X_BYTES), peer);
-      xfull_peer[b] = cluster_map(smem_u32(&bar[kXFull0 + b]), peer);
-      xfree_peer[b] = cluster_map(smem_u32(&bar[kXFree0 + b]), peer);
-    }
-    // This CTA's query columns of item `it` into TMEM (bf16 pairs, the A
-    // operand of the score product): 64-column chunks in contraction order.
+    // Thread = (head r = TMEM lane, half h): positions 32h .. 32h + 31 of each
+    // tile, value columns 128h .. 128h + 127 of O.
+    constexpr int kHalfN = kMN / 2;
+    const int r = (warp & 3) * 32 + lane;
+    const int h = warp >> 2;
+    const int partner = tid ^ 128;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t x_peer = cluster_map(smem_u32(sX), peer);
+    const uint32_t xfull_peer = cluster_map(smem_u32(&bar[kXFull]), peer);
+    const uint32_t xfree_peer = cluster_map(smem_u32(&bar[kXFree]), peer);
+    // This CTA's query columns of sequence s into TMEM (bf16 pairs, the A
+    // operand of the score product): 64-column chunks in contraction order,
+    // the two halves of a row taking alternate chunks.
     auto load_q = [&](int s) {
       const uint4 *qrow = reinterpret_cast<const uint4 *>(a.q) + ((size_t)s * kMlaH + r) * (kMlaW / 8);
-      // two rounds of at most three 64-column chunks (the rows were
-      // prefetched into L2 while the previous item ran)
+#pragma unroll 1
+      for (int i = h; i < nch; i += 2) {  // one chunk at a time (the rows are in L2)
+        uint4 qv[8];
 #pragma unroll
-      for (int i0 = 0; i0 < kMaxChunks; i0 += 3) {
-        uint4 qv[3][8];
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-          if (i0 + i < nch) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x) qv[i][x] = __ldg(qrow + chunk_of(rank, i0 + i) * 8 + x);
-          }
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-          if (i0 + i < nch)
-            tc_st32(tmem + lane_off + kTmemQ + (i0 + i) * 32,
-                    *reinterpret_cast<const uint32_t(*)[32]>(qv[i]));
+        for (int x = 0; x < 8; ++x) qv[x] = __ldg(qrow + chunk_of(rank, i) * 8 + x);
+        tc_st32(tmem + lane_off + kTmemQ + i * 32, *reinterpret_cast<const uint32_t(*)[32]>(qv));
       }
       tc_wait_st();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kQFull]);
     };
-    // Read S of tile t out of TMEM, free the buffer, stage the values and
-    // push them into the peer's exchange buffer t & 1 with one bulk copy
-    // (completion counted on the peer's mbarrier).  Row r: 16 float4 slots,
-    // slot v stored at v ^ (r % 8), so the rows a quarter-warp touches fall
-    // in different banks.  The single staging buffer is reused once the
-    // previous copy has read it.
-    auto fetch_send = [&](uint32_t t, float (&v)[kMN]) {
+    // Read this thread's 32 scores of tile t out of TMEM, free the buffer,
+    // stage them and push the tile into the peer's exchange buffer with one
+    // bulk copy (completion counted on the peer's mbarrier).  Row r: 16
+    // float4 slots, slot v stored at v ^ (r % 8), so the rows a quarter-warp
+    // touches fall in different banks.  Both buffers hold one tile: the
+    // staging buffer is reused once the previous copy has read it, the
+    // peer's buffer once the peer has consumed tile t - 1.
+    auto fetch_send = [&](uint32_t t, float (&v)[kHalfN]) {
       mbar_wait(&bar[kSFull], t & 1, dead, a.status);
       tc_fence_after();
-      uint32_t raw[kMN];
-      tc_ld32(tmem + lane_off + kTmemS, *reinterpret_cast<uint32_t(*)[32]>(raw));
-      tc_ld32(tmem + lane_off + kTmemS + 32, *reinterpret_cast<uint32_t(*)[32]>(raw + 32));
+      uint32_t raw[kHalfN];
+      tc_ld32(tmem + lane_off + kTmemS + h * kHalfN, raw);
       tc_wait_ld();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kSFree]);
 #pragma unroll
-      for (int x = 0; x < kMN; ++x) v[x] = __uint_as_float(raw[x]);
-      const int b = t & 1;
-      if (r == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      named_sync(1, 128);
+      for (int x = 0; x < kHalfN; ++x) v[x] = __uint_as_float(raw[x]);
+      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      named_sync(1, kSoftThreads);
       float4 *st4 = reinterpret_cast<float4 *>(sXS + r * kMN * 4);
 #pragma unroll
-      for (int x = 0; x < kMN / 4; ++x)
-        st4[x ^ (r & 7)] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+      for (int x = 0; x < kHalfN / 4; ++x)
+        st4[(8 * h + x) ^ (r & 7)] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
       fence_proxy_async();
-      named_sync(1, 128);
-      if (r == 0) {
-        // the peer's buffer b is free once it has consumed tile t - 2
-        if (t >= 2) mbar_wait_cluster(&bar[kXFree0 + b], ((t >> 1) - 1) & 1, dead, a.status);
-        bulk_copy_to_peer(x_peer[b], sXS, X_BYTES, xfull_peer[b]);
+      named_sync(1, kSoftThreads);
+      if (tid == 0) {
+        if (t >= 1) mbar_wait_cluster(&bar[kXFree], (t - 1) & 1, dead, a.status);
+        bulk_copy_to_peer(x_peer, sXS, X_BYTES, xfull_peer);
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     };
@@ -422,55 +452,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         const int pfirst = kv_lo / bs, plast = (kv_hi - 1) / bs;
         const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
         int bad = 0;
-        for (int lp = pfirst + r; lp <= plast; lp += 128) {
+        for (int lp = pfirst + tid; lp <= plast; lp += kSoftThreads) {
           const int pg = lp < a.max_blocks_per_seq ? __ldg(bt + lp) : -1;
           if (pg < 0 || pg >= a.num_blocks) bad = 1;
         }
         bad = __any_sync(0xffffffffu, bad);
-        if (r == 0) s_bad[items & 1] = 0;
-        named_sync(1, 128);
+        if (tid == 0) s_bad[items & 1] = 0;
+        named_sync(1, kSoftThreads);
         if (bad && lane == 0) atomicOr(&s_bad[items & 1], 1);
-        named_sync(1, 128);
+        named_sync(1, kSoftThreads);
       }
       const bool item_bad = s_bad[items & 1] != 0;
       // the next piece's queries reach L2 while this one runs
       if (have_next) {
         const char *qn =
             reinterpret_cast<const char *>(a.q) + ((size_t)next_piece.s * kMlaH + r) * kMlaW * 2;
-        for (int i = 0; i < nch; ++i)
+        for (int i = h; i < nch; i += 2)
           asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + chunk_of(rank, i) * 128) : "memory");
       }
-      float cur[kMN], nxt[kMN];
+      float cur[kHalfN], nxt[kHalfN];
       fetch_send(g, cur);
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f;  // l: this half's share of the row sum
       for (int j = 0; j < nt; ++j) {
         const uint32_t t = g + j;
-        const int b = t & 1;
-        const int base = kv_lo + j * kMN;
-        if (j + 1 < nt) fetch_send(t + 1, nxt);
+        const int base = kv_lo + j * kMN + h * kHalfN;
         // the peer's partial scores of tile t
-        if (r == 0) mbar_arrive_expect_tx(&bar[kXFull0 + b], X_BYTES);
-        mbar_wait_cluster(&bar[kXFull0 + b], (t >> 1) & 1, dead, a.status);
-        const float4 *xr = reinterpret_cast<const float4 *>(sX + b * X_BYTES + r * kMN * 4);
-#pragma unroll
-        for (int x = 0; x < kMN / 4; ++x) {
-          const float4 o4 = xr[x ^ (r & 7)];
-          cur[4 * x] += o4.x;
-          cur[4 * x + 1] += o4.y;
-          cur[4 * x + 2] += o4.z;
-          cur[4 * x + 3] += o4.w;
-        }
-        named_sync(1, 128);
-        // Hand buffer b back to the peer: every read of it has returned and
-        // the barrier above orders them before this arrive.
-        if (r == 0) mbar_arrive_remote_relaxed(xfree_peer[b]);
+        if (tid == 0) mbar_arrive_expect_tx(&bar[kXFull], X_BYTES);
+        mbar_wait_cluster(&bar[kXFull], t & 1, dead, a.status);
+        const float4 *xr = reinterpret_cast<const float4 *>(sX + r * kMN * 4);
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int c = 0; c < kMN; ++c) {
-          cur[c] = (base + c < kv_hi) ? cur[c] * a.scale_log2 : -INFINITY;
-          mxa[c & 3] = fmaxf(mxa[c & 3], cur[c]);
+        for (int x = 0; x < kHalfN / 4; ++x) {
+          const float4 o4 = xr[(8 * h + x) ^ (r & 7)];
+          const float e[4] = {o4.x, o4.y, o4.z, o4.w};
+#pragma unroll
+          for (int y = 0; y < 4; ++y) {
+            const int c = 4 * x + y;
+            cur[c] = (base + c < kv_hi) ? (cur[c] + e[y]) * a.scale_log2 : -INFINITY;
+            mxa[y] = fmaxf(mxa[y], cur[c]);
+          }
         }
-        const float mx = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        // (the named barriers of the previous tile's exchange separate this
+        // write from the partner's read of the previous maximum)
+        float *red = s_red;
+        red[tid] = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        // every read of the exchange buffer is done, both halves' maxima are posted
+        named_sync(1, kSoftThreads);
+        if (tid == 0) mbar_arrive_remote_relaxed(xfree_peer);
+        const float mx = fmaxf(red[tid], red[partner]);
+        // then this CTA's partial scores of the next tile go to the peer
+        if (j + 1 < nt) fetch_send(t + 1, nxt);
         // P and O were last touched by the value product of tile t - 1
         if (t > 0) mbar_wait(&bar[kODone], (t - 1) & 1, dead, a.status);
         tc_fence_after();
@@ -484,38 +515,39 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         }
         if (__any_sync(0xffffffffu, rescale)) {
           const float al = rescale ? alpha : 1.f;
-          for (int c0 = 0; c0 < kVHalf; c0 += 32) {
+          for (int c0 = 0; c0 < kVHalf / 2; c0 += 32) {
             uint32_t o[32];
-            tc_ld32(tmem + lane_off + kTmemO + c0, o);
+            tc_ld32(tmem + lane_off + kTmemO + h * (kVHalf / 2) + c0, o);
             tc_wait_ld();
 #pragma unroll
             for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * al);
-            tc_st32(tmem + lane_off + kTmemO + c0, o);
+            tc_st32(tmem + lane_off + kTmemO + h * (kVHalf / 2) + c0, o);
           }
           tc_wait_st();
         }
         const float mu = m == -INFINITY ? 0.f : m;
         float suma[4] = {0.f, 0.f, 0.f, 0.f};
-        uint32_t pw[kMN / 2];
+        uint32_t pw[kHalfN / 2];
 #pragma unroll
-        for (int x = 0; x < kMN / 2; ++x) {
+        for (int x = 0; x < kHalfN / 2; ++x) {
           const float p0 = fast_exp2(cur[2 * x] - mu);
           const float p1 = fast_exp2(cur[2 * x + 1] - mu);
           suma[x & 3] += p0 + p1;
           const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
           pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
         }
-        tc_st32(tmem + lane_off + kTmemP, pw);
+        tc_st16(tmem + lane_off + kTmemP + h * (kHalfN / 2), pw);
         tc_wait_st();
         l += (suma[0] + suma[1]) + (suma[2] + suma[3]);
-        if (j == nt - 1 && kv_hi - base < kMN) {
+        const int tile0 = kv_lo + j * kMN;
+        if (j == nt - 1 && kv_hi - tile0 < kMN) {
           // slots past the sequence end may hold anything; 0 * NaN is NaN.
           // S of this tile is done, so its K rows may be overwritten too.
           mbar_wait(&bar[kKVFull0 + t % kMlaStages], (t / kMlaStages) & 1, dead, a.status);
-          const int first = kv_hi - base;
+          const int first = kv_hi - tile0;
           uint8_t *vb = sKV + (t % kMlaStages) * STAGE_BYTES;
           const int per_chunk = (kMN - first) * 8;
-          for (int e = r; e < 4 * per_chunk; e += 128) {
+          for (int e = tid; e < 4 * per_chunk; e += kSoftThreads) {
             const int ci = e / per_chunk, rem = e % per_chunk;
             *reinterpret_cast<uint4 *>(vb + ci * kChunkKV + (first + rem / 8) * 128 + (rem % 8) * 16) =
                 make_uint4(0, 0, 0, 0);
@@ -527,7 +559,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         if (lane == 0) mbar_arrive(&bar[kPFull]);
         if (j + 1 < nt) {
 #pragma unroll
-          for (int x = 0; x < kMN; ++x) cur[x] = nxt[x];
+          for (int x = 0; x < kHalfN; ++x) cur[x] = nxt[x];
         }
       }
       // the next piece's queries, once the last score product of this one is done
@@ -536,7 +568,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         tc_fence_after();
         load_q(next_piece.s);
       }
-      // ---- epilogue
+      // ---- epilogue: the row sum is the two halves' shares
+      {
+        float *red = s_red;
+        named_sync(1, kSoftThreads);
+        red[tid] = l;
+        named_sync(1, kSoftThreads);
+        l = red[tid] + red[partner];
+        named_sync(1, kSoftThreads);
+      }
       const uint32_t glast = g + nt - 1;
       mbar_wait(&bar[kODone], glast & 1, dead, a.status);
       tc_fence_after();
@@ -545,13 +585,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       const float inv = l > 0.f ? 1.f / l : 0.f;
       const uint32_t keep = item_bad ? 0u : 0xffffffffu;
       const long long prow = ((long long)s * kMlaH + r) * a.max_splits + split;
-      for (int c0 = 0; c0 < kVHalf; c0 += 32) {
+      for (int c0 = 0; c0 < kVHalf / 2; c0 += 32) {
         uint32_t o[32];
-        tc_ld32(tmem + lane_off + kTmemO + c0, o);
+        tc_ld32(tmem + lane_off + kTmemO + h * (kVHalf / 2) + c0, o);
         tc_wait_ld();
 #pragma unroll
         for (int x = 0; x < 32; ++x) o[x] &= keep;
-        const int col = (int)rank * kVHalf + c0;
+        const int col = (int)rank * kVHalf + h * (kVHalf / 2) + c0;
         if (direct) {
           uint4 *dst = reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(a.out) +
                                                  ((size_t)s * kMlaH + r) * kMlaL + col);
@@ -576,7 +616,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
                                  __uint_as_float(o[4 * v + 3]) * inv);
         }
       }
-      if (!direct && rank == 0)
+      if (!direct && rank == 0 && h == 0)
         a.part_lse[prow] = item_bad ? __int_as_float(0x7fc00000) : (l > 0.f ? m + log2f(l) : -INFINITY);
       tc_fence_before();
       __syncwarp();
@@ -586,18 +626,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       piece = next_piece;
       have = have_next;
     }
-    if (r == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (tid == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   cluster_sync_all();  // no remote access to this CTA's shared memory remains
   tc_fence_after();
-  if (warp == 5) tc_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc_dealloc(tmem, kTmemCols);
 }
 
-// ---------------------------------------------------------------------------
-// merge of split partials: one block per (sequence, head) row
-// ---------------------------------------------------------------------------
 // One warp per (sequence, head) row: lane q < 32 holds split q's
 // log-sum-exp (more splits loop), every lane 16 of the 512 columns.
 constexpr int kMergeWarps = 8;
@@ -779,12 +816,24 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
   a.part_lse = reinterpret_cast<float *>(w + lay.part_lse);
   a.status = status;
 
-  CUtensorMap tm_kv;
+  // page_tiles: every 64-position tile is 64 slots of one page (automatic
+  // splits are whole tiles; a fixed split must be a multiple of 64 too)
+  a.page_tiles = (block_size % 64 == 0 && kv_split_tokens % 64 == 0) ? 1 : 0;
+  const unsigned box_slots = a.page_tiles ? kMN : kMHalf;
+  CUtensorMap tm_kv, tm_kv4;
   const unsigned long long kd[3] = {kMlaW, (unsigned long long)block_size,
                                     (unsigned long long)num_blocks};
   const unsigned long long ks[2] = {kMlaW * 2, (unsigned long long)block_size * kMlaW * 2};
-  const unsigned int kb[3] = {64, kMHalf, 1};
-  if (!encode_tiled(&tm_kv, kv_cache, PA_BF16, 3, kd, ks, kb, true)) return PA_ERR_CUDA;
+  const unsigned int kb[3] = {64, box_slots, 1};
+  // the same rows as {64 columns, slots, 9 chunks of 64 columns, pages}: one
+  // box of 4 chunks x 64 slots lands as [chunk][slot][128 B]
+  const unsigned long long k4d[4] = {64, (unsigned long long)block_size, kMlaW / 64,
+                                     (unsigned long long)num_blocks};
+  const unsigned long long k4s[3] = {kMlaW * 2, 128, (unsigned long long)block_size * kMlaW * 2};
+  const unsigned int k4b[4] = {64, kMN, 4, 1};
+  if (!encode_tiled(&tm_kv, kv_cache, PA_BF16, 3, kd, ks, kb, true) ||
+      !encode_tiled(&tm_kv4, kv_cache, PA_BF16, 4, k4d, k4s, k4b, true))
+    return PA_ERR_CUDA;
 
   int slot = prof_begin(PA_K_PLAN, st);
   cudaError_t err = launch_dependent(mla_plan_kernel, dim3(1), dim3(1024), 0, st, a);
@@ -792,7 +841,7 @@ pa_status pa_mla_decode(const void *q, const void *kv_cache, const int32_t *bloc
   if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA, st);
   err = launch_dependent(mla_kernel, dim3(2 * a.num_clusters), dim3(kMlaThreads), MLA_SMEM, st,
-                         tm_kv, a);
+                         tm_kv, tm_kv4, a);
   prof_end(slot, st);
   if (err != cudaSuccess) return PA_ERR_CUDA;
   slot = prof_begin(PA_K_MLA_MERGE, st);
