@@ -236,7 +236,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
     prefetch_tensor_map(&tm_kv);
     prefetch_tensor_map(&tm_kv4);
     for (int b = 0; b < kNumMBars; ++b) {
-      const bool per_warp = b == kQFull || b == kSFree || b == kPFull || b == kOFree;
+      const bool per_warp =
+          b == kQFull || b == kSFree || b == kPFull || b == kOFree || b == kXFree;
       mbar_init(&bar[b], per_warp ? (uint32_t)kSoftWarps : 1u);
     }
     fence_mbar_init();
@@ -405,13 +406,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kQFull]);
     };
+    // Exchange buffers (the peer's, and this CTA's staging copy) hold one
+    // tile as [half][head][8 float4]: each warp's 32 rows x 128 B are one
+    // contiguous 4 KB block, which the warp copies to the peer by itself.
+    // Slot x of row r is stored at x ^ (r % 8), so the rows a quarter-warp
+    // touches fall in different banks.
+    const uint32_t xrow = (uint32_t)(h * 128 + r) * 128;
+    const uint32_t xwarp = (uint32_t)(h * 128 + (warp & 3) * 32) * 128;
     // Read this thread's 32 scores of tile t out of TMEM, free the buffer,
-    // stage them and push the tile into the peer's exchange buffer with one
-    // bulk copy (completion counted on the peer's mbarrier).  Row r: 16
-    // float4 slots, slot v stored at v ^ (r % 8), so the rows a quarter-warp
-    // touches fall in different banks.  Both buffers hold one tile: the
-    // staging buffer is reused once the previous copy has read it, the
-    // peer's buffer once the peer has consumed tile t - 1.
+    // stage them and push the warp's block into the peer's exchange buffer
+    // with one bulk copy (completion counted on the peer's mbarrier).  The
+    // staging block is reused once the warp's previous copy has read it, the
+    // peer's buffer once every peer warp has consumed tile t - 1.
     auto fetch_send = [&](uint32_t t, float (&v)[kHalfN]) {
       mbar_wait(&bar[kSFull], t & 1, dead, a.status);
       tc_fence_after();
@@ -423,17 +429,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       if (lane == 0) mbar_arrive(&bar[kSFree]);
 #pragma unroll
       for (int x = 0; x < kHalfN; ++x) v[x] = __uint_as_float(raw[x]);
-      if (tid == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      named_sync(1, kSoftThreads);
-      float4 *st4 = reinterpret_cast<float4 *>(sXS + r * kMN * 4);
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      __syncwarp();
+      float4 *st4 = reinterpret_cast<float4 *>(sXS + xrow);
 #pragma unroll
       for (int x = 0; x < kHalfN / 4; ++x)
-        st4[(8 * h + x) ^ (r & 7)] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+        st4[x ^ (r & 7)] = make_float4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
       fence_proxy_async();
-      named_sync(1, kSoftThreads);
-      if (tid == 0) {
+      __syncwarp();
+      if (lane == 0) {
         if (t >= 1) mbar_wait_cluster(&bar[kXFree], (t - 1) & 1, dead, a.status);
-        bulk_copy_to_peer(x_peer, sXS, X_BYTES, xfull_peer);
+        bulk_copy_to_peer(x_peer + xwarp, sXS + xwarp, 32 * 128, xfull_peer);
         asm volatile("cp.async.bulk.commit_group;" ::: "memory");
       }
     };
@@ -479,11 +485,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         // the peer's partial scores of tile t
         if (tid == 0) mbar_arrive_expect_tx(&bar[kXFull], X_BYTES);
         mbar_wait_cluster(&bar[kXFull], t & 1, dead, a.status);
-        const float4 *xr = reinterpret_cast<const float4 *>(sX + r * kMN * 4);
+        const float4 *xr = reinterpret_cast<const float4 *>(sX + xrow);
         float mxa[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int x = 0; x < kHalfN / 4; ++x) {
-          const float4 o4 = xr[(8 * h + x) ^ (r & 7)];
+          const float4 o4 = xr[x ^ (r & 7)];
           const float e[4] = {o4.x, o4.y, o4.z, o4.w};
 #pragma unroll
           for (int y = 0; y < 4; ++y) {
@@ -492,14 +498,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
             mxa[y] = fmaxf(mxa[y], cur[c]);
           }
         }
-        // (the named barriers of the previous tile's exchange separate this
-        // write from the partner's read of the previous maximum)
-        float *red = s_red;
-        red[tid] = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
-        // every read of the exchange buffer is done, both halves' maxima are posted
-        named_sync(1, kSoftThreads);
-        if (tid == 0) mbar_arrive_remote_relaxed(xfree_peer);
-        const float mx = fmaxf(red[tid], red[partner]);
+        // this warp is done with the peer's buffer
+        __syncwarp();
+        if (lane == 0) mbar_arrive_remote_relaxed(xfree_peer);
+        // the two halves of a row meet through shared memory (the first pair
+        // barrier keeps this write clear of the partner's previous read)
+        named_sync(2 + (warp & 3), 64);
+        s_red[tid] = fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3]));
+        named_sync(2 + (warp & 3), 64);
+        const float mx = fmaxf(s_red[tid], s_red[partner]);
         // then this CTA's partial scores of the next tile go to the peer
         if (j + 1 < nt) fetch_send(t + 1, nxt);
         // P and O were last touched by the value product of tile t - 1
@@ -569,14 +576,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
         load_q(next_piece.s);
       }
       // ---- epilogue: the row sum is the two halves' shares
-      {
-        float *red = s_red;
-        named_sync(1, kSoftThreads);
-        red[tid] = l;
-        named_sync(1, kSoftThreads);
-        l = red[tid] + red[partner];
-        named_sync(1, kSoftThreads);
-      }
+      named_sync(2 + (warp & 3), 64);
+      s_red[tid] = l;
+      named_sync(2 + (warp & 3), 64);
+      l = s_red[tid] + s_red[partner];
       const uint32_t glast = g + nt - 1;
       mbar_wait(&bar[kODone], glast & 1, dead, a.status);
       tc_fence_after();
