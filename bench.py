@@ -464,14 +464,17 @@ def secondary_workloads(pa, flush, peaks):
         ms = time_per_step(lambda: pa.mla_decode(m, out=out), 10, flush)
         gbs = mla_bytes(hm) / ms / 1e6
         tf = mla_flops(hm) / ms / 1e9
+        # the roofline floor is the larger of the HBM time and the tensor time
+        floor_ms = max(mla_bytes(hm) / hbm / 1e6, mla_flops(hm) / tfl / 1e9)
         res["mla_decode"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm, "tflops": tf,
-                             "tensor_frac": tf / tfl}
+                             "tensor_frac": tf / tfl, "roofline_floor_ms": floor_ms,
+                             "roofline_frac": floor_ms / ms}
     else:
         res["mla_decode"] = {"unavailable": pa.status_string(st)}
     del m, out
 
-    # non-absorbed MLA prefill / extend: decompression (two GEMMs over every
-    # cached position) plus causal attention with 192-wide keys
+    # non-absorbed MLA prefill / extend: decompression (the up-projection
+    # GEMM over every cached position) plus causal attention with 192-wide keys
     hp = inputs.mla_prefill_deepseek(poison=False)
     mp = pa.to_device(hp)
     outp = torch.empty((hp.num_tokens, hp.num_heads, hp.v_head_dim), dtype=torch.bfloat16,
@@ -498,6 +501,10 @@ def secondary_workloads(pa, flush, peaks):
                               "kernel_ms": kms}
         if "tile" in kms:
             res["mla_prefill"]["tile_tflops"] = att / kms["tile"] / 1e9
+        if "upproj" in kms:
+            up_tf = up / kms["upproj"] / 1e9
+            res["mla_prefill"]["upproj_tflops"] = up_tf
+            res["mla_prefill"]["upproj_tensor_frac"] = up_tf / tfl
     else:
         res["mla_prefill"] = {"unavailable": pa.status_string(st)}
     del mp, outp

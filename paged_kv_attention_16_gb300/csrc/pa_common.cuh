@@ -641,18 +641,6 @@ __device__ inline void mbar_wait_cluster(uint64_t *bar, uint32_t parity, bool &d
   }
 }
 
-// Asynchronous 16-byte store into another CTA's shared memory (a cluster
-// address); its bytes complete as transaction bytes on that CTA's mbarrier
-// `mbar_cluster`, which the receiver waits on (no release fence needed).
-__device__ inline void st_async_v4(uint32_t cluster_addr, float a, float b, float c, float d,
-                                   uint32_t mbar_cluster) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::
-          "r"(cluster_addr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar_cluster)
-      : "memory");
-}
-
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to
 // another CTA of the cluster; completion is counted as transaction bytes on
 // the destination CTA's mbarrier.
