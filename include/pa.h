@@ -158,6 +158,22 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
  *          -m_h * sqrt(p - j) when alibi_sqrt is 1.  Caller-owned, 4-byte
  *          aligned, valid until the call's kernels have run.
  *   alibi_sqrt  0 or 1 (else PA_ERR_INVALID_ARG); ignored without slopes.
+ *   max_query_len  0 = unknown; otherwise the caller's host-known bound on
+ *          every request's new tokens (a serving scheduler knows it when it
+ *          builds the batch).  1 declares a decode-only batch: with bf16
+ *          inputs, head_dim 64 or 128, at most 16 query heads per KV head,
+ *          num_tokens == num_seqs and at most as many (request, KV head)
+ *          pairs as the row kernel has resident blocks (small batches, where
+ *          launches dominate), the call then runs as ONE kernel launch --
+ *          the row kernel sizes its own KV splits from max_seq_len and merges
+ *          a row's splits in the thread block that finishes last -- instead
+ *          of planner, row, tile and merge launches.  The contract is then
+ *          query_start_loc[s] == s for every s: a request that breaks it
+ *          (or whose seq_len is out of range) sets PA_DEV_BAD_QSL (or
+ *          PA_DEV_BAD_SEQLEN) and its row s is written as zeros.  The split
+ *          counters it uses live in a small library-owned buffer that is
+ *          grown outside capture (PA_ERR_WORKSPACE during capture).  Other
+ *          values only have to be >= 0 (else PA_ERR_INVALID_ARG).
  * Errors as for pa_forward.
  */
 typedef struct {
@@ -166,6 +182,7 @@ typedef struct {
   int sliding_window;
   const float *alibi_slopes;
   int alibi_sqrt;
+  int max_query_len;
 } pa_forward_options;
 
 pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,

@@ -531,6 +531,10 @@ struct DeviceState {
   unsigned int *status = nullptr;
   void *ws = nullptr;
   size_t ws_bytes = 0;
+  // decode-only batches: [0] item counter, [1] blocks done taking items,
+  // then one split count per (request, kv head); all zero between calls
+  unsigned long long *fast_ctr = nullptr;
+  size_t fast_groups = 0;
 };
 
 std::mutex g_mu;
@@ -605,6 +609,29 @@ pa_status ensure_workspace(DeviceState *d, size_t bytes, cudaStream_t stream) {
     want = bytes;
   }
   d->ws_bytes = want;
+  return PA_OK;
+}
+
+// The decode-only path's counters for `groups` row groups, zeroed when
+// (re)allocated; they return to zero at the end of every call.
+pa_status ensure_fast_counters(DeviceState *d, size_t groups, cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (d->fast_ctr && d->fast_groups >= groups) return PA_OK;
+  if (stream_capturing(stream)) return PA_ERR_WORKSPACE;
+  if (d->fast_ctr) {
+    cudaFree(d->fast_ctr);  // synchronises the device: no call still uses it
+    d->fast_ctr = nullptr;
+    d->fast_groups = 0;
+  }
+  const size_t want = groups + groups / 4 + 64;
+  const size_t bytes = 2 * sizeof(unsigned long long) + want * sizeof(unsigned int);
+  if (cudaMalloc(&d->fast_ctr, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    d->fast_ctr = nullptr;
+    return PA_ERR_CUDA;
+  }
+  if (cudaMemset(d->fast_ctr, 0, bytes) != cudaSuccess) return PA_ERR_CUDA;
+  d->fast_groups = want;
   return PA_OK;
 }
 
@@ -738,6 +765,117 @@ bool tile_path_ok(int dtype, int head_dim, int group) {
   return tile_kernel_supported(dtype, head_dim, group);
 }
 
+// Decode-only batches (the caller declares max_query_len == 1): the split
+// length and the bound on splits per row come from host-known extents, so no
+// planner runs.  Contexts are taken to average about half their bound.
+struct FastPlan {
+  int split = 0, nsmax = 0;
+  long long part_rows = 0;
+  size_t part_o = 0, part_lse = 0, ws_bytes = 0;
+};
+
+bool fast_decode_plan(const FwdCall &c, int num_sms, FastPlan *f) {
+  if (c.max_query_len != 1 || c.dtype != PA_BF16 || c.all_tile || c.num_seqs <= 0 ||
+      c.num_tokens != c.num_seqs)
+    return false;
+  const int group = c.num_heads / c.num_kv_heads;
+  if (!row_mma_supported(c.dtype, c.head_dim, group)) return false;
+  const long long msl = c.max_seq_len > 0 ? c.max_seq_len : 1;
+  const long long row_ctas =
+      (long long)row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * (num_sms > 0 ? num_sms : 1);
+  // Only batches with at most one row group per resident block: there the
+  // planner, tile and merge launches are most of the call.  On larger
+  // batches the separate merge pass is cheaper than merging in the row
+  // kernel (every split would pay a fence and an atomic before its block
+  // moves on), so they keep the planned path.
+  if ((long long)c.num_seqs * c.num_kv_heads > row_ctas) return false;
+  const long long target = (group >= 8 ? 4ll : 8ll) * row_ctas;
+  long long L = ceil_div_h(ceil_div_h((long long)c.num_seqs * c.num_kv_heads * msl, 2 * target), 64) * 64;
+  if (L < kRowMinSplit) L = kRowMinSplit;
+  const long long lmin = ceil_div_h(ceil_div_h(msl, 64), 64) * 64;  // at most 64 splits a row
+  if (L < lmin) L = lmin;
+  // rows of at most 1024 positions are not split: a merge costs more than it saves
+  if (msl <= 1024) L = ceil_div_h(msl, 64) * 64;
+  if (c.kv_split_tokens > 0 && c.kv_split_tokens < L) L = c.kv_split_tokens;
+  const long long nsmax = ceil_div_h(msl, L);
+  if (L > kRowMaxSplit || nsmax > 64) return false;
+  f->split = (int)L;
+  f->nsmax = (int)nsmax;
+  f->part_rows = (long long)c.num_seqs * c.num_heads * nsmax;
+  f->part_o = 0;
+  f->part_lse = align256((size_t)f->part_rows * c.head_dim * sizeof(float));
+  f->ws_bytes = f->part_lse + align256((size_t)f->part_rows * sizeof(float));
+  return true;
+}
+
+// The row kernel's K / V tensor maps: bf16 boxes of 16 slots x both 64-dim
+// halves of one KV head, dims {64 dims, slots, halves, kv heads, pages} (the
+// slot stride is larger than the half stride; TMA takes strides in any
+// order).  In the HND layout a box is one contiguous run of 16 x head_dim.
+bool encode_row_maps(const FwdCall &c, CUtensorMap *tm_k, CUtensorMap *tm_v) {
+  const unsigned long long es = 2, row = (unsigned long long)c.head_dim * es;
+  const bool hnd = c.kv_layout == PA_KV_HND;
+  const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
+                                      (unsigned long long)(c.head_dim / 64),
+                                      (unsigned long long)c.num_kv_heads,
+                                      (unsigned long long)c.num_blocks};
+  const unsigned long long strides[4] = {
+      hnd ? row : (unsigned long long)c.num_kv_heads * row, 64 * es,
+      hnd ? (unsigned long long)c.block_size * row : row,
+      (unsigned long long)c.block_size * c.num_kv_heads * row};
+  const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
+  return (!tm_k || encode_tiled(tm_k, c.k_cache, c.dtype, 5, dims, strides, box, true)) &&
+         encode_tiled(tm_v, c.v_cache, c.dtype, 5, dims, strides, box, true);
+}
+
+pa_status fast_decode_launch(const FwdCall &c, const FastPlan &f, void *workspace,
+                             unsigned int *status, unsigned long long *fast_ctr, int num_sms,
+                             cudaStream_t st) {
+  const int group = c.num_heads / c.num_kv_heads;
+  uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
+  FwdParams p{};
+  p.q = c.q;
+  p.out = c.out;
+  p.block_table = c.block_table;
+  p.seq_lens = c.seq_lens;
+  p.qsl = c.qsl;
+  p.num_seqs = c.num_seqs;
+  p.num_tokens = c.num_tokens;
+  p.num_heads = c.num_heads;
+  p.num_kv_heads = c.num_kv_heads;
+  p.head_dim = c.head_dim;
+  p.block_size = c.block_size;
+  p.max_blocks_per_seq = c.max_blocks_per_seq;
+  p.num_blocks = c.num_blocks;
+  p.max_seq_len = c.max_seq_len;
+  p.kv_split_tokens = c.kv_split_tokens;
+  p.scale = c.scale;
+  p.scale_log2 = c.scale * kLog2e;
+  p.dtype = c.dtype;
+  p.part_o = reinterpret_cast<float *>(ws + f.part_o);
+  p.part_lse = reinterpret_cast<float *>(ws + f.part_lse);
+  p.part_cap = f.part_rows;
+  p.status = status;
+  p.sinks = c.sinks;
+  p.window = c.sliding_window;
+  p.alibi = c.alibi_slopes;
+  p.alibi_sqrt = c.alibi_sqrt;
+  p.head_dim_qk = c.head_dim;
+  p.fast = 1;
+  p.fast_split = f.split;
+  p.fast_nsmax = f.nsmax;
+  p.fast_work = fast_ctr;
+  p.fast_cnt = reinterpret_cast<unsigned int *>(fast_ctr + 2);
+  CUtensorMap tm_k, tm_v;
+  if (!encode_row_maps(c, &tm_k, &tm_v)) return PA_ERR_CUDA;
+  const int row_ctas = row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * num_sms;
+  p.row_ctas = row_ctas;
+  const int slot = prof_begin(PA_K_ROW, st);
+  const cudaError_t err = launch_row_mma_kernel(p, tm_k, tm_v, row_ctas, st);
+  prof_end(slot, st);
+  return err == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // namespace
 
 pa_status fwd_check(const FwdCall &c) {
@@ -834,23 +972,9 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     // kernel reads K and V through them, the tile kernel V.  In the HND
     // layout a box is one contiguous run of 16 x head_dim elements.
     CUtensorMap tm_kr, tm_vr;
-    if (c.dtype == PA_BF16) {
-      const unsigned long long es = 2, row = (unsigned long long)c.head_dim * es;
-      const bool hnd = c.kv_layout == PA_KV_HND;
-      const unsigned long long dims[5] = {64, (unsigned long long)c.block_size,
-                                          (unsigned long long)(c.head_dim / 64),
-                                          (unsigned long long)c.num_kv_heads,
-                                          (unsigned long long)c.num_blocks};
-      const unsigned long long strides[4] = {
-          hnd ? row : (unsigned long long)c.num_kv_heads * row, 64 * es,
-          hnd ? (unsigned long long)c.block_size * row : row,
-          (unsigned long long)c.block_size * c.num_kv_heads * row};
-      const unsigned int box[5] = {64, 16, (unsigned int)(c.head_dim / 64), 1, 1};
-      // (all-tile calls have no row items: their K rows may be wider than V's)
-      if ((!c.all_tile && !encode_tiled(&tm_kr, c.k_cache, c.dtype, 5, dims, strides, box, true)) ||
-          !encode_tiled(&tm_vr, c.v_cache, c.dtype, 5, dims, strides, box, true))
-        return PA_ERR_CUDA;
-    }
+    // (all-tile calls have no row items: their K rows may be wider than V's)
+    if (c.dtype == PA_BF16 && !encode_row_maps(c, c.all_tile ? nullptr : &tm_kr, &tm_vr))
+      return PA_ERR_CUDA;
     // The tile kernel's K: one 64-element (128-byte) swizzled box per half
     // and 16 slots, so the S product sees a uniform row stride.
     // When every 64-position tile lies in one page (block_size a multiple of
@@ -1065,6 +1189,8 @@ pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
     c.sliding_window = options->sliding_window;
     c.alibi_slopes = options->alibi_slopes;
     c.alibi_sqrt = options->alibi_sqrt;
+    if (options->max_query_len < 0) return PA_ERR_INVALID_ARG;
+    c.max_query_len = options->max_query_len;
   }
   pa_status s = fwd_check(c);
   if (s != PA_OK || num_tokens == 0) return s;
@@ -1072,6 +1198,14 @@ pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
   DeviceState *d = nullptr;
   s = device_state(st, &d);
   if (s != PA_OK) return s;
+  FastPlan fp;
+  if (fast_decode_plan(c, d->num_sms, &fp)) {
+    s = ensure_workspace(d, fp.ws_bytes, st);
+    if (s != PA_OK) return s;
+    s = ensure_fast_counters(d, (size_t)c.num_seqs * c.num_kv_heads, st);
+    if (s != PA_OK) return s;
+    return fast_decode_launch(c, fp, d->ws, d->status, d->fast_ctr, d->num_sms, st);
+  }
   s = ensure_workspace(d, fwd_workspace_bytes(c), st);
   if (s != PA_OK) return s;
   return fwd_launch(c, d->ws, d->status, d->num_sms, st, true);

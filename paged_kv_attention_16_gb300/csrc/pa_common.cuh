@@ -97,6 +97,15 @@ struct FwdParams {
   int alibi_sqrt;           // 1: the bias grows with the square root of the distance
   int k_rope_split;         // 1: the last 64 key columns come from a separate
                             // [pages, slots, 1, 64] tensor shared by all heads
+  // Decode-only batches declared by the caller (one launch, no planner): the
+  // row kernel walks num_seqs x kv_heads x fast_nsmax item slots, splits of
+  // fast_split positions; partial rows (s * H + head) * fast_nsmax + split;
+  // fast_work: [0] item counter, [1] CTAs done taking items; fast_cnt:
+  // [num_seqs * kv_heads] splits finished per row group (zero between calls).
+  int fast;
+  int fast_split, fast_nsmax;
+  unsigned long long *fast_work;
+  unsigned int *fast_cnt;
 };
 
 // First KV position the query at position `pos` sees: with a sliding window

@@ -90,6 +90,7 @@ struct FwdCall {
   // columns of every (position, head) key row, k_rope the last 64 columns,
   // shared by all heads: [num_blocks, block_size, 64].  Null: keys whole.
   const void *k_rope = nullptr;
+  int max_query_len = 0;  // caller's bound on new tokens per request (0: unknown)
 };
 // Host-side argument checks of pa_forward (PA_OK also when num_tokens == 0).
 pa_status fwd_check(const FwdCall &c);

@@ -82,6 +82,7 @@ struct MmaRowDesc {
   int mask_lo;      // first visible position (kv_lo is rounded down to a box)
   int qpos;         // the query's position
   long long prow0;  // partial row of head 0 of the group (split partials)
+  int nmerge;       // decode-only batches: the row group's splits (merged in-kernel)
 };
 static_assert(sizeof(MmaRowDesc) <= 64, "descriptor slot is 64 bytes");
 
@@ -144,6 +145,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int S = p.num_seqs, H = p.num_heads, bs = p.block_size;
+  __shared__ int s_last;  // this block finished a row group's last split
 
   if (tid == 0) {
     prefetch_tensor_map(&tm_k);
@@ -165,17 +167,57 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
 
   if (warp == C::NWARP) {
     // ===================================================== producer warp
-    const long long n_items = p.plan->n[kListRow];
+    const int Hk = p.num_kv_heads;
+    const long long n_items =
+        p.fast ? (long long)S * Hk * p.fast_nsmax : p.plan->n[kListRow];
     const long long *row_end = p.list_end + (size_t)kListRow * S;
+    unsigned long long *counter = p.fast ? p.fast_work : &p.plan->counter[kListRow];
     uint32_t g = 0, seq = 0;  // stages issued, descriptors written
     for (;;) {
       long long item = 0;
-      if (lane == 0) item = (long long)atomicAdd(&p.plan->counter[kListRow], 1ull);
+      if (lane == 0) item = (long long)atomicAdd(counter, 1ull);
       item = __shfl_sync(0xffffffffu, item, 0);
       MmaRowDesc d{};
-      int npages = 0, pfirst = 0, s = 0;
+      int npages = 0, pfirst = 0, s = 0, inval = 0;
       if (item >= n_items) {
         d.done = 1;
+      } else if (p.fast) {
+        // decode-only batch, no planner: item = (request, kv head, split),
+        // a row group's splits consecutive, so that they finish close
+        // together and their merges spread over the whole launch
+        const int grp = (int)(item / p.fast_nsmax);
+        d.split = (int)(item % p.fast_nsmax);
+        s = grp / Hk;
+        d.kvh = grp % Hk;
+        d.tok = s;
+        d.i = 0;
+        const int ctx = __ldg(p.seq_lens + s);
+        const bool qok = __ldg(p.qsl + s) == s && __ldg(p.qsl + s + 1) == s + 1;
+        const bool cok = ctx >= 1 && ctx <= p.max_seq_len &&
+                         ceil_div_ll(ctx, bs) <= (long long)p.max_blocks_per_seq;
+        if (!qok || !cok) {
+          if (d.split != 0) continue;  // split 0 zeroes the request's row
+          if (lane == 0) atomicOr(p.status, qok ? PA_DEV_BAD_SEQLEN : PA_DEV_BAD_QSL);
+          inval = 1;
+          d.direct = 1;
+        } else {
+          d.qpos = ctx - 1;
+          d.mask_lo = window_lo(d.qpos, p.window);
+          const int kv_base = d.mask_lo & ~15;
+          const int L = p.fast_split;
+          const int nsplit = (int)ceil_div_ll(ctx - kv_base, L);
+          if (d.split >= nsplit) continue;
+          const int s_lo = kv_base + d.split * L;
+          d.kv_hi = min(d.qpos + 1, s_lo + L);
+          if (max(s_lo, d.mask_lo) >= d.kv_hi) continue;
+          d.kv_lo = max(s_lo, d.mask_lo & ~15);
+          d.direct = nsplit == 1;
+          d.nsplit = p.fast_nsmax;  // the stride between a head's partial rows
+          d.nmerge = nsplit;
+          d.prow0 = ((long long)s * H + d.kvh * G) * p.fast_nsmax + d.split;
+          pfirst = d.kv_lo / bs;
+          npages = (d.kv_hi - 1) / bs - pfirst + 1;
+        }
       } else {
         const int k = list_find(row_end, S, item);
         const long long start = k ? row_end[k - 1] : 0;
@@ -212,6 +254,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       }
       d.bad = __any_sync(0xffffffffu, bad);
       if (d.bad && lane == 0) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+      d.bad |= inval;
       __syncwarp();
       const int slot = seq & 1;
       if (lane == 0) {
@@ -220,7 +263,18 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
         mbar_arrive(&item_full[slot]);
       }
       ++seq;
-      if (d.done) break;
+      if (d.done) {
+        if (p.fast && lane == 0) {
+          // the last block to stop taking items resets the counters
+          __threadfence();
+          if (atomicAdd(p.fast_work + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+            __threadfence();
+            atomicExch(p.fast_work, 0ull);
+            atomicExch(p.fast_work + 1, 0ull);
+          }
+        }
+        break;
+      }
       if (d.bad) continue;
       // stream the split: per stage, lane -> (box, K|V)
       const int nst = (d.kv_hi - d.kv_lo + C::ST - 1) / C::ST;
@@ -281,6 +335,65 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       qa[ks][3] = gq + 8 < G ? __ldg(qrow + (gq + 8) * (D / 2) + c + 4) : 0u;
     }
   };
+  // Decode-only batches: after a split's partial rows are written, the block
+  // that finishes a row group's last split merges its splits (log-sum-exp,
+  // the sink joining the denominator) into the output and clears the count.
+  auto fast_finish = [&](const MmaRowDesc &x) {
+    __threadfence();
+    named_sync(1, 128);
+    const size_t grp = (size_t)x.tok * p.num_kv_heads + x.kvh;
+    if (tid == 0) s_last = atomicAdd(p.fast_cnt + grp, 1u) == (unsigned)x.nmerge - 1 ? 1 : 0;
+    named_sync(1, 128);
+    if (!s_last) return;
+    __threadfence();
+    float *s_wt = s_o;             // [G][64] merge weights of the splits
+    float *s_iv = s_o + G * 64;    // [G] reciprocal denominators (0: the row is zero)
+    const long long row0 = ((long long)x.tok * H + x.kvh * G) * p.fast_nsmax;
+    // one warp per head: lane q holds split q's log-sum-exp (two when a row
+    // has more than 32 splits)
+    for (int hh = warp; hh < G; hh += C::NWARP) {
+      const long long r = row0 + (long long)hh * p.fast_nsmax;
+      const float v0 = lane < x.nmerge ? __ldcg(p.part_lse + r + lane) : -INFINITY;
+      const float v1 = lane + 32 < x.nmerge ? __ldcg(p.part_lse + r + lane + 32) : -INFINITY;
+      int badp = (isnan(v0) || isnan(v1)) ? 1 : 0;
+      float M = fmaxf(isnan(v0) ? -INFINITY : v0, isnan(v1) ? -INFINITY : v1);
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        badp |= __shfl_xor_sync(0xffffffffu, badp, o);
+      }
+      const float sink2 = p.sinks ? __ldg(p.sinks + x.kvh * G + hh) * kLog2eF : -INFINITY;
+      M = fmaxf(M, sink2);
+      const bool any = !badp && M != -INFINITY;
+      const float w0 = (any && v0 != -INFINITY) ? fast_exp2(v0 - M) : 0.f;
+      const float w1 = (any && v1 != -INFINITY) ? fast_exp2(v1 - M) : 0.f;
+      if (lane < x.nmerge) s_wt[hh * 64 + lane] = w0;
+      if (lane + 32 < x.nmerge) s_wt[hh * 64 + lane + 32] = w1;
+      float L = w0 + w1;
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+      if (any && p.sinks) L += fast_exp2(sink2 - M);
+      if (lane == 0) s_iv[hh] = (!any || !(L > 0.f)) ? 0.f : 1.f / L;
+    }
+    named_sync(1, 128);
+    // the partial rows, eight splits at a time (independent loads)
+    __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)x.tok * H + x.kvh * G) * D;
+    for (int e = tid; e < G * D; e += 128) {
+      const int h = e / D, dd = e % D;
+      const float *src = p.part_o + (row0 + (long long)h * p.fast_nsmax) * D + dd;
+      float acc = 0.f;
+      for (int q0 = 0; q0 < x.nmerge; q0 += 8) {
+        float pv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pv[u] = q0 + u < x.nmerge ? __ldcg(src + (size_t)(q0 + u) * D) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (q0 + u < x.nmerge) acc = fmaf(s_wt[h * 64 + q0 + u], pv[u], acc);
+      }
+      dst[e] = __float2bfloat16_rn(acc * s_iv[h]);
+    }
+    if (tid == 0) p.fast_cnt[grp] = 0u;
+  };
   MmaRowDesc nd = take(seq);
   if (!nd.done && !nd.bad) load_q(nd);
   for (;;) {
@@ -299,6 +412,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
           if (dd == 0) p.part_lse[prow] = __int_as_float(0x7fc00000);  // NaN: bad split
         }
       }
+      if (p.fast && !d.direct) fast_finish(d);
       nd = take(++seq);
       if (!nd.done && !nd.bad) load_q(nd);
       continue;
@@ -491,6 +605,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
         if (d0 == 0) p.part_lse[prow] = L > 0.f ? M + log2f(L) : -INFINITY;
       }
     }
+    if (p.fast && !d.direct) fast_finish(d);
   }
 }
 

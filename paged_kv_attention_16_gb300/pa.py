@@ -39,7 +39,7 @@ class ForwardOptions(ctypes.Structure):
     logits, or None."""
     _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int),
                 ("sliding_window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
-                ("alibi_sqrt", ctypes.c_int)]
+                ("alibi_sqrt", ctypes.c_int), ("max_query_len", ctypes.c_int)]
 
 
 def layout_code(kv_layout):
@@ -151,7 +151,8 @@ def _check(status, where):
 def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_heads,
                num_kv_heads, head_dim, block_size, scale, out, stream=None, *, max_seq_len,
                kv_split_tokens=0, num_blocks=None, sinks=None, kv_layout="nhd",
-               sliding_window=0, alibi_slopes=None, alibi_sqrt=False, check=True):
+               sliding_window=0, alibi_slopes=None, alibi_sqrt=False, max_query_len=0,
+               check=True):
     """Unified paged attention (see include/pa.h).  Shapes are read from the
     tensors; max_seq_len is the host-known bound on seq_lens.  The options --
     sinks and alibi_slopes (fp32 device tensors of num_heads values), an HND
@@ -165,7 +166,7 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
         int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
         int(kv_split_tokens))
     if (sinks is None and layout == PA_KV_NHD and not sliding_window
-            and alibi_slopes is None):
+            and alibi_slopes is None and not max_query_len):
         st, where = lib().pa_forward(*args), "pa_forward"
     else:
         for name, t in (("sinks", sinks), ("alibi_slopes", alibi_slopes)):
@@ -173,7 +174,7 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
                                                 or t.numel() != num_heads):
                 raise TypeError(f"{name} must be a float32 tensor of num_heads elements")
         opts = ForwardOptions(_ptr(sinks), layout, int(sliding_window), _ptr(alibi_slopes),
-                              int(bool(alibi_sqrt)))
+                              int(bool(alibi_sqrt)), int(max_query_len))
         st, where = lib().pa_forward_ex(*args, ctypes.byref(opts)), "pa_forward_ex"
     if check:
         _check(st, where)
@@ -314,7 +315,7 @@ def to_device(batch, device="cuda"):
 
 
 def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None, sliding_window=0,
-            alibi_slopes=None, alibi_sqrt=False):
+            alibi_slopes=None, alibi_sqrt=False, max_query_len=0):
     """pa_forward on a device-resident PagedBatch (pa_forward_ex when an
     option is set: sinks / alibi_slopes as fp32 device tensors of num_heads
     values, a sliding window, sqrt ALiBi, the batch's HND layout); returns
@@ -326,7 +327,7 @@ def forward(b, out=None, stream=None, kv_split_tokens=None, sinks=None, sliding_
                max_seq_len=b.max_seq_len,
                kv_split_tokens=b.kv_split_tokens if kv_split_tokens is None else kv_split_tokens,
                sinks=sinks, kv_layout=b.kv_layout, sliding_window=sliding_window,
-               alibi_slopes=alibi_slopes, alibi_sqrt=alibi_sqrt)
+               alibi_slopes=alibi_slopes, alibi_sqrt=alibi_sqrt, max_query_len=max_query_len)
     return out
 
 

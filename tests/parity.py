@@ -29,7 +29,7 @@ def oracle_mla(b, rows=None):
 
 
 def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0, sinks=None,
-                sliding_window=0, alibi_slopes=None, alibi_sqrt=False):
+                sliding_window=0, alibi_slopes=None, alibi_sqrt=False, max_query_len=0):
     d = pa.to_device(b)
     if sinks is not None:
         sinks = torch.as_tensor(sinks, dtype=torch.float32).cuda()
@@ -37,7 +37,7 @@ def gpu_forward(b, kv_split_tokens=None, out=None, expect_status=0, sinks=None,
         alibi_slopes = torch.as_tensor(alibi_slopes, dtype=torch.float32).cuda()
     got = pa.forward(d, out=out, kv_split_tokens=kv_split_tokens, sinks=sinks,
                      sliding_window=sliding_window, alibi_slopes=alibi_slopes,
-                     alibi_sqrt=alibi_sqrt)
+                     alibi_sqrt=alibi_sqrt, max_query_len=max_query_len)
     status = pa.pa_get_device_status()
     assert status == expect_status, f"device status {status:#x}, expected {expect_status:#x}"
     return got.float().cpu().numpy().astype(np.float64)

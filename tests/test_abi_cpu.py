@@ -107,7 +107,7 @@ def test_cache_write_host_argument_checks(lib, kw, want):
 class _Options(ctypes.Structure):
     _fields_ = [("sinks", ctypes.c_void_p), ("kv_layout", ctypes.c_int),
                 ("sliding_window", ctypes.c_int), ("alibi_slopes", ctypes.c_void_p),
-                ("alibi_sqrt", ctypes.c_int)]
+                ("alibi_sqrt", ctypes.c_int), ("max_query_len", ctypes.c_int)]
 
 
 def _forward_ex(lib, options, **kw):
@@ -223,12 +223,13 @@ def test_binding_options_struct_matches_the_header(tmp_path):
     src = tmp_path / "layout.c"
     src.write_text('#include <stdio.h>\n#include <stddef.h>\n#include "pa.h"\n'
                    "int main(void) {\n"
-                   '  printf("%zu %zu %zu %zu %zu %zu\\n", sizeof(pa_forward_options),\n'
+                   '  printf("%zu %zu %zu %zu %zu %zu %zu\\n", sizeof(pa_forward_options),\n'
                    "         offsetof(pa_forward_options, sinks),\n"
                    "         offsetof(pa_forward_options, kv_layout),\n"
                    "         offsetof(pa_forward_options, sliding_window),\n"
                    "         offsetof(pa_forward_options, alibi_slopes),\n"
-                   "         offsetof(pa_forward_options, alibi_sqrt));\n"
+                   "         offsetof(pa_forward_options, alibi_sqrt),\n"
+                   "         offsetof(pa_forward_options, max_query_len));\n"
                    "  return 0;\n}\n")
     exe = tmp_path / "layout"
     subprocess.run(["gcc", "-std=c99", "-I", os.path.dirname(HEADER), str(src), "-o", str(exe)],
