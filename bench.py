@@ -354,6 +354,13 @@ def secondary_workloads(pa, flush, peaks):
         res["llama_decode_b1"]["graph_replay"] = {"ms": gms, "kv_gbs": kv_bytes(hb) / gms / 1e6}
     except Exception as e:  # report, never abort the benchmark
         res["llama_decode_b1"]["graph_replay"] = {"error": str(e)[:200]}
+    # the same step declared decode-only (max_query_len = 1): one kernel launch
+    fn1 = lambda: pa.forward(b, out=out, max_query_len=1)  # noqa: E731
+    for _ in range(5):
+        fn1()
+    ms1 = time_per_step(fn1, 50, flush)
+    res["llama_decode_b1"]["one_launch"] = {"ms": ms1, "kv_gbs": kv_bytes(hb) / ms1 / 1e6,
+                                            "note": "pa_forward_ex with max_query_len = 1"}
     del b, out
 
     # the headline decode batch with NHD and with head-major (HND) caches
