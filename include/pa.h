@@ -41,6 +41,9 @@
  *      PA_DEV_OVERFLOW    the plan needs more split partials than the workspace
  *                         holds (only if seq_lens exceed max_seq_len); every row is 0
  *      PA_DEV_TIMEOUT     a bounded wait inside a kernel gave up (never expected)
+ *      PA_DEV_INTERNAL    a kernel found its launch set-up unusable (its shared
+ *                         memory window not 1024-byte aligned) and wrote
+ *                         nothing (never expected)
  */
 #ifndef PA_H_
 #define PA_H_
@@ -82,6 +85,7 @@ typedef enum {
 #define PA_DEV_BAD_QSL 0x8u
 #define PA_DEV_OVERFLOW 0x10u
 #define PA_DEV_TIMEOUT 0x20u
+#define PA_DEV_INTERNAL 0x40u
 
 /*
  * pa_forward -- unified paged attention over a mixed batch.

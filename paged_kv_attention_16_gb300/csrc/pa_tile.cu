@@ -11,16 +11,25 @@
 // GB300 design.  One work item = 128 query rows (128/G tokens x the G heads of
 // one KV head, GQA-packed so the M = 128 MMA is full and the causal diagonal of
 // a tile is only 128/G positions wide) x one KV split.  Per CTA (2 per SM):
-//   warp 4   TMA producer: Q tile (128-byte swizzled boxes of G heads x 128/G
-//            tokens), then per 64-position KV tile the K page boxes {64 dims x
-//            16 slots} and the V page boxes {16 slots x all dims} named by the
-//            block table (K double-buffered, V one tile behind K);
+//   warps 4, 7, 6  TMA producers: the Q tile (128-byte swizzled boxes of G
+//            heads x 128/G tokens), then per 64-position KV tile the K page
+//            boxes {64 dims x 16 slots} (half the 64-dim chunks from warp 4,
+//            half from warp 7) and the V page boxes {16 slots x all dims}
+//            (warp 6) named by the block table, into rings of three K and two
+//            V tiles.  A TMA copy holds its issuing warp for about as long as
+//            the data takes to land (measured: some 20 bytes per clock per
+//            warp, whatever the depth of the ring), so one warp could not
+//            keep up with two CTAs' products; three can.  (The 192-wide keys
+//            fit only one K stage beside Q: there warp 4 alone loads K of
+//            tile j, then V of tile j - 1.)
 //   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
 //            K=head_dim, bf16 in, fp32 in TMEM) into one of two S buffers,
 //            running a tile ahead of the softmax, then O += P V with P read
 //            from TMEM (N=head_dim, K=64, V read MN-major straight from its
 //            page layout);
-//   warps 0-3  softmax: thread r owns row r (TMEM lane r): loads its S row,
+//   warps 0-3  softmax: thread r owns row r (TMEM lane r): reads its S row
+//            (twice -- for the maximum, then for the weights -- where 128
+//            registers a thread leave no room to hold 64 scores),
 //            masks by select (causal bound, split bound), keeps a base-2
 //            online softmax with lazy rescaling of O in TMEM (only when the
 //            running max grows by more than 8), stores P as packed bf16 over
@@ -42,11 +51,13 @@ namespace {
 // it measured slower (mixed batch 2.00 ms against 1.62 ms).
 constexpr int kBN = 64;
 constexpr int kBox = 16;           // slots per TMA box
-constexpr int kTileThreads = 192;  // 4 softmax warps, 1 producer warp, 1 MMA warp
-constexpr int kKStages = 2;        // K tiles in flight per CTA (at most; see TileCfg::KST)
+constexpr int kKWarp0 = 4, kMmaWarp = 5, kVWarp = 6, kKWarp1 = 7;
+constexpr int kKStages = 3;        // K tiles in flight per CTA (at most; see TileCfg::KST)
 constexpr int kVStages = 2;        // V tiles in flight per CTA
-constexpr int kTileCtasPerSm = kBN == 64 ? 2 : 1;  // resident CTAs per SM (grid = SMs x this)
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
+// Dynamic shared memory one CTA may take with `ctas` CTAs per SM (228 KB
+// per SM, 1 KB of it reserved per CTA).
+constexpr int tile_smem_budget(int ctas) { return 233472 / ctas - 1024; }
 constexpr uint32_t kTmemCols = kBN == 64 ? 256 : 512;
 // Tensor memory: two S buffers of kBN fp32 columns; P (kBN bf16 per row =
 // kBN / 2 columns) is written over the first half of its own S buffer; O after
@@ -76,14 +87,30 @@ struct TileCfg {
   static constexpr int K_BYTES = NHQ * KV_HALF;
   static constexpr int V_BYTES = NHV * KV_HALF;
   static constexpr int V_BOX = NHV * kBox * 128;    // one V box: [chunks][16 rows][128 B]
-  // K stages: two while they fit two CTAs per SM beside Q and two V stages
-  static constexpr int KST = Q_BYTES + 2 * K_BYTES + kVStages * V_BYTES <= 100 * 1024 ? 2 : 1;
+  // Two CTAs per SM (two softmax pipelines share the tensor pipe), two V
+  // stages, and as many K stages, up to three, as fit beside Q.  Where two or
+  // more fit, the loads come from three producer warps and the softmax
+  // (128 registers a thread) reads S from TMEM twice; where only one fits
+  // (the 192-wide keys), a single producer warp interleaves K and V, and the
+  // softmax (168 registers) reads S once and holds it.  (A one-stage V ring
+  // gave wrong results on the 192-wide keys and is not used.)
+  static constexpr int TAIL = kNumBars * 8 + 64;
+  static constexpr bool fits(int k, int v) {
+    return Q_BYTES + k * K_BYTES + v * V_BYTES + TAIL <= tile_smem_budget(2);
+  }
+  static constexpr bool SPLIT = fits(2, kVStages);
+  static constexpr int KST = fits(3, kVStages) ? 3 : SPLIT ? 2 : 1;
+  static constexpr int VST = kVStages;
+  static constexpr int THREADS = SPLIT ? 256 : 192;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
-  static constexpr int OFF_BAR = OFF_V + kVStages * V_BYTES;
+  static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
-  static constexpr int SMEM = OFF_MISC + 64 + 1024;  // + slack for 1024-byte alignment
+  // no alignment slack: the dynamic window is declared 1024-aligned (and
+  // the kernel checks that it is)
+  static constexpr int SMEM = OFF_MISC + 64;
+  static_assert(fits(KST, VST), "shared memory budget");
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, DV, 1);
   static_assert(DQK % 64 == 0 && DQK <= 256 && (DV == 64 || DV == 128), "tile widths");
@@ -133,14 +160,14 @@ __device__ inline bool decode_tile_item(const FwdParams &p, long long item, int 
 
 // PB64: every 64-position tile is one page's 64 slots (one box per tile).
 template <int DQK, int DV, bool PB64>
-__global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
+__global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
     tile_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_kr,
                 const FwdParams p) {
   using C = TileCfg<DQK, DV>;
-  extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzled operand tiles need 1024-byte alignment.
-  uint8_t *smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = smem_raw;
   uint8_t *sQ = smem + C::OFF_Q;
   uint8_t *sK = smem + C::OFF_K;
   uint8_t *sV = smem + C::OFF_V;
@@ -156,6 +183,10 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   pdl_wait();  // the plan, and the row kernel before us in the stream
   const long long n_items = p.plan->n[kListTile];
   if (n_items == 0) return;  // no extend / prefill rows in this batch
+  if (smem_u32(smem_raw) & 1023) {  // the same for every thread: all leave together
+    if (tid == 0) atomicOr(p.status, PA_DEV_INTERNAL);
+    return;
+  }
 
   if (tid == 0) {
     prefetch_tensor_map(&tm_q);
@@ -168,93 +199,163 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
     }
     fence_mbar_init();
   }
-  if (warp == 5) tc_alloc(s_tmem, kTmemCols);
+  if (warp == kMmaWarp) tc_alloc(s_tmem, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   bool dead = false;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------- producer
-    uint32_t tiles = 0, items = 0;
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
-      TileItem it;
-      if (!decode_tile_item(p, item, G, it)) continue;
-      const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
-      PageCache kc, vc;  // one per stream: each only moves forward
-      kc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
-      vc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
-      if (lane == 0) {
-        if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
-        mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
-        for (int h = 0; h < C::NHQ; ++h)
-          tma_load_3d(sQ + h * 128 * 128, &tm_q, h * 64, it.kvh * G, it.q_start + it.t0,
-                      &bar[kQFull]);
-      }
-      // K of tile j, then V of tile j - 1 (V is consumed a softmax later).
-      for (int j = 0; j <= it.nt; ++j) {
-        for (int which = 0; which < 2; ++which) {
-          const int jj = which == 0 ? j : j - 1;
-          if (jj < 0 || jj >= it.nt) continue;
-          const uint32_t g = tiles + jj;
+  if (warp == kKWarp0 || warp == kKWarp1 || warp == kVWarp) {
+    if constexpr (C::SPLIT) {
+      // ------------------------------------------------------------- producers
+      // A TMA copy holds up the warp that issues it for about as long as its
+      // data takes to arrive (some 20 bytes per clock per warp), so the loads
+      // are spread over three warps: K chunks [0, KH) and Q (kKWarp0, which
+      // also posts each K tile's byte count), K chunks [KH, NHQ) (kKWarp1; its
+      // bytes may land first: the tile cannot complete while kKWarp0's arrival
+      // is pending), and V (kVWarp).  Each walks the same items and tiles.
+      const bool is_v = warp == kVWarp, lead = warp == kKWarp0;
+      constexpr int KH = (C::NHQ + 1) / 2;
+      const int h_lo = warp == kKWarp1 ? KH : 0, h_hi = warp == kKWarp0 ? KH : C::NHQ;
+      uint32_t tiles = 0, items = 0;
+      for (long long item = blockIdx.x; item < n_items && (is_v || h_lo < h_hi);
+           item += gridDim.x) {
+        TileItem it;
+        if (!decode_tile_item(p, item, G, it)) continue;
+        const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
+        PageCache pc;  // the pages of this warp's stream: only moves forward
+        pc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
+        if (lead && lane == 0) {
+          if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
+          mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
+          for (int h = 0; h < C::NHQ; ++h)
+            tma_load_3d(sQ + h * 128 * 128, &tm_q, h * 64, it.kvh * G, it.q_start + it.t0,
+                        &bar[kQFull]);
+        }
+        for (int j = 0; j < it.nt; ++j) {
+          const uint32_t g = tiles + j;
           // 16-slot boxes, one per lane; or, when a tile is one page's 64
-          // slots, a single 64-slot box from lane 0 (a quarter of the TMA
-          // operations: their count, not their bytes, limits the loads)
-          const int pos = it.kv_lo + jj * kBN + (pb64 ? 0 : lane * kBox);
+          // slots, a single 64-slot box from lane 0
+          const int pos = it.kv_lo + j * kBN + (pb64 ? 0 : lane * kBox);
           const bool need = (pb64 ? lane == 0 : lane < kBN / kBox) && pos < it.kv_hi;
-          const int page = (which == 0 ? kc : vc).get(need ? pos / bs : -1, lane);
+          const int page = pc.get(need ? pos / bs : -1, lane);
           const bool ok = need && page >= 0 && page < p.num_blocks;
-          if (need && !ok) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+          if (need && !ok && !is_v) atomicOr(p.status, PA_DEV_BAD_BLOCK);
           const unsigned mask = __ballot_sync(0xffffffffu, ok);
-          uint64_t *full;
-          uint8_t *dst;
-          const CUtensorMap *map;
-          if (which == 0) {
-            const int st = g % C::KST;
-            full = &bar[kKFull0 + st];
-            dst = sK + st * C::K_BYTES;
-            map = &tm_k;
-            if (lane == 0 && g >= C::KST)
-              mbar_wait(&bar[kKFree0 + st], ((g / C::KST) - 1) & 1, dead, p.status);
+          if (is_v) {
+            const int st = g % C::VST;
+            if (lane == 0) {
+              if (g >= C::VST)
+                mbar_wait(&bar[kVFree0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
+              mbar_arrive_expect_tx(&bar[kVFull0 + st],
+                                    __popc(mask) * C::NHV * (pb64 ? kBN : kBox) * 128);
+            }
+            __syncwarp();
+            // V: [16-slot boxes][chunks][16 rows], or [chunks][64 rows] (each
+            // K = 16 step of the PV product is one box)
+            if (ok)
+              tma_load_5d(sV + st * C::V_BYTES + (pb64 ? 0 : lane * C::V_BOX), &tm_v, 0, pos % bs,
+                          0, it.kvh, page, &bar[kVFull0 + st]);
           } else {
-            const int st = g % kVStages;
-            full = &bar[kVFull0 + st];
-            dst = sV + st * C::V_BYTES;
-            map = &tm_v;
-            if (lane == 0 && g >= kVStages)
-              mbar_wait(&bar[kVFree0 + st], ((g / kVStages) - 1) & 1, dead, p.status);
-          }
-          if (lane == 0)
-            mbar_arrive_expect_tx(full, __popc(mask) * (which == 0 ? C::NHQ : C::NHV) *
-                                            (pb64 ? kBN : kBox) * 128);
-          __syncwarp();
-          // K: one box per 64-dim half ([halves][64 rows] for the S product's
-          // uniform row stride); V: one box per 16 slots with both halves
-          // ([16-row boxes][halves]: each K = 16 step of the PV product is one
-          // box), half as many TMA boxes.
-          if (ok) {
-            if (which == 0) {
-              for (int h = 0; h < C::NHQ; ++h) {
+            const int st = g % C::KST;
+            if (lane == 0) {
+              if (g >= C::KST)
+                mbar_wait(&bar[kKFree0 + st], ((g / C::KST) - 1) & 1, dead, p.status);
+              if (lead)
+                mbar_arrive_expect_tx(&bar[kKFull0 + st],
+                                      __popc(mask) * C::NHQ * (pb64 ? kBN : kBox) * 128);
+            }
+            __syncwarp();
+            // K: one box per 64-dim chunk ([chunks][64 rows] for the S
+            // product's uniform row stride)
+            if (ok) {
+              for (int h = h_lo; h < h_hi; ++h) {
                 // split keys: the last 64 columns are the shared rotary key
                 const bool rope = p.k_rope_split && h == C::NHQ - 1;
-                tma_load_4d(dst + h * C::KV_HALF + (pb64 ? 0 : lane * kBox * 128),
-                            rope ? &tm_kr : map, rope ? 0 : h * 64, rope ? 0 : it.kvh, pos % bs,
-                            page, full);
+                tma_load_4d(sK + st * C::K_BYTES + h * C::KV_HALF + (pb64 ? 0 : lane * kBox * 128),
+                            rope ? &tm_kr : &tm_k, rope ? 0 : h * 64, rope ? 0 : it.kvh, pos % bs,
+                            page, &bar[kKFull0 + st]);
               }
-            } else {
-              // V: [16-slot boxes][chunks][16 rows], or [chunks][64 rows]
-              tma_load_5d(dst + (pb64 ? 0 : lane * C::V_BOX), map, 0, pos % bs, 0, it.kvh, page,
-                          full);
             }
           }
-
+          __syncwarp();
         }
+        tiles += it.nt;
+        ++items;
       }
-      tiles += it.nt;
-      ++items;
+    } else {
+      // One producer warp (warp 4): Q, then K of tile j and V of tile j - 1
+      // (V is consumed a softmax later).
+      uint32_t tiles = 0, items = 0;
+      for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+        TileItem it;
+        if (!decode_tile_item(p, item, G, it)) continue;
+        const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
+        PageCache kc, vc;  // one per stream: each only moves forward
+        kc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
+        vc.start(bt, p.max_blocks_per_seq, it.kv_lo / bs, lane);
+        if (lane == 0) {
+          if (items > 0) mbar_wait(&bar[kQFree], (items - 1) & 1, dead, p.status);
+          mbar_arrive_expect_tx(&bar[kQFull], C::Q_BYTES);
+          for (int h = 0; h < C::NHQ; ++h)
+            tma_load_3d(sQ + h * 128 * 128, &tm_q, h * 64, it.kvh * G, it.q_start + it.t0,
+                        &bar[kQFull]);
+        }
+        for (int j = 0; j <= it.nt; ++j) {
+#pragma unroll
+          for (int which = 0; which < 2; ++which) {
+            const int jj = which == 0 ? j : j - 1;
+            if (jj < 0 || jj >= it.nt) continue;
+            const uint32_t g = tiles + jj;
+            const int pos = it.kv_lo + jj * kBN + (pb64 ? 0 : lane * kBox);
+            const bool need = (pb64 ? lane == 0 : lane < kBN / kBox) && pos < it.kv_hi;
+            // (each cache by name: a reference chosen at run time would move
+            // both caches to local memory, a slow round trip per look-up)
+            const int page = which == 0 ? kc.get(need ? pos / bs : -1, lane)
+                                        : vc.get(need ? pos / bs : -1, lane);
+            const bool ok = need && page >= 0 && page < p.num_blocks;
+            if (need && !ok) atomicOr(p.status, PA_DEV_BAD_BLOCK);
+            const unsigned mask = __ballot_sync(0xffffffffu, ok);
+            if (which == 0) {
+              const int st = g % C::KST;
+              if (lane == 0) {
+                if (g >= C::KST)
+                  mbar_wait(&bar[kKFree0 + st], ((g / C::KST) - 1) & 1, dead, p.status);
+                mbar_arrive_expect_tx(&bar[kKFull0 + st],
+                                      __popc(mask) * C::NHQ * (pb64 ? kBN : kBox) * 128);
+              }
+              __syncwarp();
+              if (ok) {
+                for (int h = 0; h < C::NHQ; ++h) {
+                  const bool rope = p.k_rope_split && h == C::NHQ - 1;
+                  tma_load_4d(sK + st * C::K_BYTES + h * C::KV_HALF +
+                                  (pb64 ? 0 : lane * kBox * 128),
+                              rope ? &tm_kr : &tm_k, rope ? 0 : h * 64, rope ? 0 : it.kvh,
+                              pos % bs, page, &bar[kKFull0 + st]);
+                }
+              }
+            } else {
+              const int st = g % C::VST;
+              if (lane == 0) {
+                if (g >= C::VST)
+                  mbar_wait(&bar[kVFree0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
+                mbar_arrive_expect_tx(&bar[kVFull0 + st],
+                                      __popc(mask) * C::NHV * (pb64 ? kBN : kBox) * 128);
+              }
+              __syncwarp();
+              if (ok)
+                tma_load_5d(sV + st * C::V_BYTES + (pb64 ? 0 : lane * C::V_BOX), &tm_v, 0,
+                            pos % bs, 0, it.kvh, page, &bar[kVFull0 + st]);
+            }
+            __syncwarp();
+          }
+        }
+        tiles += it.nt;
+        ++items;
+      }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       uint32_t tiles = 0, items = 0;
@@ -285,9 +386,9 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
         if (it.nt > 1) issue_s(tiles + 1);
         for (int j = 0; j < it.nt; ++j) {
           const uint32_t g = tiles + j;
-          const int pb = g & 1, vs = g % kVStages;
+          const int pb = g & 1, vs = g % C::VST;
           mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, p.status);
-          mbar_wait(&bar[kVFull0 + vs], (g / kVStages) & 1, dead, p.status);
+          mbar_wait(&bar[kVFull0 + vs], (g / C::VST) & 1, dead, p.status);
           if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
           tc_fence_after();
           const uint32_t vb = sv + vs * C::V_BYTES;
@@ -352,47 +453,68 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
       const float c2 = p.scale_log2;
       const bool fold = c2 > 0.f && !p.alibi;
       float m = -INFINITY, l = 0.f;
+      // With registers to spare (one producer warp) a tile's 64 scores are
+      // read from TMEM once and held; with three producer warps (128
+      // registers a thread) S is read twice, once for the row maximum, once
+      // for the weights.
+      constexpr bool kOnePass = !C::SPLIT;
       for (int j = 0; j < it.nt; ++j) {
         const uint32_t g = tiles + j;
         const int base = it.kv_lo + j * kBN;
         const int pb = g & 1;  // S buffer of this tile; P goes over its first half
         mbar_wait(&bar[kSFull0 + pb], (g >> 1) & 1, dead, p.status);
         tc_fence_after();
-        float s[kBN];
         if (warp_active) {
-          uint32_t raw[kBN];
+          // raw S of this tile -> scaled (and biased) scores, masked to the
+          // row's visible range; column c is position base + c
+          const bool cross = __any_sync(0xffffffffu, base + kBN > row_hi || base < row_lo);
+          auto scores = [&](float (&x)[kBN]) {
+            {
+              uint32_t raw[kBN];
 #pragma unroll
-          for (int c0 = 0; c0 < kBN; c0 += 32)
-            tc_ld32(tmem + lane_off + kTmemS + pb * kBN + c0,
-                    *reinterpret_cast<uint32_t(*)[32]>(raw + c0));
-          tc_wait_ld();
+              for (int c0 = 0; c0 < kBN; c0 += 32)
+                tc_ld32(tmem + lane_off + kTmemS + pb * kBN + c0,
+                        *reinterpret_cast<uint32_t(*)[32]>(raw + c0));
+              tc_wait_ld();
 #pragma unroll
-          for (int x = 0; x < kBN; ++x) s[x] = __uint_as_float(raw[x]);
-        }
-        if (warp_active) {
-          if (!fold) {
-            if (p.alibi) {
-              const float dist0 = (float)(qpos - base);
-#pragma unroll
-              for (int c = 0; c < kBN; ++c)
-                s[c] = fmaf(s[c], c2, alibi_bias(al, dist0 - (float)c, p.alibi_sqrt));
-            } else {
-#pragma unroll
-              for (int c = 0; c < kBN; ++c) s[c] *= c2;
+              for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(raw[c]);
             }
-          }
-          // Only tiles that cross a row's bounds need the select.
-          if (__any_sync(0xffffffffu, base + kBN > row_hi || base < row_lo)) {
+            if (!fold) {
+              if (p.alibi) {
+                const float dist0 = (float)(qpos - base);
 #pragma unroll
-            for (int c = 0; c < kBN; ++c)
-              s[c] = (base + c < row_hi && base + c >= row_lo) ? s[c] : -INFINITY;
-          }
+                for (int c = 0; c < kBN; ++c)
+                  x[c] = fmaf(x[c], c2, alibi_bias(al, dist0 - (float)c, p.alibi_sqrt));
+              } else {
+#pragma unroll
+                for (int c = 0; c < kBN; ++c) x[c] *= c2;
+              }
+            }
+            if (cross) {
+#pragma unroll
+              for (int c = 0; c < kBN; ++c) {
+                const int pos = base + c;
+                x[c] = (pos < row_hi && pos >= row_lo) ? x[c] : -INFINITY;
+              }
+            }
+          };
           // row max with 8 independent chains (a single chain is 64 deep)
           float mxa[8];
+          auto row_max = [&](const float (&x)[kBN]) {
 #pragma unroll
-          for (int x = 0; x < 8; ++x) mxa[x] = s[x];
+            for (int c = 0; c < 8; ++c) mxa[c] = x[c];
 #pragma unroll
-          for (int c = 8; c < kBN; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], s[c]);
+            for (int c = 8; c < kBN; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], x[c]);
+          };
+          float sv[kOnePass ? kBN : 1];  // the scores, held in one-pass mode
+          if constexpr (kOnePass) {
+            scores(*reinterpret_cast<float(*)[kBN]>(sv));
+            row_max(*reinterpret_cast<float(*)[kBN]>(sv));
+          } else {
+            float x[kBN];
+            scores(x);
+            row_max(x);
+          }
           float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
                            fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
           if (fold && mx != -INFINITY) mx *= c2;
@@ -423,27 +545,38 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
           const float mu = m == -INFINITY ? 0.f : m;
           const float cs = fold ? c2 : 1.f;
           float suma[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          uint32_t pw[kBN / 2];
+          // P of columns [c0, c0 + 32) (16 packed words) goes over S columns
+          // [c0 / 2, c0 / 2 + 16), already read.
+          auto weights = [&](const float (&x)[kBN]) {
 #pragma unroll
-          for (int x = 0; x < kBN / 2; ++x) {
-            const float p0 = fast_exp2(fmaf(s[2 * x], cs, -mu));
-            const float p1 = fast_exp2(fmaf(s[2 * x + 1], cs, -mu));
-            suma[x & 7] += p0 + p1;
-            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-            pw[x] = *reinterpret_cast<const uint32_t *>(&h2);
+            for (int c0 = 0; c0 < kBN; c0 += 32) {
+              uint32_t pw[16];
+#pragma unroll
+              for (int w = 0; w < 16; ++w) {
+                const float p0 = fast_exp2(fmaf(x[c0 + 2 * w], cs, -mu));
+                const float p1 = fast_exp2(fmaf(x[c0 + 2 * w + 1], cs, -mu));
+                suma[w & 7] += p0 + p1;
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                pw[w] = *reinterpret_cast<const uint32_t *>(&h2);
+              }
+              tc_st16(tmem + lane_off + kTmemS + pb * kBN + c0 / 2, pw);
+            }
+          };
+          if constexpr (kOnePass) {
+            weights(*reinterpret_cast<const float(*)[kBN]>(sv));
+          } else {
+            float x[kBN];
+            scores(x);
+            weights(x);
           }
-#pragma unroll
-          for (int c0 = 0; c0 < kBN / 2; c0 += 32)
-            tc_st32(tmem + lane_off + kTmemS + pb * kBN + c0,
-                    *reinterpret_cast<const uint32_t(*)[32]>(pw + c0));
           tc_wait_st();
           l += ((suma[0] + suma[1]) + (suma[2] + suma[3])) + ((suma[4] + suma[5]) + (suma[6] + suma[7]));
         }
         if (j == it.nt - 1 && it.kv_hi - base < kBN) {
           // Rows past the tile's KV end may hold anything (NaN tails, stale
           // data); P is 0 there but 0 * NaN is NaN, so zero those V rows.
-          const int vst = g % kVStages;
-          mbar_wait(&bar[kVFull0 + vst], (g / kVStages) & 1, dead, p.status);
+          const int vst = g % C::VST;
+          mbar_wait(&bar[kVFull0 + vst], (g / C::VST) & 1, dead, p.status);
           const int first = it.kv_hi - base;
           const int nchunks = (kBN - first) * 8 * C::NHV;
           uint8_t *vs = sV + vst * C::V_BYTES;
@@ -521,7 +654,7 @@ __global__ void __launch_bounds__(kTileThreads, kTileCtasPerSm)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 5) tc_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc_dealloc(tmem, kTmemCols);
 }
 
 template <int DQK, int DV, bool PB64>
@@ -535,7 +668,7 @@ cudaError_t launch_v(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  return launch_dependent(kern, dim3(num_sms * kTileCtasPerSm), dim3(kTileThreads), C::SMEM,
+  return launch_dependent(kern, dim3(num_sms * 2), dim3(C::THREADS), C::SMEM,
                           stream, tq, tk, tv, tkr, p);
 }
 

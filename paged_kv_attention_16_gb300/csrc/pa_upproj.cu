@@ -18,15 +18,21 @@
 //            16-aligned runs per request, and a 16-row run of positions lies
 //            in one page when block_size is a multiple of 16), one barrier per
 //            64-column chunk so the next unit's chunk k loads as soon as the
-//            last MMA reading this unit's chunk k is done; then per head eight
-//            B chunks of 256 w_kv rows x 64 columns through a 3-stage ring;
+//            last MMA reading this unit's chunk k is done;
+//   warps 6-9  TMA producers of B: per head eight chunks of 256 w_kv rows x
+//            64 columns through a 3-stage ring, each warp a quarter (64 rows)
+//            of every chunk.  A TMA copy holds up the warp that issues it for
+//            about as long as the data takes to arrive, so one warp moves
+//            only some 20 bytes per clock; a chunk (32 KB) is consumed in
+//            about 500 clocks, so four warps share the loads;
 //   warp 5   MMA issuer (one thread): per head, D (M = 128, N = 256, fp32 in
 //            TMEM) += A_k B_k^T over the eight chunks, into one of two TMEM
 //            accumulators, so the epilogue of head h overlaps the MMAs of
 //            head h + 1;
-//   warps 0-3  epilogue: thread r owns dense row r (TMEM lane r) and writes
-//            its 128 key and 128 value entries, rounded to nearest-even bf16,
-//            into that head's key and value rows.
+//   warps 0-3  epilogue: thread r owns dense row r (TMEM lane r); its 128 key
+//            and 128 value entries, rounded to nearest-even bf16, go to that
+//            head's key and value rows, two neighbouring lanes storing each
+//            whole 32-byte sector together.
 #include "pa_internal.h"
 
 namespace pa {
@@ -40,7 +46,10 @@ constexpr int kUpM = 128;          // dense rows per tile
 constexpr int kUpKC = kUpL / 64;   // 64-column chunks of the contraction
 constexpr int kUpGroups = kUpM / 16;
 constexpr int kUpBStages = 3;
-constexpr int kUpThreads = 192;    // 4 epilogue warps, producer warp, MMA warp
+constexpr int kUpWWarps = 4;       // warps loading B, a quarter of each chunk each
+constexpr int kUpWarpW0 = 6;       // first of them
+constexpr int kUpWRows = kUpN / kUpWWarps;
+constexpr int kUpThreads = 32 * (kUpWarpW0 + kUpWWarps);  // + 4 epilogue, A producer, MMA
 constexpr int kUpHeadsPerUnit = 8; // heads sharing one resident A tile
 constexpr uint32_t kUpTmemCols = 512;  // two N = 256 fp32 accumulators
 
@@ -116,7 +125,7 @@ __global__ void __launch_bounds__(kUpThreads, 1)
 
   if (warp == 4) {
     // ------------------------------------------------------------- producer
-    uint32_t bcount = 0, ucount = 0;
+    uint32_t ucount = 0;
     for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
       long long r0;
       int h0, h1;
@@ -139,32 +148,46 @@ __global__ void __launch_bounds__(kUpThreads, 1)
         }
       }
       const unsigned mask = __ballot_sync(0xffffffffu, ok);
-      for (int h = h0; h < h1; ++h) {
-        for (int kc = 0; kc < kUpKC; ++kc) {
-          if (h == h0) {
-            // A chunk kc of this unit, once the previous unit's last MMA on it is done
-            if (lane == 0) {
-              if (ucount > 0) mbar_wait(&bar[kAFree0 + kc], (ucount - 1) & 1, dead, a.status);
-              mbar_arrive_expect_tx(&bar[kAFull0 + kc], __popc(mask) * 16 * 128);
-            }
-            __syncwarp();
-            if (ok)
-              tma_load_3d(sA + kc * A_CHUNK + lane * 16 * 128, &tm_c, kc * 64, slot, page,
-                          &bar[kAFull0 + kc]);
-          }
-          if (lane == 0) {
-            const int st = bcount % kUpBStages;
-            if (bcount >= kUpBStages)
-              mbar_wait(&bar[kBFree0 + st], ((bcount / kUpBStages) - 1) & 1, dead, a.status);
-            mbar_arrive_expect_tx(&bar[kBFull0 + st], B_STAGE);
-            tma_load_2d(sB + st * B_STAGE, &tm_w, kc * 64, h * kUpN, &bar[kBFull0 + st]);
-          }
-          ++bcount;
-          __syncwarp();
+      for (int kc = 0; kc < kUpKC; ++kc) {
+        // A chunk kc of this unit, once the previous unit's last MMA on it is done
+        if (lane == 0) {
+          if (ucount > 0) mbar_wait(&bar[kAFree0 + kc], (ucount - 1) & 1, dead, a.status);
+          mbar_arrive_expect_tx(&bar[kAFull0 + kc], __popc(mask) * 16 * 128);
         }
+        __syncwarp();
+        if (ok)
+          tma_load_3d(sA + kc * A_CHUNK + lane * 16 * 128, &tm_c, kc * 64, slot, page,
+                      &bar[kAFull0 + kc]);
+        __syncwarp();
       }
       ++ucount;
     }
+  } else if (warp >= kUpWarpW0) {
+    // ------------------------------------------------------------- B producers
+    // Warp q loads rows [64 q, 64 q + 64) of every chunk; the first also
+    // posts the chunk's byte count (the others' bytes may land before it: the
+    // stage cannot complete while that arrival is pending).
+    const int q = warp - kUpWarpW0;
+    if (lane == 0) {
+      uint32_t bcount = 0;
+      for (long long u = blockIdx.x; u < n_units; u += gridDim.x) {
+        long long r0;
+        int h0, h1;
+        unit_of(u, r0, h0, h1);
+        for (int h = h0; h < h1; ++h) {
+          for (int kc = 0; kc < kUpKC; ++kc) {
+            const int st = bcount % kUpBStages;
+            if (bcount >= kUpBStages)
+              mbar_wait(&bar[kBFree0 + st], ((bcount / kUpBStages) - 1) & 1, dead, a.status);
+            if (q == 0) mbar_arrive_expect_tx(&bar[kBFull0 + st], B_STAGE);
+            tma_load_2d(sB + st * B_STAGE + q * kUpWRows * 128, &tm_w, kc * 64,
+                        h * kUpN + q * kUpWRows, &bar[kBFull0 + st]);
+            ++bcount;
+          }
+        }
+      }
+    }
+    __syncwarp();
   } else if (warp == 5) {
     // ------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -209,32 +232,50 @@ __global__ void __launch_bounds__(kUpThreads, 1)
       long long r0;
       int h0, h1;
       unit_of(u, r0, h0, h1);
-      const long long row = r0 + r;
-      const bool write = row < total;
+      // Lanes 2k and 2k + 1 (rows 2k and 2k + 1 of the warp) store together:
+      // each store of the pair fills one whole 32-byte sector of one row, so
+      // no sector is half written (which would make L2 fetch the other half
+      // from DRAM).  rowA / rowB: the pair's even and odd row.
+      const bool odd = lane & 1;
+      const long long rowA = r0 + (r & ~1), rowB = r0 + (r | 1);
+      const bool writeA = rowA < total, writeB = rowB < total;
       for (int h = h0; h < h1; ++h) {
         const uint32_t acc = tcount & 1;
         mbar_wait(&bar[kAccFull0 + acc], (tcount >> 1) & 1, dead, a.status);
         tc_fence_after();
-        __nv_bfloat16 *kdst = a.k_nope + ((size_t)row * H + h) * kUpHalf;
-        __nv_bfloat16 *vdst = a.v + ((size_t)row * H + h) * kUpHalf;
 #pragma unroll 1
         for (int c0 = 0; c0 < kUpN; c0 += 32) {
           uint32_t raw[32];
           tc_ld32(tmem + lane_off + acc * kUpN + c0, raw);
           tc_wait_ld();
-          if (write) {
-            uint4 *dst = reinterpret_cast<uint4 *>(c0 < kUpHalf ? kdst + c0 : vdst + (c0 - kUpHalf));
+          uint4 ch[4];  // this row's 64 bytes: four 16-byte chunks
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint32_t w[4];
+          for (int v = 0; v < 4; ++v) {
+            uint32_t w[4];
 #pragma unroll
-              for (int x = 0; x < 4; ++x) {
-                const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(raw[v * 8 + 2 * x]),
-                                                                __uint_as_float(raw[v * 8 + 2 * x + 1]));
-                w[x] = *reinterpret_cast<const uint32_t *>(&h2);
-              }
-              dst[v] = make_uint4(w[0], w[1], w[2], w[3]);
+            for (int x = 0; x < 4; ++x) {
+              const __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(raw[v * 8 + 2 * x]),
+                                                              __uint_as_float(raw[v * 8 + 2 * x + 1]));
+              w[x] = *reinterpret_cast<const uint32_t *>(&h2);
             }
+            ch[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+          const bool is_k = c0 < kUpHalf;
+          const int cc = is_k ? c0 : c0 - kUpHalf;  // first column in the key / value row
+          __nv_bfloat16 *baseA = (is_k ? a.k_nope : a.v) + ((size_t)rowA * H + h) * kUpHalf + cc;
+          __nv_bfloat16 *baseB = (is_k ? a.k_nope : a.v) + ((size_t)rowB * H + h) * kUpHalf + cc;
+#pragma unroll
+          for (int pv = 0; pv < 2; ++pv) {
+            const uint4 lo = ch[2 * pv], hi = ch[2 * pv + 1];
+            const uint4 send = odd ? lo : hi;
+            uint4 got;
+            got.x = __shfl_xor_sync(0xffffffffu, send.x, 1);
+            got.y = __shfl_xor_sync(0xffffffffu, send.y, 1);
+            got.z = __shfl_xor_sync(0xffffffffu, send.z, 1);
+            got.w = __shfl_xor_sync(0xffffffffu, send.w, 1);
+            const int chunk = 2 * pv + (odd ? 1 : 0);
+            if (writeA) reinterpret_cast<uint4 *>(baseA)[chunk] = odd ? got : lo;
+            if (writeB) reinterpret_cast<uint4 *>(baseB)[chunk] = odd ? hi : got;
           }
         }
         tc_fence_before();
@@ -261,10 +302,10 @@ cudaError_t launch_upproj(const UpprojArgs &a, const void *kv_cache, const void 
                                     (unsigned long long)a.num_blocks};
   const unsigned long long cs[2] = {kUpW * 2, (unsigned long long)a.block_size * kUpW * 2};
   const unsigned int cb[3] = {64, 16, 1};
-  // w_kv as [num_heads * 256 rows, 512 columns], boxes of 64 columns x 256 rows
+  // w_kv as [num_heads * 256 rows, 512 columns], boxes of 64 columns x 64 rows
   const unsigned long long wd[2] = {kUpL, (unsigned long long)a.num_heads * kUpN};
   const unsigned long long ws[1] = {kUpL * 2};
-  const unsigned int wb[2] = {64, kUpN};
+  const unsigned int wb[2] = {64, kUpWRows};
   if (!encode_tiled(&tm_c, kv_cache, PA_BF16, 3, cd, cs, cb, true) ||
       !encode_tiled(&tm_w, w_kv, PA_BF16, 2, wd, ws, wb, true))
     return cudaErrorInvalidValue;

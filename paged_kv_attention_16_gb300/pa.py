@@ -23,6 +23,7 @@ PA_DEV_BAD_SEQLEN = 0x4
 PA_DEV_BAD_QSL = 0x8
 PA_DEV_OVERFLOW = 0x10
 PA_DEV_TIMEOUT = 0x20
+PA_DEV_INTERNAL = 0x40
 PA_KV_NHD, PA_KV_HND = 0, 1  # pa_kv_layout
 
 # Every entry point declared in include/pa.h.
