@@ -164,20 +164,21 @@ pa_status pa_forward(const void *q, const void *k_cache, const void *v_cache,
  *   alibi_sqrt  0 or 1 (else PA_ERR_INVALID_ARG); ignored without slopes.
  *   max_query_len  0 = unknown; otherwise the caller's host-known bound on
  *          every request's new tokens (a serving scheduler knows it when it
- *          builds the batch).  1 declares a decode-only batch: with bf16
- *          inputs, head_dim 64 or 128, at most 16 query heads per KV head,
- *          num_tokens == num_seqs and at most as many (request, KV head)
- *          pairs as the row kernel has resident blocks (small batches, where
- *          launches dominate), the call then runs as ONE kernel launch --
- *          the row kernel sizes its own KV splits from max_seq_len and merges
- *          a row's splits in the thread block that finishes last -- instead
- *          of planner, row, tile and merge launches.  The contract is then
- *          query_start_loc[s] == s for every s: a request that breaks it
- *          (or whose seq_len is out of range) sets PA_DEV_BAD_QSL (or
- *          PA_DEV_BAD_SEQLEN) and its row s is written as zeros.  The split
- *          counters it uses live in a small library-owned buffer that is
- *          grown outside capture (PA_ERR_WORKSPACE during capture).  Other
- *          values only have to be >= 0 (else PA_ERR_INVALID_ARG).
+ *          builds the batch).  A request with more new tokens than the
+ *          bound is bad metadata: PA_DEV_BAD_QLEN, its rows written as
+ *          zeros.  1 declares a decode-only batch, and no tile kernel is
+ *          launched.  With bf16 inputs, head_dim 64 or 128, at most 16 query
+ *          heads per KV head, num_tokens == num_seqs <= 1024 and max_seq_len
+ *          <= 524288, such a call runs as ONE kernel launch -- the row kernel
+ *          sizes the KV splits from seq_lens itself (at most 64 a row) and
+ *          merges a row's splits in the thread block that finishes last --
+ *          instead of planner, row and merge launches.  The
+ *          contract is then query_start_loc[s] == s for every s: a request
+ *          that breaks it (or whose seq_len is out of range) sets
+ *          PA_DEV_BAD_QSL (or PA_DEV_BAD_SEQLEN) and its row s is written as
+ *          zeros.  The split counters it uses live in a small library-owned
+ *          buffer that is grown outside capture (PA_ERR_WORKSPACE during
+ *          capture).  Values must be >= 0 (else PA_ERR_INVALID_ARG).
  * Errors as for pa_forward.
  */
 typedef struct {

@@ -45,7 +45,7 @@ __device__ inline ReqScalars classify(const FwdParams &p, int q_start, int q_end
   r.q_len = q_end - q_start;
   r.ctx = ctx;
   r.valid = !qsl_bad && r.q_len >= 0 && r.ctx >= 0 && r.q_len <= r.ctx &&
-            r.ctx <= p.max_seq_len &&
+            (p.max_qlen <= 0 || r.q_len <= p.max_qlen) && r.ctx <= p.max_seq_len &&
             ceil_div_ll(r.ctx, p.block_size) <= (long long)p.max_blocks_per_seq;
   if (r.q_len == 1) r.cls = kDecode;
   else if (r.q_len == r.ctx) r.cls = kPrefill;
@@ -92,7 +92,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     v1[0] += 1ll << (21 * r.cls);
     if (r.valid && r.q_len == 1) v1[1] += p.window > 0 ? min(r.ctx, p.window) : r.ctx;
     if (!qsl_bad && !r.valid) {
-      if (r.q_len < 0 || r.q_len > r.ctx) metabad |= PA_DEV_BAD_QLEN;
+      if (r.q_len < 0 || r.q_len > r.ctx || (p.max_qlen > 0 && r.q_len > p.max_qlen))
+        metabad |= PA_DEV_BAD_QLEN;
       if (r.ctx < 0 || r.ctx > p.max_seq_len ||
           ceil_div_ll(r.ctx, p.block_size) > (long long)p.max_blocks_per_seq)
         metabad |= PA_DEV_BAD_SEQLEN;
@@ -765,41 +766,33 @@ bool tile_path_ok(int dtype, int head_dim, int group) {
   return tile_kernel_supported(dtype, head_dim, group);
 }
 
-// Decode-only batches (the caller declares max_query_len == 1): the split
-// length and the bound on splits per row come from host-known extents, so no
-// planner runs.  Contexts are taken to average about half their bound.
+// Decode-only batches (the caller declares max_query_len == 1): one row-kernel
+// launch, no planner.  The kernel sizes the splits from seq_lens itself; the
+// host only bounds the splits per row (so the partial rows fit a workspace
+// sized from max_seq_len) at fast_nsmax <= 64, the most a row's in-kernel
+// merge takes.
 struct FastPlan {
-  int split = 0, nsmax = 0;
+  int nsmax = 0;
   long long part_rows = 0;
   size_t part_o = 0, part_lse = 0, ws_bytes = 0;
 };
 
 bool fast_decode_plan(const FwdCall &c, int num_sms, FastPlan *f) {
+  (void)num_sms;
   if (c.max_query_len != 1 || c.dtype != PA_BF16 || c.all_tile || c.num_seqs <= 0 ||
-      c.num_tokens != c.num_seqs)
+      c.num_tokens != c.num_seqs || c.num_seqs > kFastMaxSeqs)
     return false;
   const int group = c.num_heads / c.num_kv_heads;
   if (!row_mma_supported(c.dtype, c.head_dim, group)) return false;
   const long long msl = c.max_seq_len > 0 ? c.max_seq_len : 1;
-  const long long row_ctas =
-      (long long)row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * (num_sms > 0 ? num_sms : 1);
-  // Only batches with at most one row group per resident block: there the
-  // planner, tile and merge launches are most of the call.  On larger
-  // batches the separate merge pass is cheaper than merging in the row
-  // kernel (every split would pay a fence and an atomic before its block
-  // moves on), so they keep the planned path.
-  if ((long long)c.num_seqs * c.num_kv_heads > row_ctas) return false;
-  const long long target = (group >= 8 ? 4ll : 8ll) * row_ctas;
-  long long L = ceil_div_h(ceil_div_h((long long)c.num_seqs * c.num_kv_heads * msl, 2 * target), 64) * 64;
-  if (L < kRowMinSplit) L = kRowMinSplit;
-  const long long lmin = ceil_div_h(ceil_div_h(msl, 64), 64) * 64;  // at most 64 splits a row
-  if (L < lmin) L = lmin;
-  // rows of at most 1024 positions are not split: a merge costs more than it saves
-  if (msl <= 1024) L = ceil_div_h(msl, 64) * 64;
-  if (c.kv_split_tokens > 0 && c.kv_split_tokens < L) L = c.kv_split_tokens;
-  const long long nsmax = ceil_div_h(msl, L);
-  if (L > kRowMaxSplit || nsmax > 64) return false;
-  f->split = (int)L;
+  if (msl > 64ll * kRowMaxSplit) return false;
+  // splits are at least kRowMinSplit long (or kv_split_tokens, if shorter)
+  long long nsmax = ceil_div_h(msl, kRowMinSplit);
+  if (c.kv_split_tokens > 0) nsmax = std::max(nsmax, ceil_div_h(msl, c.kv_split_tokens));
+  if (nsmax > 64) {
+    if (c.kv_split_tokens > 0) return false;  // the requested splits are too short
+    nsmax = 64;
+  }
   f->nsmax = (int)nsmax;
   f->part_rows = (long long)c.num_seqs * c.num_heads * nsmax;
   f->part_o = 0;
@@ -862,7 +855,6 @@ pa_status fast_decode_launch(const FwdCall &c, const FastPlan &f, void *workspac
   p.alibi_sqrt = c.alibi_sqrt;
   p.head_dim_qk = c.head_dim;
   p.fast = 1;
-  p.fast_split = f.split;
   p.fast_nsmax = f.nsmax;
   p.fast_work = fast_ctr;
   p.fast_cnt = reinterpret_cast<unsigned int *>(fast_ctr + 2);
@@ -952,6 +944,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.alibi_sqrt = c.alibi_sqrt;
   p.head_dim_qk = dqk;
   p.all_tile = c.all_tile ? 1 : 0;
+  p.max_qlen = c.max_query_len;
 
   int slot = timed ? prof_begin(PA_K_PLAN, st) : -1;
   // One thread per request, whole warps, at most kPlanThreads: small batches
@@ -1031,7 +1024,9 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
     }
     prof_end(slot, st);
     if (row_err != cudaSuccess) return PA_ERR_CUDA;
-    if (tile_ok) {
+    // A decode-only batch (the caller's bound max_query_len == 1; a request
+    // above it is zeroed as bad metadata) has no tile items: no launch.
+    if (tile_ok && c.max_query_len != 1) {
       // Q as [tokens, heads, dim] with 64-element (128-byte) swizzled boxes of
       // G heads x (128 / G) tokens.
       CUtensorMap tm_q;

@@ -97,13 +97,15 @@ struct FwdParams {
   int alibi_sqrt;           // 1: the bias grows with the square root of the distance
   int k_rope_split;         // 1: the last 64 key columns come from a separate
                             // [pages, slots, 1, 64] tensor shared by all heads
+  int max_qlen;             // the caller's bound on q_len (0: none); a request
+                            // above it is bad metadata (PA_DEV_BAD_QLEN)
   // Decode-only batches declared by the caller (one launch, no planner): the
-  // row kernel walks num_seqs x kv_heads x fast_nsmax item slots, splits of
-  // fast_split positions; partial rows (s * H + head) * fast_nsmax + split;
-  // fast_work: [0] item counter, [1] CTAs done taking items; fast_cnt:
-  // [num_seqs * kv_heads] splits finished per row group (zero between calls).
+  // row kernel sizes the splits itself from seq_lens (at most fast_nsmax a
+  // row); partial rows (s * H + head) * fast_nsmax + split; fast_work: [0]
+  // item counter, [1] CTAs done taking items; fast_cnt: [num_seqs *
+  // kv_heads] splits finished per row group (zero between calls).
   int fast;
-  int fast_split, fast_nsmax;
+  int fast_nsmax;
   unsigned long long *fast_work;
   unsigned int *fast_cnt;
 };
@@ -142,6 +144,9 @@ __device__ inline float sink_inv(const float *sinks, int head, float m, float l)
 // Largest split length of the row kernel (bounds its per-item page list).
 constexpr int kRowMaxSplit = 8192;
 constexpr int kRowMinSplit = 256;
+// Decode-only batches run as one row-kernel launch up to this many requests
+// (the kernel keeps one prefix entry per request in shared memory).
+constexpr int kFastMaxSeqs = 1024;
 // Rows per tensor-core tile of the extend/prefill kernel.
 constexpr int kTileRows = 128;
 

@@ -59,18 +59,24 @@ struct MmaRowCfg {
   static constexpr int KS = D / 16;                  // k-steps of S = Q K^T
   static constexpr int NT = D / 8;                   // n-tiles of O
   static constexpr int SCR_BYTES = NWARP * G * D * 4;
-  // two resident CTAs per SM: about 113 KB of shared memory each
-  static constexpr int NSTAGE0 = (112 * 1024 - SCR_BYTES - 4096) / STAGE_BYTES;
-  static constexpr int NSTAGE = NSTAGE0 < 2 ? 2 : (NSTAGE0 > 6 ? 6 : NSTAGE0);
   static constexpr int MAX_PAGES = kRowMaxSplit / BOX + 2;
+  static constexpr int FPREF_BYTES = (kFastMaxSeqs + 1) * 4;  // decode-only item prefix
+  // everything but the ring and the scratch (barriers for up to 6 stages)
+  static constexpr int MISC_BYTES = 2 * NWARP * G * 4 + MAX_PAGES * 4 + 2 * 64 + FPREF_BYTES + 16 * 8 + 16;
+  // two resident CTAs per SM: 228 KB less 1 KB reserved each, less the
+  // 1024-byte alignment slack
+  static constexpr int NSTAGE0 = (233472 / 2 - 1024 - 1024 - 64 - SCR_BYTES - MISC_BYTES) / STAGE_BYTES;
+  static constexpr int NSTAGE = NSTAGE0 < 2 ? 2 : (NSTAGE0 > 6 ? 6 : NSTAGE0);
   static constexpr int OFF_RING = 0;  // 1024-byte aligned (swizzle atoms)
   static constexpr int OFF_SCR = OFF_RING + NSTAGE * STAGE_BYTES;
   static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;
   static constexpr int OFF_PAGES = OFF_ML + 2 * NWARP * G * 4;
   static constexpr int OFF_DESC = OFF_PAGES + MAX_PAGES * 4;
-  static constexpr int OFF_BAR = (OFF_DESC + 2 * 64 + 15) / 16 * 16;
+  static constexpr int OFF_FPREF = OFF_DESC + 2 * 64;
+  static constexpr int OFF_BAR = (OFF_FPREF + FPREF_BYTES + 15) / 16 * 16;
   static constexpr int NBAR = 2 * NSTAGE + 4;
   static constexpr int SMEM = OFF_BAR + NBAR * 8 + 1024;  // + alignment slack
+  static_assert(2 * (SMEM + 64 + 1024) <= 233472, "two CTAs per SM");
   static constexpr int OPT = (G * D + 127) / 128;         // merge outputs per thread
   static_assert(D == 64 || D == 128, "head_dim 64 or 128");
   static_assert(G >= 1 && G <= 16, "at most 16 query heads per KV head");
@@ -125,6 +131,22 @@ __device__ inline uint32_t swz_addr(uint32_t base, int r, int c) {
 }
 
 
+// Decode-only batches: the KV positions row s reads (from its window's first
+// 16-slot boundary to its end), or -1 when its metadata is bad.
+__device__ inline int fast_work(const FwdParams &p, int s) {
+  const int ctx = __ldg(p.seq_lens + s);
+  const bool qok = __ldg(p.qsl + s) == s && __ldg(p.qsl + s + 1) == s + 1;
+  const bool cok = ctx >= 1 && ctx <= p.max_seq_len &&
+                   ceil_div_ll(ctx, p.block_size) <= (long long)p.max_blocks_per_seq;
+  if (!qok || !cok) return -1;
+  return ctx - (window_lo(ctx - 1, p.window) & ~15);
+}
+
+__device__ inline unsigned fast_bad_bits(const FwdParams &p, int s) {
+  const bool qok = __ldg(p.qsl + s) == s && __ldg(p.qsl + s + 1) == s + 1;
+  return qok ? PA_DEV_BAD_SEQLEN : PA_DEV_BAD_QSL;
+}
+
 template <int D, int G>
 __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensorMap tm_k,
                                                 const __grid_constant__ CUtensorMap tm_v,
@@ -168,8 +190,65 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
   if (warp == C::NWARP) {
     // ===================================================== producer warp
     const int Hk = p.num_kv_heads;
-    const long long n_items =
-        p.fast ? (long long)S * Hk * p.fast_nsmax : p.plan->n[kListRow];
+    // Decode-only batches: this warp sizes the splits from seq_lens -- the
+    // split length spreads the whole KV work over about (8 or, from G = 8,
+    // 4) items per resident block, at most fast_nsmax splits a row -- and
+    // lays the items out request by request, KV head by KV head (a row
+    // group's splits consecutive, so that they finish close together):
+    // s_fpref[s] = items before request s (a request with bad metadata has
+    // one item per KV head, which writes its row as zeros).
+    int *s_fpref = reinterpret_cast<int *>(smem + C::OFF_FPREF);
+    int fL = 0;
+    if (p.fast) {
+      long long wsum = 0;
+      int wmax = 0;
+      for (int s = lane; s < S; s += 32) {
+        const int w = fast_work(p, s);
+        s_fpref[s + 1] = w;
+        if (w > 0) {
+          wsum += w;
+          wmax = max(wmax, w);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o >= 1; o >>= 1) {
+        wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+        wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
+      }
+      const long long target = (G >= 8 ? 4ll : 8ll) * gridDim.x;
+      long long L = ceil_div_ll(ceil_div_ll(wsum * Hk, target), 64) * 64;
+      L = max(L, (long long)kRowMinSplit);
+      L = max(L, ceil_div_ll(ceil_div_ll(wmax, p.fast_nsmax), 64) * 64);
+      L = min(L, (long long)kRowMaxSplit);
+      // rows of at most 1024 positions are not split: a merge costs more than it saves
+      if (wmax <= 1024) L = max(64ll, ceil_div_ll(wmax, 64) * 64);
+      if (p.kv_split_tokens > 0 && p.kv_split_tokens < L) L = p.kv_split_tokens;
+      fL = (int)L;
+      // item counts: lane l takes a contiguous run of requests, an exclusive
+      // scan over the lanes, then each lane writes its run's inclusive ends
+      // over the works it alone has read
+      const int chunk = (S + 31) / 32, s0 = min(S, lane * chunk), s1 = min(S, s0 + chunk);
+      int cnt = 0;
+      for (int s = s0; s < s1; ++s) {
+        const int w = s_fpref[s + 1];
+        cnt += w < 0 ? Hk : (int)ceil_div_ll(w, fL) * Hk;
+      }
+      int run = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, run, o);
+        if (lane >= o) run += t;
+      }
+      run -= cnt;
+      for (int s = s0; s < s1; ++s) {
+        const int w = s_fpref[s + 1];
+        run += w < 0 ? Hk : (int)ceil_div_ll(w, fL) * Hk;
+        s_fpref[s + 1] = run;
+      }
+      if (lane == 0) s_fpref[0] = 0;
+      __syncwarp();
+    }
+    const long long n_items = p.fast ? (long long)s_fpref[S] : p.plan->n[kListRow];
     const long long *row_end = p.list_end + (size_t)kListRow * S;
     unsigned long long *counter = p.fast ? p.fast_work : &p.plan->counter[kListRow];
     uint32_t g = 0, seq = 0;  // stages issued, descriptors written
@@ -182,34 +261,33 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       if (item >= n_items) {
         d.done = 1;
       } else if (p.fast) {
-        // decode-only batch, no planner: item = (request, kv head, split),
-        // a row group's splits consecutive, so that they finish close
-        // together and their merges spread over the whole launch
-        const int grp = (int)(item / p.fast_nsmax);
-        d.split = (int)(item % p.fast_nsmax);
-        s = grp / Hk;
-        d.kvh = grp % Hk;
+        // decode-only batch, no planner: item -> (request, kv head, split)
+        int lo = 0, hi = S - 1;
+        while (lo < hi) {  // the request whose items include `item`
+          const int mid = (lo + hi + 1) >> 1;
+          if (s_fpref[mid] <= item) lo = mid; else hi = mid - 1;
+        }
+        s = lo;
+        const int local = (int)(item - s_fpref[s]);
+        const int w = fast_work(p, s);
         d.tok = s;
         d.i = 0;
-        const int ctx = __ldg(p.seq_lens + s);
-        const bool qok = __ldg(p.qsl + s) == s && __ldg(p.qsl + s + 1) == s + 1;
-        const bool cok = ctx >= 1 && ctx <= p.max_seq_len &&
-                         ceil_div_ll(ctx, bs) <= (long long)p.max_blocks_per_seq;
-        if (!qok || !cok) {
-          if (d.split != 0) continue;  // split 0 zeroes the request's row
-          if (lane == 0) atomicOr(p.status, qok ? PA_DEV_BAD_SEQLEN : PA_DEV_BAD_QSL);
+        if (w < 0) {
+          // bad metadata: one item per KV head zeroes its heads of row s
+          d.kvh = local;
+          d.split = 0;
+          if (local == 0 && lane == 0) atomicOr(p.status, fast_bad_bits(p, s));
           inval = 1;
           d.direct = 1;
         } else {
+          const int ctx = __ldg(p.seq_lens + s);
+          const int nsplit = (int)ceil_div_ll(w, fL);
+          d.kvh = local / nsplit;
+          d.split = local % nsplit;
           d.qpos = ctx - 1;
           d.mask_lo = window_lo(d.qpos, p.window);
-          const int kv_base = d.mask_lo & ~15;
-          const int L = p.fast_split;
-          const int nsplit = (int)ceil_div_ll(ctx - kv_base, L);
-          if (d.split >= nsplit) continue;
-          const int s_lo = kv_base + d.split * L;
-          d.kv_hi = min(d.qpos + 1, s_lo + L);
-          if (max(s_lo, d.mask_lo) >= d.kv_hi) continue;
+          const int s_lo = (d.mask_lo & ~15) + d.split * fL;
+          d.kv_hi = min(d.qpos + 1, s_lo + fL);
           d.kv_lo = max(s_lo, d.mask_lo & ~15);
           d.direct = nsplit == 1;
           d.nsplit = p.fast_nsmax;  // the stride between a head's partial rows
@@ -339,13 +417,22 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
   // that finishes a row group's last split merges its splits (log-sum-exp,
   // the sink joining the denominator) into the output and clears the count.
   auto fast_finish = [&](const MmaRowDesc &x) {
-    __threadfence();
-    named_sync(1, 128);
+    named_sync(1, 128);  // every partial row of this block written
     const size_t grp = (size_t)x.tok * p.num_kv_heads + x.kvh;
-    if (tid == 0) s_last = atomicAdd(p.fast_cnt + grp, 1u) == (unsigned)x.nmerge - 1 ? 1 : 0;
+    if (tid == 0) {
+      // One acquire-release count at GPU scope: it publishes this block's
+      // partial rows (ordered before it by the barrier) and, for the block
+      // that counts last, makes every other block's rows visible to the merge
+      // below (the barrier after it passes that on to the other threads).
+      unsigned old;
+      asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], 1;"
+                   : "=r"(old)
+                   : "l"(p.fast_cnt + grp)
+                   : "memory");
+      s_last = old == (unsigned)x.nmerge - 1 ? 1 : 0;
+    }
     named_sync(1, 128);
     if (!s_last) return;
-    __threadfence();
     float *s_wt = s_o;             // [G][64] merge weights of the splits
     float *s_iv = s_o + G * 64;    // [G] reciprocal denominators (0: the row is zero)
     const long long row0 = ((long long)x.tok * H + x.kvh * G) * p.fast_nsmax;

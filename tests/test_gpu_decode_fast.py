@@ -1,10 +1,11 @@
-"""Decode-only batches declared with max_query_len == 1 (pa_forward_ex): on
-small batches, one row-kernel launch that sizes its own KV splits and merges
-a row's splits in the thread block that finishes last (larger batches keep
-the planned path, which the same calls check too).  Checked against the fp64 oracle on the
-decode workloads, with the model variants, both layouts, every GQA group the
-row kernel takes, repeated and graph-replayed calls (the split counters must
-return to zero), and bad metadata."""
+"""Decode-only batches declared with max_query_len == 1 (pa_forward_ex): up to
+1024 requests, one row-kernel launch that sizes the KV splits from seq_lens
+and merges a row's splits in the thread block that finishes last (more
+requests, fp32, or a looser bound keep the planned path, which the same
+calls check too).  Checked against the fp64 oracle on the decode workloads,
+with the model variants, both layouts, every GQA group the row kernel
+takes, split counts up to the 64 a row allows, repeated and graph-replayed
+calls (the split counters must return to zero), and bad metadata."""
 import numpy as np
 import pytest
 import torch
@@ -135,3 +136,54 @@ def test_fp32_and_mixed_batches_take_the_planned_path():
     b = inputs.paged_batch([1, 30, 1], [500, 64, 40], 32, 8, 128, 16, dtype="bf16", seed=38)
     got = parity.gpu_forward(b, max_query_len=30)
     parity.compare(got, parity.oracle_forward(b), "bf16", what="bound 30")
+
+
+def test_requests_above_the_bound_are_bad_metadata():
+    """A request with more new tokens than max_query_len is flagged
+    PA_DEV_BAD_QLEN and its rows are zeros; the others stay exact (planned
+    path: decode-only bound on a batch with one 3-token request, whose tile
+    launch is skipped; and a bound of 30 on a batch with a 40-token extend)."""
+    ctx = [300 + 37 * k for k in range(64)]
+    q_lens = [1] * 64
+    q_lens[40] = 3
+    b = inputs.paged_batch(q_lens, ctx, 32, 8, 128, 16, dtype="bf16", seed=39)
+    want = parity.oracle_forward(b)
+    got = parity.gpu_forward(b, max_query_len=1, expect_status=pa.PA_DEV_BAD_QLEN)
+    qsl = b.query_start_loc.numpy()
+    bad = np.arange(qsl[40], qsl[41])
+    keep = np.setdiff1d(np.arange(b.num_tokens), bad)
+    assert np.all(got[bad] == 0.0)
+    parity.compare(got[keep], want[keep], "bf16", what="bound 1, healthy rows")
+    b = inputs.paged_batch([1, 40, 12, 1], [500, 900, 64, 40], 32, 8, 128, 16, dtype="bf16",
+                           seed=40)
+    want = parity.oracle_forward(b)
+    got = parity.gpu_forward(b, max_query_len=30, expect_status=pa.PA_DEV_BAD_QLEN)
+    qsl = b.query_start_loc.numpy()
+    bad = np.arange(qsl[1], qsl[2])
+    keep = np.setdiff1d(np.arange(b.num_tokens), bad)
+    assert np.all(got[bad] == 0.0)
+    parity.compare(got[keep], want[keep], "bf16", what="bound 30, healthy rows")
+
+
+def test_large_batch_one_launch():
+    """300 requests x 8 KV heads (more row groups than resident blocks)."""
+    rng = np.random.default_rng(41)
+    ctx = [int(x) for x in rng.integers(1, 6000, 300)]
+    b = inputs.paged_batch([1] * 300, ctx, 32, 8, 128, 16, dtype="bf16", seed=41)
+    parity.compare(fast(b), parity.oracle_forward(b), "bf16", what="fast 300 requests")
+
+
+def test_up_to_64_splits_a_row():
+    """kv_split_tokens 1024 on a 60K context: 59 splits, merged in-kernel."""
+    b = inputs.paged_batch([1] * 3, [60000, 100, 33000], 16, 2, 128, 64, dtype="bf16", seed=42)
+    parity.compare(fast(b, kv_split_tokens=1024), parity.oracle_forward(b), "bf16",
+                   what="fast 59 splits")
+
+
+@pytest.mark.parametrize("n", [1024, 1025])
+def test_request_count_bound(n):
+    """1024 requests run as one launch, 1025 on the planned path."""
+    rng = np.random.default_rng(n)
+    ctx = [int(x) for x in rng.integers(1, 300, n)]
+    b = inputs.paged_batch([1] * n, ctx, 8, 2, 64, 16, dtype="bf16", seed=n)
+    parity.compare(fast(b), parity.oracle_forward(b), "bf16", what=f"fast {n} requests")
