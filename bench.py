@@ -343,24 +343,27 @@ def secondary_workloads(pa, flush, peaks):
     hb = inputs.llama_decode(1, poison=False)
     b = pa.to_device(hb)
     out = torch.empty_like(b.q)
+    # declared decode-only (max_query_len = 1, as the headline): one launch
+    fn1 = lambda: pa.forward(b, out=out, max_query_len=1)  # noqa: E731
     for _ in range(5):
-        pa.forward(b, out=out)
-    ms = time_per_step(lambda: pa.forward(b, out=out), 50, flush)
+        fn1()
+    ms = time_per_step(fn1, 50, flush)
     gbs = kv_bytes(hb) / ms / 1e6
     res["llama_decode_b1"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm,
-                              "note": "2 MB of KV: launch-latency bound"}
-    try:  # the same step replayed from a CUDA graph (20 steps per graph)
+                              "note": "2 MB of KV: latency bound; pa_forward_ex with "
+                                      "max_query_len = 1, one kernel launch per call"}
+    # the same call without the declaration: planner, row and merge launches
+    fn0 = lambda: pa.forward(b, out=out)  # noqa: E731
+    for _ in range(5):
+        fn0()
+    ms0 = time_per_step(fn0, 50, flush)
+    res["llama_decode_b1"]["undeclared"] = {"ms": ms0, "kv_gbs": kv_bytes(hb) / ms0 / 1e6,
+                                            "note": "max_query_len = 0: planned path"}
+    try:  # the undeclared step replayed from a CUDA graph (20 steps per graph)
         gms = graph_step_ms(pa, b, out)
         res["llama_decode_b1"]["graph_replay"] = {"ms": gms, "kv_gbs": kv_bytes(hb) / gms / 1e6}
     except Exception as e:  # report, never abort the benchmark
         res["llama_decode_b1"]["graph_replay"] = {"error": str(e)[:200]}
-    # the same step declared decode-only (max_query_len = 1): one kernel launch
-    fn1 = lambda: pa.forward(b, out=out, max_query_len=1)  # noqa: E731
-    for _ in range(5):
-        fn1()
-    ms1 = time_per_step(fn1, 50, flush)
-    res["llama_decode_b1"]["one_launch"] = {"ms": ms1, "kv_gbs": kv_bytes(hb) / ms1 / 1e6,
-                                            "note": "pa_forward_ex with max_query_len = 1"}
     del b, out
 
     # the headline decode batch with NHD and with head-major (HND) caches

@@ -786,8 +786,8 @@ bool fast_decode_plan(const FwdCall &c, int num_sms, FastPlan *f) {
   if (!row_mma_supported(c.dtype, c.head_dim, group)) return false;
   const long long msl = c.max_seq_len > 0 ? c.max_seq_len : 1;
   if (msl > 64ll * kRowMaxSplit) return false;
-  // splits are at least kRowMinSplit long (or kv_split_tokens, if shorter)
-  long long nsmax = ceil_div_h(msl, kRowMinSplit);
+  // splits are at least kFastMinSplit long (or kv_split_tokens, if shorter)
+  long long nsmax = ceil_div_h(msl, kFastMinSplit);
   if (c.kv_split_tokens > 0) nsmax = std::max(nsmax, ceil_div_h(msl, c.kv_split_tokens));
   if (nsmax > 64) {
     if (c.kv_split_tokens > 0) return false;  // the requested splits are too short

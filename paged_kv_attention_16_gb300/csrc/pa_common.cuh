@@ -147,6 +147,7 @@ constexpr int kRowMinSplit = 256;
 // Decode-only batches run as one row-kernel launch up to this many requests
 // (the kernel keeps one prefix entry per request in shared memory).
 constexpr int kFastMaxSeqs = 1024;
+constexpr int kFastMinSplit = 64;  // their shortest split: one row-kernel stage
 // Rows per tensor-core tile of the extend/prefill kernel.
 constexpr int kTileRows = 128;
 

@@ -216,12 +216,12 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
         wmax = max(wmax, __shfl_xor_sync(0xffffffffu, wmax, o));
       }
       const long long target = (G >= 8 ? 4ll : 8ll) * gridDim.x;
+      // (down to one 64-position stage: on a small batch one block streams
+      // only some tens of GB/s, so a short row still gains from its splits)
       long long L = ceil_div_ll(ceil_div_ll(wsum * Hk, target), 64) * 64;
-      L = max(L, (long long)kRowMinSplit);
+      L = max(L, (long long)kFastMinSplit);
       L = max(L, ceil_div_ll(ceil_div_ll(wmax, p.fast_nsmax), 64) * 64);
       L = min(L, (long long)kRowMaxSplit);
-      // rows of at most 1024 positions are not split: a merge costs more than it saves
-      if (wmax <= 1024) L = max(64ll, ceil_div_ll(wmax, 64) * 64);
       if (p.kv_split_tokens > 0 && p.kv_split_tokens < L) L = p.kv_split_tokens;
       fL = (int)L;
       // item counts: lane l takes a contiguous run of requests, an exclusive
@@ -252,10 +252,15 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
     const long long *row_end = p.list_end + (size_t)kListRow * S;
     unsigned long long *counter = p.fast ? p.fast_work : &p.plan->counter[kListRow];
     uint32_t g = 0, seq = 0;  // stages issued, descriptors written
+    // Block b's first item is b (no round trip to the counter); the counter
+    // hands out the rest, from gridDim.x on.
+    bool first = true;
     for (;;) {
       long long item = 0;
-      if (lane == 0) item = (long long)atomicAdd(counter, 1ull);
+      if (lane == 0)
+        item = first ? (long long)blockIdx.x : (long long)gridDim.x + (long long)atomicAdd(counter, 1ull);
       item = __shfl_sync(0xffffffffu, item, 0);
+      first = false;
       MmaRowDesc d{};
       int npages = 0, pfirst = 0, s = 0, inval = 0;
       if (item >= n_items) {
