@@ -357,6 +357,13 @@ __device__ inline float fast_exp2(float x) {
 
 // Packed two-lane fp32 FMA (one instruction, two IEEE fma results):
 // returns {a0 * b0 + c0, a1 * b1 + c1}.
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ inline float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
 __device__ inline void ffma2(float &c0, float &c1, float a0, float a1, float b0, float b1) {
   asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
       "mov.b64 ra, {%2, %3};\n\t"

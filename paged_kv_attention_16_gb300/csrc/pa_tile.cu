@@ -504,7 +504,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
 #pragma unroll
             for (int c = 0; c < 8; ++c) mxa[c] = x[c];
 #pragma unroll
-            for (int c = 8; c < kBN; ++c) mxa[c & 7] = fmaxf(mxa[c & 7], x[c]);
+            for (int c = 8; c < kBN; c += 2) mxa[(c >> 1) & 7] = fmax3(mxa[(c >> 1) & 7], x[c], x[c + 1]);
           };
           float sv[kOnePass ? kBN : 1];  // the scores, held in one-pass mode
           if constexpr (kOnePass) {
@@ -515,8 +515,8 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
             scores(x);
             row_max(x);
           }
-          float mx = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+          float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
+                           fmaxf(mxa[6], mxa[7]));
           if (fold && mx != -INFINITY) mx *= c2;
           float alpha = 1.f;
           bool rescale = false;
@@ -553,9 +553,12 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
               uint32_t pw[16];
 #pragma unroll
               for (int w = 0; w < 16; ++w) {
-                const float p0 = fast_exp2(fmaf(x[c0 + 2 * w], cs, -mu));
-                const float p1 = fast_exp2(fmaf(x[c0 + 2 * w + 1], cs, -mu));
-                suma[w & 7] += p0 + p1;
+                // packed (f32x2) multiply-adds: half the issue slots of the
+                // scalar ones, on a loop that is issue-bound
+                float a0 = -mu, a1 = -mu;
+                ffma2(a0, a1, x[c0 + 2 * w], x[c0 + 2 * w + 1], cs, cs);
+                const float p0 = fast_exp2(a0), p1 = fast_exp2(a1);
+                ffma2(suma[2 * (w & 3)], suma[2 * (w & 3) + 1], p0, p1, 1.f, 1.f);
                 const __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
                 pw[w] = *reinterpret_cast<const uint32_t *>(&h2);
               }
