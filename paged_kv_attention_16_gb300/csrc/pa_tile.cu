@@ -468,7 +468,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
           // raw S of this tile -> scaled (and biased) scores, masked to the
           // row's visible range; column c is position base + c
           const bool cross = __any_sync(0xffffffffu, base + kBN > row_hi || base < row_lo);
-          auto scores = [&](float (&x)[kBN]) {
+          auto scores = [&](float (&x)[kBN], bool transformed) {
             {
               uint32_t raw[kBN];
 #pragma unroll
@@ -479,6 +479,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
 #pragma unroll
               for (int c = 0; c < kBN; ++c) x[c] = __uint_as_float(raw[c]);
             }
+            if (transformed) return;  // S already holds the biased, masked scores
             if (!fold) {
               if (p.alibi) {
                 const float dist0 = (float)(qpos - base);
@@ -508,12 +509,21 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
           };
           float sv[kOnePass ? kBN : 1];  // the scores, held in one-pass mode
           if constexpr (kOnePass) {
-            scores(*reinterpret_cast<float(*)[kBN]>(sv));
+            scores(*reinterpret_cast<float(*)[kBN]>(sv), false);
             row_max(*reinterpret_cast<float(*)[kBN]>(sv));
           } else {
             float x[kBN];
-            scores(x);
+            scores(x, false);
             row_max(x);
+            if (!fold) {
+              // a bias (or a scale that cannot fold) costs per score: store
+              // the finished scores over S so the second read skips it
+#pragma unroll
+              for (int c0 = 0; c0 < kBN; c0 += 32)
+                tc_st32(tmem + lane_off + kTmemS + pb * kBN + c0,
+                        *reinterpret_cast<const uint32_t(*)[32]>(x + c0));
+              tc_wait_st();
+            }
           }
           float mx = fmax3(fmax3(mxa[0], mxa[1], mxa[2]), fmax3(mxa[3], mxa[4], mxa[5]),
                            fmaxf(mxa[6], mxa[7]));
@@ -569,7 +579,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
             weights(*reinterpret_cast<const float(*)[kBN]>(sv));
           } else {
             float x[kBN];
-            scores(x);
+            scores(x, !fold);
             weights(x);
           }
           tc_wait_st();
