@@ -351,7 +351,19 @@ def secondary_workloads(pa, flush, peaks):
     gbs = kv_bytes(hb) / ms / 1e6
     res["llama_decode_b1"] = {"ms": ms, "kv_gbs": gbs, "hbm_frac": gbs / hbm,
                               "note": "2 MB of KV: latency bound; pa_forward_ex with "
-                                      "max_query_len = 1, one kernel launch per call"}
+                                      "max_query_len = 1, one kernel launch per call; "
+                                      "L2 flushed before each call"}
+    # the same calls back to back (the host enqueues while the device runs):
+    # per-call time of a stream of single-step calls, caches warm
+    st = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(st)
+    for _ in range(200):
+        fn1()
+    e1.record(st)
+    e1.synchronize()
+    res["llama_decode_b1"]["back_to_back_ms"] = e0.elapsed_time(e1) / 200
     # the same call without the declaration: planner, row and merge launches
     fn0 = lambda: pa.forward(b, out=out)  # noqa: E731
     for _ in range(5):

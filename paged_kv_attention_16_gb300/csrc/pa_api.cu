@@ -18,6 +18,7 @@
 // "vLLM AMD ROCm attention backend optimisation", section "Chunked context
 // processing": LSE-based merge): out = sum_p w_p O_p with
 // w_p = 2^(lse_p - M) / sum_q 2^(lse_q - M), M = max_p lse_p (base 2).
+#include <algorithm>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -536,6 +537,12 @@ struct DeviceState {
   // then one split count per (request, kv head); all zero between calls
   unsigned long long *fast_ctr = nullptr;
   size_t fast_groups = 0;
+  // the row kernel's K / V tensor maps of the last decode-only call (a
+  // serving loop calls with the same caches: encoding them is host time)
+  bool maps_valid = false;
+  const void *maps_k = nullptr, *maps_v = nullptr;
+  int maps_key[6] = {0, 0, 0, 0, 0, 0};
+  CUtensorMap map_k, map_v;
 };
 
 std::mutex g_mu;
@@ -821,9 +828,12 @@ bool encode_row_maps(const FwdCall &c, CUtensorMap *tm_k, CUtensorMap *tm_v) {
          encode_tiled(tm_v, c.v_cache, c.dtype, 5, dims, strides, box, true);
 }
 
-pa_status fast_decode_launch(const FwdCall &c, const FastPlan &f, void *workspace,
-                             unsigned int *status, unsigned long long *fast_ctr, int num_sms,
+pa_status fast_decode_launch(const FwdCall &c, const FastPlan &f, DeviceState *d,
                              cudaStream_t st) {
+  void *workspace = d->ws;
+  unsigned int *status = d->status;
+  unsigned long long *fast_ctr = d->fast_ctr;
+  const int num_sms = d->num_sms;
   const int group = c.num_heads / c.num_kv_heads;
   uint8_t *ws = reinterpret_cast<uint8_t *>(workspace);
   FwdParams p{};
@@ -859,7 +869,24 @@ pa_status fast_decode_launch(const FwdCall &c, const FastPlan &f, void *workspac
   p.fast_work = fast_ctr;
   p.fast_cnt = reinterpret_cast<unsigned int *>(fast_ctr + 2);
   CUtensorMap tm_k, tm_v;
-  if (!encode_row_maps(c, &tm_k, &tm_v)) return PA_ERR_CUDA;
+  {
+    const int key[6] = {c.dtype, c.kv_layout, c.num_blocks, c.block_size, c.num_kv_heads,
+                        c.head_dim};
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (d->maps_valid && d->maps_k == c.k_cache && d->maps_v == c.v_cache &&
+        std::equal(key, key + 6, d->maps_key)) {
+      tm_k = d->map_k;
+      tm_v = d->map_v;
+    } else {
+      if (!encode_row_maps(c, &tm_k, &tm_v)) return PA_ERR_CUDA;
+      d->map_k = tm_k;
+      d->map_v = tm_v;
+      d->maps_k = c.k_cache;
+      d->maps_v = c.v_cache;
+      std::copy(key, key + 6, d->maps_key);
+      d->maps_valid = true;
+    }
+  }
   const int row_ctas = row_ctas_per_sm_cached(c.dtype, c.head_dim, group) * num_sms;
   p.row_ctas = row_ctas;
   const int slot = prof_begin(PA_K_ROW, st);
@@ -1199,7 +1226,7 @@ pa_status pa_forward_ex(const void *q, const void *k_cache, const void *v_cache,
     if (s != PA_OK) return s;
     s = ensure_fast_counters(d, (size_t)c.num_seqs * c.num_kv_heads, st);
     if (s != PA_OK) return s;
-    return fast_decode_launch(c, fp, d->ws, d->status, d->fast_ctr, d->num_sms, st);
+    return fast_decode_launch(c, fp, d, st);
   }
   s = ensure_workspace(d, fwd_workspace_bytes(c), st);
   if (s != PA_OK) return s;

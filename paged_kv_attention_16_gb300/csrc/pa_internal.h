@@ -2,9 +2,28 @@
 // libpa.so (not part of the public C ABI).
 #pragma once
 
+#include <atomic>
+
 #include "pa_common.cuh"
 
 namespace pa {
+
+// A kernel's launch attributes (dynamic shared memory size, carveout) are
+// per device: set them on the kernel's first launch on each device only
+// (each cudaFuncSetAttribute costs host time on every call otherwise).
+template <typename Kernel>
+cudaError_t set_smem_attrs_once(Kernel kernel, int smem, std::atomic<unsigned long long> &done) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const unsigned long long bit = dev < 64 ? 1ull << dev : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Launches `kernel` with programmatic stream serialization: its CTAs may be
 // scheduled while the previous kernel of the stream drains.  The kernel must

@@ -257,8 +257,12 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
     bool first = true;
     for (;;) {
       long long item = 0;
+      // (when the items fit the grid, every item is some block's first and
+      // the counter is never touched)
       if (lane == 0)
-        item = first ? (long long)blockIdx.x : (long long)gridDim.x + (long long)atomicAdd(counter, 1ull);
+        item = first ? (long long)blockIdx.x
+               : n_items <= (long long)gridDim.x ? n_items
+                                                 : (long long)gridDim.x + (long long)atomicAdd(counter, 1ull);
       item = __shfl_sync(0xffffffffu, item, 0);
       first = false;
       MmaRowDesc d{};
@@ -347,7 +351,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       }
       ++seq;
       if (d.done) {
-        if (p.fast && lane == 0) {
+        if (p.fast && lane == 0 && n_items > (long long)gridDim.x) {
           // the last block to stop taking items resets the counters
           __threadfence();
           if (atomicAdd(p.fast_work + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
@@ -441,6 +445,22 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
     float *s_wt = s_o;             // [G][64] merge weights of the splits
     float *s_iv = s_o + G * 64;    // [G] reciprocal denominators (0: the row is zero)
     const long long row0 = ((long long)x.tok * H + x.kvh * G) * p.fast_nsmax;
+    // The first eight splits' partial values of this thread's elements,
+    // loaded now: their latency overlaps the weights' (a short row is one
+    // round trip, not two).
+    constexpr int EPT = (G * D + 127) / 128;  // elements per thread
+    constexpr bool kPre = EPT <= 4;
+    float pre[kPre ? EPT : 1][8];
+    if constexpr (kPre) {
+#pragma unroll
+      for (int k = 0; k < EPT; ++k) {
+        const int e = tid + 128 * k;
+        const bool in = e < G * D;
+        const float *src = p.part_o + (row0 + (long long)(e / D) * p.fast_nsmax) * D + e % D;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pre[k][u] = in && u < x.nmerge ? __ldcg(src + (size_t)u * D) : 0.f;
+      }
+    }
     // one warp per head: lane q holds split q's log-sum-exp (two when a row
     // has more than 32 splits)
     for (int hh = warp; hh < G; hh += C::NWARP) {
@@ -470,14 +490,22 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
     named_sync(1, 128);
     // the partial rows, eight splits at a time (independent loads)
     __nv_bfloat16 *dst = reinterpret_cast<__nv_bfloat16 *>(p.out) + ((size_t)x.tok * H + x.kvh * G) * D;
-    for (int e = tid; e < G * D; e += 128) {
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+      const int e = tid + 128 * k;
+      if (e >= G * D) break;
       const int h = e / D, dd = e % D;
       const float *src = p.part_o + (row0 + (long long)h * p.fast_nsmax) * D + dd;
       float acc = 0.f;
       for (int q0 = 0; q0 < x.nmerge; q0 += 8) {
         float pv[8];
+        if (kPre && q0 == 0) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) pv[u] = q0 + u < x.nmerge ? __ldcg(src + (size_t)(q0 + u) * D) : 0.f;
+          for (int u = 0; u < 8; ++u) pv[u] = pre[kPre ? k : 0][u];
+        } else {
+#pragma unroll
+          for (int u = 0; u < 8; ++u) pv[u] = q0 + u < x.nmerge ? __ldcg(src + (size_t)(q0 + u) * D) : 0.f;
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
           if (q0 + u < x.nmerge) acc = fmaf(s_wt[h * 64 + q0 + u], pv[u], acc);
@@ -704,11 +732,8 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
 template <int D, int G>
 cudaError_t set_attrs() {
   using C = MmaRowCfg<D, G>;
-  cudaError_t e = cudaFuncSetAttribute(row_mma_kernel<D, G>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(row_mma_kernel<D, G>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                              cudaSharedmemCarveoutMaxShared);
+  static std::atomic<unsigned long long> done{0};
+  return set_smem_attrs_once(row_mma_kernel<D, G>, C::SMEM, done);
 }
 
 template <typename Fn>

@@ -676,10 +676,8 @@ cudaError_t launch_v(const FwdParams &p, const CUtensorMap &tq, const CUtensorMa
                      cudaStream_t stream) {
   using C = TileCfg<DQK, DV>;
   auto kern = tile_kernel<DQK, DV, PB64>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = set_smem_attrs_once(kern, C::SMEM, done);
   if (e != cudaSuccess) return e;
   return launch_dependent(kern, dim3(num_sms * 2), dim3(C::THREADS), C::SMEM,
                           stream, tq, tk, tv, tkr, p);

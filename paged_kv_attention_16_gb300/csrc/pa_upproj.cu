@@ -309,11 +309,8 @@ cudaError_t launch_upproj(const UpprojArgs &a, const void *kv_cache, const void 
   if (!encode_tiled(&tm_c, kv_cache, PA_BF16, 3, cd, cs, cb, true) ||
       !encode_tiled(&tm_w, w_kv, PA_BF16, 2, wd, ws, wb, true))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(upproj_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       UP_SMEM);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(upproj_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
+  static std::atomic<unsigned long long> done{0};
+  const cudaError_t e = set_smem_attrs_once(upproj_kernel, UP_SMEM, done);
   if (e != cudaSuccess) return e;
   return launch_dependent(upproj_kernel, dim3(num_sms), dim3(kUpThreads), UP_SMEM, stream, tm_c,
                           tm_w, a);

@@ -128,12 +128,35 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _stream_ptr(stream):
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream_ptr(stream, device=None):
+    """The cudaStream_t to launch on: `stream`, else the current stream of
+    `device` (the raw query costs a fraction of torch.cuda.current_stream(),
+    which builds a Python object per call)."""
     if stream is None:
+        if _raw_stream is not None and device is not None and device >= 0:
+            return _raw_stream(device)
         return torch.cuda.current_stream().cuda_stream
     if isinstance(stream, int):
         return stream
     return stream.cuda_stream
+
+
+_options_cache = {}
+
+
+def _forward_options(sinks, layout, sliding_window, alibi_slopes, alibi_sqrt, max_query_len):
+    """A pa_forward_options struct, reused for a repeated set of options."""
+    key = (_ptr(sinks), layout, int(sliding_window), _ptr(alibi_slopes), int(bool(alibi_sqrt)),
+           int(max_query_len))
+    opts = _options_cache.get(key)
+    if opts is None:
+        if len(_options_cache) > 256:
+            _options_cache.clear()
+        opts = _options_cache[key] = ForwardOptions(*key)
+    return opts
 
 
 def _dtype_code(t):
@@ -162,8 +185,8 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
     args = (
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
         _ptr(query_start_loc), int(num_heads), int(num_kv_heads), int(head_dim),
-        int(block_size), float(scale), _ptr(out), _stream_ptr(stream), _dtype_code(q),
-        int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
+        int(block_size), float(scale), _ptr(out), _stream_ptr(stream, q.get_device()),
+        _dtype_code(q), int(seq_lens.shape[0]), int(q.shape[0]), int(block_table.shape[1]),
         int(num_blocks if num_blocks is not None else k_cache.shape[0]), int(max_seq_len),
         int(kv_split_tokens))
     if (sinks is None and layout == PA_KV_NHD and not sliding_window
@@ -174,8 +197,8 @@ def pa_forward(q, k_cache, v_cache, block_table, seq_lens, query_start_loc, num_
             if isinstance(t, torch.Tensor) and (t.dtype != torch.float32
                                                 or t.numel() != num_heads):
                 raise TypeError(f"{name} must be a float32 tensor of num_heads elements")
-        opts = ForwardOptions(_ptr(sinks), layout, int(sliding_window), _ptr(alibi_slopes),
-                              int(bool(alibi_sqrt)), int(max_query_len))
+        opts = _forward_options(sinks, layout, sliding_window, alibi_slopes, alibi_sqrt,
+                                max_query_len)
         st, where = lib().pa_forward_ex(*args, ctypes.byref(opts)), "pa_forward_ex"
     if check:
         _check(st, where)
