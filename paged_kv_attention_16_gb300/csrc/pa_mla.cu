@@ -41,7 +41,6 @@ constexpr int kSoftWarps = 8;       // two per TMEM lane quarter: each thread ha
 constexpr int kSoftThreads = 32 * kSoftWarps;
 constexpr int kProducerWarp = kSoftWarps, kMmaWarp = kSoftWarps + 1;
 constexpr int kMlaThreads = 32 * (kSoftWarps + 2);
-constexpr int kPrefetchTiles = 4;   // KV tiles brought into L2 ahead of the ring
 constexpr int kMlaStages = 4;
 constexpr int kChunkKV = kMN * 128; // one 64-column chunk of a tile: 64 rows x 128 B
 constexpr int kMaxChunks = 5;
@@ -253,9 +252,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------- producer
     // The whole warp walks the pieces (the page caches are warp-wide); lanes
-    // 0 and 1 handle the two 32-slot halves of each tile, lane 0 waits.  A
-    // second cursor brings the tile kPrefetchTiles ahead into L2, so that a
-    // ring load, issued once its stage is free, is served from L2.
+    // 0 and 1 handle the two 32-slot halves of each tile, lane 0 waits.  (An
+    // L2 prefetch of the tile four ahead measured 1.5 % slower: the
+    // prefetch copies take this warp's issue time too.)
     uint32_t tiles = 0;
     PieceWalk walk;
     walk.start(a, cluster, nclusters);
@@ -264,32 +263,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMlaThreads, 1)
       const int s = pc_.s, kv_lo = pc_.kv_lo, kv_hi = pc_.kv_hi;
       const int nt = (kv_hi - kv_lo + kMN - 1) / kMN;
       const int32_t *bt = a.block_table + (size_t)s * a.max_blocks_per_seq;
-      PageCache pc, pf;
+      PageCache pc;
       pc.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
-      pf.start(bt, a.max_blocks_per_seq, kv_lo / bs, lane);
       // A tile's rows: with page_tiles, one box of 4 latent chunks x 64 slots
       // (whole 512-byte row spans, so the copy engine moves few large pieces)
       // plus, on CTA 0, one box for the rope chunk; otherwise one 64-column x
       // 32-slot box per chunk and half tile (lanes 0 and 1).
       const bool big = a.page_tiles != 0;
       const int c4 = rank == 0 ? 0 : 4;  // first latent chunk of this CTA
-      auto prefetch = [&](int j) {
-        const int pos = kv_lo + j * kMN + lane * kMHalf;
-        const bool need = (big ? lane == 0 : lane < 2) && j < nt && pos < kv_hi;
-        const int page = pf.get(need ? pos / bs : -1, lane);
-        if (need && page >= 0 && page < a.num_blocks) {
-          if (big) {
-            tma_prefetch_4d(&tm_kv4, 0, pos % bs, c4, page);
-            if (rank == 0) tma_prefetch_3d(&tm_kv, 8 * 64, pos % bs, page);
-          } else {
-            for (int i = 0; i < nch; ++i)
-              tma_prefetch_3d(&tm_kv, chunk_of(rank, i) * 64, pos % bs, page);
-          }
-        }
-      };
-      for (int j = 0; j < kPrefetchTiles; ++j) prefetch(j);
       for (int j = 0; j < nt; ++j) {
-        prefetch(j + kPrefetchTiles);
         const uint32_t g = tiles + j;
         const int st = g % kMlaStages;
         const int pos = kv_lo + j * kMN + lane * kMHalf;
