@@ -275,13 +275,18 @@ def max_over_ranks(x, world):
     return float(t.item())
 
 
-def time_per_step(fn, steps, flush):
+def time_per_step(fn, steps, flush, settle=False):
     """Median device time of `steps` calls, each timed with events on the
-    current stream, with an L2 flush (outside the events) between calls."""
+    current stream, with an L2 flush (outside the events) between calls.
+    settle: the device also spins for about 0.25 ms after the flush, so the
+    host has enqueued the whole call before the device reaches it (per-kernel
+    event brackets then hold device time only, not the host's launch work)."""
     st = torch.cuda.current_stream()
     times = []
     for _ in range(steps):
         flush.zero_()
+        if settle:
+            torch.cuda._sleep(500_000)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(st)
         fn()
@@ -297,7 +302,7 @@ def plain_and_profiled(pa, fn, steps, flush):
     ms = time_per_step(fn, steps, flush)
     pa.pa_profile_enable(True)
     pa.pa_profile_read()
-    time_per_step(fn, steps, flush)
+    time_per_step(fn, steps, flush, settle=True)
     prof = pa.pa_profile_read()
     pa.pa_profile_enable(False)
     return ms, {k: v[0] / v[1] for k, v in prof.items()}

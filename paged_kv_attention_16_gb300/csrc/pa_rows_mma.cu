@@ -58,11 +58,12 @@ struct MmaRowCfg {
   static constexpr int STAGE_BYTES = 2 * KV_BYTES;
   static constexpr int KS = D / 16;                  // k-steps of S = Q K^T
   static constexpr int NT = D / 8;                   // n-tiles of O
-  static constexpr int SCR_BYTES = NWARP * G * D * 4;
+  static constexpr int NSLOT = 2;                    // merge scratch slots
+  static constexpr int SCR_BYTES = NSLOT * G * D * 4;
   static constexpr int MAX_PAGES = kRowMaxSplit / BOX + 2;
   static constexpr int FPREF_BYTES = (kFastMaxSeqs + 1) * 4;  // decode-only item prefix
   // everything but the ring and the scratch (barriers for up to 6 stages)
-  static constexpr int MISC_BYTES = 2 * NWARP * G * 4 + MAX_PAGES * 4 + 2 * 64 + FPREF_BYTES + 16 * 8 + 16;
+  static constexpr int MISC_BYTES = 2 * NSLOT * G * 4 + MAX_PAGES * 4 + 2 * 64 + FPREF_BYTES + 16 * 8 + 16;
   // two resident CTAs per SM: 228 KB less 1 KB reserved each, less the
   // 1024-byte alignment slack
   static constexpr int NSTAGE0 = (233472 / 2 - 1024 - 1024 - 64 - SCR_BYTES - MISC_BYTES) / STAGE_BYTES;
@@ -70,7 +71,7 @@ struct MmaRowCfg {
   static constexpr int OFF_RING = 0;  // 1024-byte aligned (swizzle atoms)
   static constexpr int OFF_SCR = OFF_RING + NSTAGE * STAGE_BYTES;
   static constexpr int OFF_ML = OFF_SCR + SCR_BYTES;
-  static constexpr int OFF_PAGES = OFF_ML + 2 * NWARP * G * 4;
+  static constexpr int OFF_PAGES = OFF_ML + 2 * NSLOT * G * 4;
   static constexpr int OFF_DESC = OFF_PAGES + MAX_PAGES * 4;
   static constexpr int OFF_FPREF = OFF_DESC + 2 * 64;
   static constexpr int OFF_BAR = (OFF_FPREF + FPREF_BYTES + 15) / 16 * 16;
@@ -157,7 +158,7 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
   uint8_t *ring = smem + C::OFF_RING;
   float *s_o = reinterpret_cast<float *>(smem + C::OFF_SCR);
   float *s_m = reinterpret_cast<float *>(smem + C::OFF_ML);
-  float *s_l = s_m + C::NWARP * G;
+  float *s_l = s_m + C::NSLOT * G;
   int *s_pages = reinterpret_cast<int *>(smem + C::OFF_PAGES);
   MmaRowDesc *s_desc = reinterpret_cast<MmaRowDesc *>(smem + C::OFF_DESC);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
@@ -668,42 +669,73 @@ __global__ void __maxnreg__(168) row_mma_kernel(const __grid_constant__ CUtensor
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
       l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
     }
-    named_sync(1, 128);  // the scratch of the previous item has been read
-    if (gq < G) {
-#pragma unroll
-      for (int n = 0; n < C::NT; ++n)
-        *reinterpret_cast<float2 *>(&s_o[(warp * G + gq) * D + n * 8 + 2 * tq]) =
-            make_float2(o[n][0], o[n][1]);
-      if (tq == 0) {
-        s_m[warp * G + gq] = m_lo;
-        s_l[warp * G + gq] = l_lo;
-      }
-    }
-    if constexpr (G > 8) {
-      if (gq + 8 < G) {
+    // Two slots of scratch: warps 2 and 3 hand their rows to warps 0 and 1,
+    // which fold them in (log-sum-exp) and hand the result on; the output
+    // stage then merges two slots.  (Four slots would cost a ring stage at
+    // G = 8.)
+    auto put = [&](int slot) {
+      if (gq < G) {
 #pragma unroll
         for (int n = 0; n < C::NT; ++n)
-          *reinterpret_cast<float2 *>(&s_o[(warp * G + gq + 8) * D + n * 8 + 2 * tq]) =
-              make_float2(o[n][2], o[n][3]);
+          *reinterpret_cast<float2 *>(&s_o[(slot * G + gq) * D + n * 8 + 2 * tq]) =
+              make_float2(o[n][0], o[n][1]);
         if (tq == 0) {
-          s_m[warp * G + gq + 8] = m_hi;
-          s_l[warp * G + gq + 8] = l_hi;
+          s_m[slot * G + gq] = m_lo;
+          s_l[slot * G + gq] = l_lo;
         }
       }
-    }
+      if constexpr (G > 8) {
+        if (gq + 8 < G) {
+#pragma unroll
+          for (int n = 0; n < C::NT; ++n)
+            *reinterpret_cast<float2 *>(&s_o[(slot * G + gq + 8) * D + n * 8 + 2 * tq]) =
+                make_float2(o[n][2], o[n][3]);
+          if (tq == 0) {
+            s_m[slot * G + gq + 8] = m_hi;
+            s_l[slot * G + gq + 8] = l_hi;
+          }
+        }
+      }
+    };
+    // fold slot `slot`'s row `row` (fragment columns c0, c0 + 1 of o) into m, l, o
+    auto fold = [&](int slot, int row, float &m, float &l, int c0) {
+      const float mp = s_m[slot * G + row], lp = s_l[slot * G + row];
+      const float mn = fmaxf(m, mp);
+      const float a = m == -INFINITY ? 0.f : fast_exp2(m - mn);
+      const float b = mp == -INFINITY ? 0.f : fast_exp2(mp - mn);
+      l = l * a + lp * b;
+      m = mn;
+#pragma unroll
+      for (int n = 0; n < C::NT; ++n) {
+        const float2 po = *reinterpret_cast<const float2 *>(&s_o[(slot * G + row) * D + n * 8 + 2 * tq]);
+        o[n][c0] = o[n][c0] * a + po.x * b;
+        o[n][c0 + 1] = o[n][c0 + 1] * a + po.y * b;
+      }
+    };
+    named_sync(1, 128);  // the scratch of the previous item has been read
+    if (warp >= 2) put(warp - 2);
     named_sync(1, 128);
-    // ---- log-sum-exp merge of the four warps, then output or partial
+    if (warp < 2) {
+      if (gq < G) fold(warp, gq, m_lo, l_lo, 0);
+      if constexpr (G > 8) {
+        if (gq + 8 < G) fold(warp, gq + 8, m_hi, l_hi, 2);
+      }
+    }
+    named_sync(1, 128);  // slots read
+    if (warp < 2) put(warp);
+    named_sync(1, 128);
+    // ---- log-sum-exp merge of the two slots, then output or partial
     const int e0 = tid * C::OPT;
     if (e0 < G * D) {
       const int h = e0 / D, d0 = e0 % D;
       float M = -INFINITY;
 #pragma unroll
-      for (int w = 0; w < C::NWARP; ++w) M = fmaxf(M, s_m[w * G + h]);
+      for (int w = 0; w < C::NSLOT; ++w) M = fmaxf(M, s_m[w * G + h]);
       float L = 0.f, acc[C::OPT];
 #pragma unroll
       for (int x = 0; x < C::OPT; ++x) acc[x] = 0.f;
 #pragma unroll
-      for (int w = 0; w < C::NWARP; ++w) {
+      for (int w = 0; w < C::NSLOT; ++w) {
         const float ms = s_m[w * G + h];
         if (ms == -INFINITY) continue;
         const float wt = fast_exp2(ms - M);
