@@ -38,6 +38,12 @@
 //            tile j+1 overlaps the PV product of tile j), and finally
 //            normalises O and stores the row (or a split partial with its
 //            log-sum-exp).
+// Work items are taken from a device counter (block b's first item is b), so a
+// CTA that drew short items takes more of them: the splits of a long request
+// are much longer than its causal tail, and a fixed deal by block index gave
+// every CTA the same split position.  The lead producer thread takes the next
+// item when it needs one and posts it in a small shared-memory ring that the
+// other roles read in order.
 // Tiles of a split that lie past every row's causal bound are never loaded.
 #include "pa_internal.h"
 
@@ -55,6 +61,7 @@ constexpr int kKWarp0 = 4, kMmaWarp = 5, kVWarp = 6, kKWarp1 = 7;
 constexpr int kKStages = 3;        // K tiles in flight per CTA (at most; see TileCfg::KST)
 constexpr int kVStages = 2;        // V tiles in flight per CTA
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
+constexpr int kItemRing = 8;       // work items posted ahead by the lead producer
 // Dynamic shared memory one CTA may take with `ctas` CTAs per SM (228 KB
 // per SM, 1 KB of it reserved per CTA).
 constexpr int tile_smem_budget(int ctas) { return 233472 / ctas - 1024; }
@@ -73,7 +80,10 @@ enum Bar { kQFull = 0, kQFree, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODo
 constexpr int kKFree0 = kKFull0 + kKStages;
 constexpr int kVFull0 = kKFree0 + kKStages;
 constexpr int kVFree0 = kVFull0 + kVStages;
-constexpr int kNumBars = kVFree0 + kVStages;
+// item ring slot x: kItemFull0 + x (posted), kItemFree0 + x (read by every role)
+constexpr int kItemFull0 = kVFree0 + kVStages;
+constexpr int kItemFree0 = kItemFull0 + kItemRing;
+constexpr int kNumBars = kItemFree0 + kItemRing;
 
 // DQK: width of the query / key rows (the S product's K dimension); DV:
 // width of the value / output rows.  They differ for the non-absorbed MLA
@@ -94,7 +104,7 @@ struct TileCfg {
   // (the 192-wide keys), a single producer warp interleaves K and V, and the
   // softmax (168 registers) reads S once and holds it.  (A one-stage V ring
   // gave wrong results on the 192-wide keys and is not used.)
-  static constexpr int TAIL = kNumBars * 8 + 64;
+  static constexpr int TAIL = kNumBars * 8 + 64 + kItemRing * 8;
   static constexpr bool fits(int k, int v) {
     return Q_BYTES + k * K_BYTES + v * V_BYTES + TAIL <= tile_smem_budget(2);
   }
@@ -107,9 +117,15 @@ struct TileCfg {
   static constexpr int OFF_V = OFF_K + KST * K_BYTES;
   static constexpr int OFF_BAR = OFF_V + VST * V_BYTES;
   static constexpr int OFF_MISC = OFF_BAR + kNumBars * 8;
+  static constexpr int OFF_ITEMS = OFF_MISC + 64;
   // no alignment slack: the dynamic window is declared 1024-aligned (and
   // the kernel checks that it is)
-  static constexpr int SMEM = OFF_MISC + 64;
+  static constexpr int SMEM = OFF_ITEMS + kItemRing * 8;
+  static_assert(SMEM == OFF_BAR + TAIL, "shared memory layout");
+  // roles that read each posted item besides the lead producer: the second
+  // K warp (when the keys have two or more 64-wide chunks), the V warp, the
+  // MMA thread and the softmax group; with one producer, the last two
+  static constexpr int ITEM_READERS = SPLIT ? (NHQ >= 2 ? 4 : 3) : 2;
   static_assert(fits(KST, VST), "shared memory budget");
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, DV, 1);
@@ -174,6 +190,8 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
   uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(smem + C::OFF_MISC);
   int *s_bad = reinterpret_cast<int *>(smem + C::OFF_MISC + 16);
+  volatile long long *s_cur = reinterpret_cast<long long *>(smem + C::OFF_MISC + 32);
+  volatile long long *s_items = reinterpret_cast<long long *>(smem + C::OFF_ITEMS);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = p.num_heads / p.num_kv_heads;
@@ -195,7 +213,8 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
     if (p.k_rope_split) prefetch_tensor_map(&tm_kr);
     for (int b = 0; b < kNumBars; ++b) {
       const bool per_warp = b == kPFull0 || b == kPFull1 || b == kOFree;
-      mbar_init(&bar[b], per_warp ? 4 : 1);
+      const bool item_free = b >= kItemFree0 && b < kItemFree0 + kItemRing;
+      mbar_init(&bar[b], per_warp ? 4 : item_free ? C::ITEM_READERS : 1);
     }
     fence_mbar_init();
   }
@@ -205,6 +224,29 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   bool dead = false;
+
+  // The item ring.  Entry k is the k-th item index this CTA handles (or
+  // n_items: no more); every role walks the entries in order and skips the
+  // same empty items, so their counts of items and tiles stay in step.
+  unsigned long long *counter = &p.plan->counter[kListTile];
+  auto ring_post = [&](uint32_t k) -> long long {  // lead producer, one thread
+    const int x = k % kItemRing;
+    if (k >= kItemRing) mbar_wait(&bar[kItemFree0 + x], ((k / kItemRing) - 1) & 1, dead, p.status);
+    long long v = k == 0 ? (long long)blockIdx.x
+                  : n_items <= (long long)gridDim.x ? n_items
+                                                    : (long long)gridDim.x + (long long)atomicAdd(counter, 1ull);
+    if (dead || v > n_items) v = n_items;  // a timed-out kernel stops taking items
+    s_items[x] = v;
+    mbar_arrive(&bar[kItemFull0 + x]);
+    return v;
+  };
+  auto ring_take = [&](uint32_t k) -> long long {  // a reading role, one thread
+    const int x = k % kItemRing;
+    mbar_wait(&bar[kItemFull0 + x], (k / kItemRing) & 1, dead, p.status);
+    const long long v = dead ? n_items : s_items[x];
+    mbar_arrive(&bar[kItemFree0 + x]);
+    return v;
+  };
 
   if (warp == kKWarp0 || warp == kKWarp1 || warp == kVWarp) {
     if constexpr (C::SPLIT) {
@@ -219,8 +261,11 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
       constexpr int KH = (C::NHQ + 1) / 2;
       const int h_lo = warp == kKWarp1 ? KH : 0, h_hi = warp == kKWarp0 ? KH : C::NHQ;
       uint32_t tiles = 0, items = 0;
-      for (long long item = blockIdx.x; item < n_items && (is_v || h_lo < h_hi);
-           item += gridDim.x) {
+      for (uint32_t k = 0; is_v || h_lo < h_hi; ++k) {
+        long long item = 0;
+        if (lane == 0) item = lead ? ring_post(k) : ring_take(k);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= n_items) break;
         TileItem it;
         if (!decode_tile_item(p, item, G, it)) continue;
         const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
@@ -288,7 +333,11 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
       // One producer warp (warp 4): Q, then K of tile j and V of tile j - 1
       // (V is consumed a softmax later).
       uint32_t tiles = 0, items = 0;
-      for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        long long item = 0;
+        if (lane == 0) item = ring_post(k);
+        item = __shfl_sync(0xffffffffu, item, 0);
+        if (item >= n_items) break;
         TileItem it;
         if (!decode_tile_item(p, item, G, it)) continue;
         const int32_t *bt = p.block_table + (size_t)it.s * p.max_blocks_per_seq;
@@ -378,7 +427,9 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
         tc_commit(&bar[kKFree0 + st]);
         tc_commit(&bar[kSFull0 + sb]);
       };
-      for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+      for (uint32_t k = 0;; ++k) {
+        const long long item = ring_take(k);
+        if (item >= n_items) break;
         TileItem it;
         if (!decode_tile_item(p, item, G, it)) continue;
         mbar_wait(&bar[kQFull], items & 1, dead, p.status);
@@ -416,7 +467,14 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
     const int r = tid;  // row of the tile == TMEM lane
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
     uint32_t tiles = 0, items = 0;
-    for (long long item = blockIdx.x; item < n_items; item += gridDim.x) {
+    for (uint32_t k = 0;; ++k) {
+      // thread 0 reads the ring for the group (all four warps then take the
+      // same items, whatever each thread's wait did): slot k & 1 is rewritten
+      // only after every thread has passed entry k + 1's barrier
+      if (r == 0) s_cur[k & 1] = ring_take(k);
+      named_sync(1, 128);
+      const long long item = s_cur[k & 1];
+      if (item >= n_items) break;
       TileItem it;
       if (!decode_tile_item(p, item, G, it)) continue;
       // Any invalid page in the item's KV range zeroes the item's rows.

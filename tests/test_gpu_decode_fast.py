@@ -187,3 +187,15 @@ def test_request_count_bound(n):
     ctx = [int(x) for x in rng.integers(1, 300, n)]
     b = inputs.paged_batch([1] * n, ctx, 8, 2, 64, 16, dtype="bf16", seed=n)
     parity.compare(fast(b), parity.oracle_forward(b), "bf16", what=f"fast {n} requests")
+
+
+def test_alternating_caches_reuse_no_stale_maps():
+    """The decode row maps are reused while the caches and extents stay the
+    same: calls that alternate between two caches of different shapes (and
+    a third with the first's shape at another address) each stay exact."""
+    b1 = inputs.paged_batch([1] * 5, [700, 40, 2000, 1, 333], 32, 8, 128, 16, dtype="bf16", seed=43)
+    b2 = inputs.paged_batch([1] * 3, [5000, 64, 900], 16, 2, 64, 64, dtype="bf16", seed=44)
+    b3 = inputs.paged_batch([1] * 5, [100, 2500, 17, 800, 64], 32, 8, 128, 16, dtype="bf16", seed=45)
+    want = {id(b): parity.oracle_forward(b) for b in (b1, b2, b3)}
+    for b in (b1, b2, b1, b3, b2, b3, b1):
+        parity.compare(fast(b), want[id(b)], "bf16", what="alternating caches")
