@@ -119,7 +119,12 @@ typedef enum {
  *  max_seq_len     host-known upper bound on seq_lens (sizes the workspace)
  *  kv_split_tokens 0 = automatic; otherwise the most KV positions one work
  *                  item covers (e.g. 32768 for chunked long context), a
- *                  multiple of 16; splits are merged by log-sum-exp
+ *                  multiple of 16; splits are merged by log-sum-exp.
+ *                  Extend / prefill rows on the tensor-core path are cut
+ *                  into equal splits of whole 64-position tiles, up to twice
+ *                  as many as the bound needs when the batch holds too few
+ *                  of them to keep every CTA busy (the workspace size allows
+ *                  for that)
  *
  * Errors: PA_ERR_INVALID_ARG for null pointers with nonzero sizes, negative
  * sizes, misaligned pointers; PA_ERR_UNSUPPORTED for shapes outside the list

@@ -84,14 +84,24 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
     if (p.qsl[s + 1] < p.qsl[s]) bad = 1;
   const bool qsl_bad = __syncthreads_or(bad) != 0;
 
-  // -- pass 1: class counts and the decode KV work (split sizing) ------------
-  long long v1[2] = {0, 0};  // packed class counts (21 bits each), decode work
+  // -- pass 1: class counts, decode KV work, tile work (split sizing) --------
+  // v1: packed class counts (21 bits each), decode KV positions, and the
+  // tile kernel's work in KV positions x query tiles (per KV head)
+  long long v1[3] = {0, 0, 0};
+  const int TQ = p.tile_ok && G <= kTileRows ? kTileRows / G : 0;  // tokens per query tile
   int metabad = 0;
   for (int s = tid; s < S; s += nthr) {
     const int4 q = raw(s);
     const ReqScalars r = classify(p, q.x, q.y, q.z, qsl_bad);
     v1[0] += 1ll << (21 * r.cls);
     if (r.valid && r.q_len == 1) v1[1] += p.window > 0 ? min(r.ctx, p.window) : r.ctx;
+    if (TQ > 0 && r.valid && r.q_len > 0 && (r.cls != kDecode || p.all_tile)) {
+      // tile t sees prefix + min((t + 1) TQ, q_len) positions
+      const int nt = (r.q_len + TQ - 1) / TQ;
+      long long w = (long long)nt * (r.ctx - r.q_len) + (((long long)TQ * (nt - 1) * nt) >> 1) + r.q_len;
+      if (p.window > 0) w = min(w, (long long)nt * (p.window + TQ));
+      v1[2] += w;
+    }
     if (!qsl_bad && !r.valid) {
       if (r.q_len < 0 || r.q_len > r.ctx || (p.max_qlen > 0 && r.q_len > p.max_qlen))
         metabad |= PA_DEV_BAD_QLEN;
@@ -102,9 +112,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   }
   if (metabad) atomicOr(p.status, (unsigned)metabad);
   if (tid == 0 && qsl_bad) atomicOr(p.status, PA_DEV_BAD_QSL);
-  long long t1[2];
-  block_scan_multi<2>(v1, scratch, t1);
-  const long long class_tot = t1[0], work_tot = t1[1];
+  long long t1[3];
+  block_scan_multi<3>(v1, scratch, t1);
+  const long long class_tot = t1[0], work_tot = t1[1], tile_tot = t1[2];
   const long long mask21 = (1ll << 21) - 1;
   const long long n_dec = class_tot & mask21, n_ext = (class_tot >> 21) & mask21;
 
@@ -118,6 +128,12 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
   const long long Lw = ceil_div_ll(ceil_div_ll(kv_work, target), 64) * 64;
   int L = (int)(Lw < kRowMinSplit ? kRowMinSplit : (Lw > kRowMaxSplit ? kRowMaxSplit : Lw));
   if (p.kv_split_tokens > 0 && p.kv_split_tokens < L) L = p.kv_split_tokens;
+  // Tile rows under a kv_split_tokens bound: equal splits of whole 64-position
+  // tiles, twice as many as the bound needs when the tile work would give each
+  // tile CTA fewer than about 4 bound-long items (the dynamic deal then ends
+  // with a long tail of single items).
+  const bool tile_fine = p.kv_split_tokens > 0 && p.tile_ctas > 0 &&
+                         tile_tot * Hk < 4ll * p.kv_split_tokens * p.tile_ctas;
   // Extend/prefill rows on the row path: at most ~4 splits per row.
   int Lr = (int)ceil_div_ll(ceil_div_ll(p.max_seq_len, 4), 16) * 16;
   if (Lr < L) Lr = L;
@@ -163,16 +179,23 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const FwdParams p) {
       // most 16 query rows per KV head); extend and prefill rows fill
       // 128-row tiles of the tcgen05 tile kernel when it applies.
       const bool row_path = !p.tile_ok || (r.cls == kDecode && !p.all_tile);
+      // With a sliding window no row looks below the first row's window:
+      // splits start there (16-aligned, so that no copy box crosses a page).
+      const int kv_base = window_lo(r.ctx - r.q_len, p.window) & ~15;
       int len;
       if (r.cls == kDecode) {
         len = L;
         if (p.kv_split_tokens > 0 && p.kv_split_tokens < len) len = p.kv_split_tokens;
+      } else if (row_path) {
+        len = Lr;
+      } else if (p.kv_split_tokens > 0) {
+        const int range = r.ctx - kv_base > 0 ? r.ctx - kv_base : 1;
+        const int ns = (int)ceil_div_ll(range, p.kv_split_tokens) * (tile_fine ? 2 : 1);
+        len = (int)ceil_div_ll(ceil_div_ll(range, ns), 64) * 64;
+        if (len > p.kv_split_tokens) len = p.kv_split_tokens;
       } else {
-        len = row_path ? Lr : (p.kv_split_tokens > 0 ? p.kv_split_tokens : (r.ctx > 0 ? r.ctx : 1));
+        len = r.ctx > 0 ? r.ctx : 1;
       }
-      // With a sliding window no row looks below the first row's window:
-      // splits start there (16-aligned, so that no copy box crosses a page).
-      const int kv_base = window_lo(r.ctx - r.q_len, p.window) & ~15;
       int nsplit = (int)ceil_div_ll(r.ctx - kv_base > 0 ? r.ctx - kv_base : 1, len);
       if (nsplit < 1) nsplit = 1;
       info.q_start = r.q_start;
@@ -665,7 +688,9 @@ long long partial_capacity(int num_seqs, int num_tokens, int num_heads, int max_
   long long cap = n_dec > 1 ? dec_rows * num_heads * n_dec : 0;
   long long n_other;
   if (tile_ok) {
-    n_other = kvs > 0 ? ceil_div_h(msl, kvs) : 1;
+    // tile rows: up to twice the splits kv_split_tokens needs (equal splits,
+    // doubled when the tile work is coarse)
+    n_other = kvs > 0 ? 2 * ceil_div_h(msl, kvs) : 1;
   } else {
     long long lr = ceil_div_h(ceil_div_h(msl, 4), 16) * 16;
     if (lr < kRowMinSplit) lr = kRowMinSplit;
@@ -956,6 +981,7 @@ pa_status fwd_launch(const FwdCall &c, void *workspace, unsigned int *status, in
   p.scale_log2 = c.scale * kLog2e;
   p.tile_ok = tile_ok ? 1 : 0;
   p.row_ctas = row_ctas;
+  p.tile_ctas = 2 * num_sms;  // the tile kernel's grid
   p.dtype = c.dtype;
   p.plan = reinterpret_cast<PlanHeader *>(ws + lay.plan);
   p.req = reinterpret_cast<ReqInfo *>(ws + lay.req);

@@ -75,6 +75,7 @@ struct FwdParams {
   float scale_log2;   // scale * log2(e): scores kept in the base-2 domain
   int tile_ok;        // extend/prefill rows go to the tensor-core tile kernel
   int row_ctas;       // resident CTAs of the row kernel (split sizing)
+  int tile_ctas;      // CTAs of the tile kernel's grid (split sizing)
   int dtype;          // pa_dtype
   // workspace
   PlanHeader *plan;
