@@ -51,10 +51,9 @@ namespace pa {
 namespace {
 
 // KV positions per tile.  64: two CTAs per SM with 256 TMEM columns each.
-// 128 also works: the S product is then an N = 128 MMA (an N = 64 one runs
-// the tensor pipe at about half rate) and one CTA per SM holds two S buffers
-// and O in 512 columns, but with one softmax pipeline per SM instead of two
-// it measured slower (mixed batch 2.00 ms against 1.62 ms).
+// 128 also works: one CTA per SM then holds two S buffers and O in 512
+// columns, but with one softmax pipeline per SM instead of two it measured
+// slower (mixed batch 2.00 ms against 1.62 ms).
 constexpr int kBN = 64;
 constexpr int kBox = 16;           // slots per TMA box
 constexpr int kKWarp0 = 4, kMmaWarp = 5, kVWarp = 6, kKWarp1 = 7;
