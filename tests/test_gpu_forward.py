@@ -291,6 +291,19 @@ def test_tile_chunked_extend_matches_unchunked():
         parity.compare(got, want, "bf16", what=f"chunk {kvs}")
 
 
+@pytest.mark.parametrize("kvs", [64, 96])
+def test_tile_equal_splits_on_a_large_extend(kvs):
+    """Tile rows under kv_split_tokens are cut into equal splits of whole
+    64-position tiles (doubled in count only when the batch's tile work is
+    small against the tile grid, which depends on the SM count): with two
+    extends of 300 and 200 tokens on 8000 and 6000 positions the 8000-position
+    request has over 80 splits, so its rows also take the merge's block pass."""
+    b = inputs.paged_batch([300, 1, 200], [8000, 3000, 6000], 16, 4, 128, 16, dtype="bf16",
+                           seed=500 + kvs)
+    got = parity.gpu_forward(b, kv_split_tokens=kvs)
+    parity.compare(got, parity.oracle_forward(b), "bf16", what=f"equal splits kvs {kvs}")
+
+
 def test_bad_block_in_extend_zeroes_its_rows():
     b = inputs.paged_batch([1, 40, 30], [100, 540, 30], 16, 2, 128, 16, dtype="bf16", seed=21)
     want = parity.oracle_forward(b)
