@@ -74,13 +74,18 @@ constexpr uint32_t kSBufsCols = kTmemO;
 
 // S buffer b = tile & 1: kSFull0 + b (S product done), kPFull0 + b (P
 // written over it), kODone0 + b (the PV product that read P is done: the
-// buffer is free for S of tile + 2).
+// buffer is free for S of tile + 2, and V stage b for V of tile + 2).  With
+// two or more K stages, kKFree0 + tile % KST (K stage free) also stands for
+// "S of the tile is done", so one commit serves both: tcgen05.commit holds
+// the issuing thread for some 60 clocks, and one thread issues every product.
+// (A barrier can stand for an event of tile t only while no later event on it
+// can complete before its waiters have seen it; with one K stage, S of tile
+// t + 1 may complete before the softmax has seen S of tile t.)
 enum Bar { kQFull = 0, kQFree, kSFull0, kSFull1, kPFull0, kPFull1, kODone0, kODone1, kOFree, kKFull0 };
 constexpr int kKFree0 = kKFull0 + kKStages;
 constexpr int kVFull0 = kKFree0 + kKStages;
-constexpr int kVFree0 = kVFull0 + kVStages;
 // item ring slot x: kItemFull0 + x (posted), kItemFree0 + x (read by every role)
-constexpr int kItemFull0 = kVFree0 + kVStages;
+constexpr int kItemFull0 = kVFull0 + kVStages;
 constexpr int kItemFree0 = kItemFull0 + kItemRing;
 constexpr int kNumBars = kItemFree0 + kItemRing;
 
@@ -110,6 +115,7 @@ struct TileCfg {
   static constexpr bool SPLIT = fits(2, kVStages);
   static constexpr int KST = fits(3, kVStages) ? 3 : SPLIT ? 2 : 1;
   static constexpr int VST = kVStages;
+  static_assert(VST == 2, "V stage g & 1 is freed by the PV product's kODone0 + (g & 1)");
   static constexpr int THREADS = SPLIT ? 256 : 192;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
             const int st = g % C::VST;
             if (lane == 0) {
               if (g >= C::VST)
-                mbar_wait(&bar[kVFree0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
+                mbar_wait(&bar[kODone0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
               mbar_arrive_expect_tx(&bar[kVFull0 + st],
                                     __popc(mask) * C::NHV * (pb64 ? kBN : kBox) * 128);
             }
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
               const int st = g % C::VST;
               if (lane == 0) {
                 if (g >= C::VST)
-                  mbar_wait(&bar[kVFree0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
+                  mbar_wait(&bar[kODone0 + st], ((g / C::VST) - 1) & 1, dead, p.status);
                 mbar_arrive_expect_tx(&bar[kVFull0 + st],
                                       __popc(mask) * C::NHV * (pb64 ? kBN : kBox) * 128);
               }
@@ -424,7 +430,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
           tc_mma_bf16(tmem + kTmemS + sb * kBN, a, b, C::IDESC_S, kk > 0);
         }
         tc_commit(&bar[kKFree0 + st]);
-        tc_commit(&bar[kSFull0 + sb]);
+        if constexpr (C::KST < 2) tc_commit(&bar[kSFull0 + sb]);
       };
       for (uint32_t k = 0;; ++k) {
         const long long item = ring_take(k);
@@ -451,8 +457,7 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
             tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
                            (j > 0 || kk > 0) ? 1u : 0u);
           }
-          tc_commit(&bar[kVFree0 + vs]);
-          tc_commit(&bar[kODone0 + pb]);
+          tc_commit(&bar[kODone0 + pb]);  // also frees V stage vs == pb
           if (j + 2 < it.nt) issue_s(g + 2);
         }
         tc_commit(&bar[kQFree]);
@@ -519,7 +524,10 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
         const uint32_t g = tiles + j;
         const int base = it.kv_lo + j * kBN;
         const int pb = g & 1;  // S buffer of this tile; P goes over its first half
-        mbar_wait(&bar[kSFull0 + pb], (g >> 1) & 1, dead, p.status);
+        if constexpr (C::KST >= 2)
+          mbar_wait(&bar[kKFree0 + g % C::KST], (g / C::KST) & 1, dead, p.status);
+        else
+          mbar_wait(&bar[kSFull0 + pb], (g >> 1) & 1, dead, p.status);
         tc_fence_after();
         if (warp_active) {
           // raw S of this tile -> scaled (and biased) scores, masked to the
