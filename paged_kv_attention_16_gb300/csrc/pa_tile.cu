@@ -56,7 +56,7 @@ namespace {
 // slower (mixed batch 2.00 ms against 1.62 ms).
 constexpr int kBN = 64;
 constexpr int kBox = 16;           // slots per TMA box
-constexpr int kKWarp0 = 4, kMmaWarp = 5, kVWarp = 6, kKWarp1 = 7;
+constexpr int kKWarp0 = 4, kMmaWarp = 5, kVWarp = 6, kSWarp = 7;
 constexpr int kKStages = 3;        // K tiles in flight per CTA (at most; see TileCfg::KST)
 constexpr int kVStages = 2;        // V tiles in flight per CTA
 constexpr float kTau = 8.0f;       // lazy-rescale headroom (base 2)
@@ -127,10 +127,10 @@ struct TileCfg {
   // the kernel checks that it is)
   static constexpr int SMEM = OFF_ITEMS + kItemRing * 8;
   static_assert(SMEM == OFF_BAR + TAIL, "shared memory layout");
-  // roles that read each posted item besides the lead producer: the second
-  // K warp (when the keys have two or more 64-wide chunks), the V warp, the
-  // MMA thread and the softmax group; with one producer, the last two
-  static constexpr int ITEM_READERS = SPLIT ? (NHQ >= 2 ? 4 : 3) : 2;
+  // roles that read each posted item besides the lead producer: the V warp,
+  // the S-issuing and PV-issuing threads and the softmax group; with one
+  // producer, one issuing thread and the softmax group
+  static constexpr int ITEM_READERS = SPLIT ? 4 : 2;
   static_assert(fits(KST, VST), "shared memory budget");
   static constexpr uint32_t IDESC_S = umma_idesc_bf16(128, kBN, 0);
   static constexpr uint32_t IDESC_PV = umma_idesc_bf16(128, DV, 1);
@@ -253,18 +253,15 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
     return v;
   };
 
-  if (warp == kKWarp0 || warp == kKWarp1 || warp == kVWarp) {
+  if (warp == kKWarp0 || (C::SPLIT && warp == kVWarp)) {
     if constexpr (C::SPLIT) {
       // ------------------------------------------------------------- producers
       // A TMA copy holds up the warp that issues it for about as long as its
       // data takes to arrive (some 20 bytes per clock per warp), so the loads
-      // are spread over three warps: K chunks [0, KH) and Q (kKWarp0, which
-      // also posts each K tile's byte count), K chunks [KH, NHQ) (kKWarp1; its
-      // bytes may land first: the tile cannot complete while kKWarp0's arrival
-      // is pending), and V (kVWarp).  Each walks the same items and tiles.
+      // come from two warps: Q and K (kKWarp0, which also posts each K tile's
+      // byte count) and V (kVWarp).  Each walks the same items and tiles.
       const bool is_v = warp == kVWarp, lead = warp == kKWarp0;
-      constexpr int KH = (C::NHQ + 1) / 2;
-      const int h_lo = warp == kKWarp1 ? KH : 0, h_hi = warp == kKWarp0 ? KH : C::NHQ;
+      const int h_lo = 0, h_hi = C::NHQ;
       uint32_t tiles = 0, items = 0;
       for (uint32_t k = 0; is_v || h_lo < h_hi; ++k) {
         long long item = 0;
@@ -409,8 +406,14 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
         ++items;
       }
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------- MMA issuer
+  } else if (warp == kMmaWarp || (C::SPLIT && warp == kSWarp)) {
+    // ------------------------------------------------------------- MMA issuers
+    // With two producer warps the S products come from their own warp
+    // (kSWarp) and the MMA warp issues the PV products: a thread issuing a
+    // tcgen05.mma is held some 70 clocks per product, so one thread issuing
+    // both kinds made each PV product wait behind the next S and S(j + 2)
+    // behind the completion of PV(j).
+    const bool s_role = !C::SPLIT || warp == kSWarp, pv_role = !C::SPLIT || warp == kMmaWarp;
     if (lane == 0) {
       uint32_t tiles = 0, items = 0;
       const uint32_t sq = smem_u32(sQ), sk = smem_u32(sK), sv = smem_u32(sV);
@@ -437,30 +440,34 @@ __global__ void __launch_bounds__((TileCfg<DQK, DV>::THREADS), 2)
         if (item >= n_items) break;
         TileItem it;
         if (!decode_tile_item(p, item, G, it)) continue;
-        mbar_wait(&bar[kQFull], items & 1, dead, p.status);
-        issue_s(tiles);
-        if (it.nt > 1) issue_s(tiles + 1);
+        if (s_role) {
+          mbar_wait(&bar[kQFull], items & 1, dead, p.status);
+          issue_s(tiles);
+          if (it.nt > 1) issue_s(tiles + 1);
+        }
         for (int j = 0; j < it.nt; ++j) {
           const uint32_t g = tiles + j;
           const int pb = g & 1, vs = g % C::VST;
-          mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, p.status);
-          mbar_wait(&bar[kVFull0 + vs], (g / C::VST) & 1, dead, p.status);
-          if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
-          tc_fence_after();
-          const uint32_t vb = sv + vs * C::V_BYTES;
+          if (pv_role) {
+            mbar_wait(&bar[kPFull0 + pb], (g >> 1) & 1, dead, p.status);
+            mbar_wait(&bar[kVFull0 + vs], (g / C::VST) & 1, dead, p.status);
+            if (j == 0 && items > 0) mbar_wait(&bar[kOFree], (items - 1) & 1, dead, p.status);
+            tc_fence_after();
+            const uint32_t vb = sv + vs * C::V_BYTES;
 #pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            // 16 V rows (K = 16 of the PV product); the leading byte offset
-            // steps to the next 64-wide chunk of the row
-            const uint64_t b = pb64 ? umma_desc_sw128(vb + kk * 16 * 128, kBN * 128, 1024)
-                                    : umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
-            tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
-                           (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kBN / 16; ++kk) {
+              // 16 V rows (K = 16 of the PV product); the leading byte offset
+              // steps to the next 64-wide chunk of the row
+              const uint64_t b = pb64 ? umma_desc_sw128(vb + kk * 16 * 128, kBN * 128, 1024)
+                                      : umma_desc_sw128(vb + kk * C::V_BOX, kBox * 128, 1024);
+              tc_mma_bf16_ts(tmem + kTmemO, tmem + kTmemS + pb * kBN + kk * 8, b, C::IDESC_PV,
+                             (j > 0 || kk > 0) ? 1u : 0u);
+            }
+            tc_commit(&bar[kODone0 + pb]);  // also frees V stage vs == pb
           }
-          tc_commit(&bar[kODone0 + pb]);  // also frees V stage vs == pb
-          if (j + 2 < it.nt) issue_s(g + 2);
+          if (s_role && j + 2 < it.nt) issue_s(g + 2);
         }
-        tc_commit(&bar[kQFree]);
+        if (s_role) tc_commit(&bar[kQFree]);
         tiles += it.nt;
         ++items;
       }
