@@ -11,22 +11,24 @@
 // GB300 design.  One work item = 128 query rows (128/G tokens x the G heads of
 // one KV head, GQA-packed so the M = 128 MMA is full and the causal diagonal of
 // a tile is only 128/G positions wide) x one KV split.  Per CTA (2 per SM):
-//   warps 4, 7, 6  TMA producers: the Q tile (128-byte swizzled boxes of G
+//   warps 4, 6  TMA producers: the Q tile (128-byte swizzled boxes of G
 //            heads x 128/G tokens), then per 64-position KV tile the K page
-//            boxes {64 dims x 16 slots} (half the 64-dim chunks from warp 4,
-//            half from warp 7) and the V page boxes {16 slots x all dims}
-//            (warp 6) named by the block table, into rings of three K and two
-//            V tiles.  A TMA copy holds its issuing warp for about as long as
-//            the data takes to land (measured: some 20 bytes per clock per
-//            warp, whatever the depth of the ring), so one warp could not
-//            keep up with two CTAs' products; three can.  (The 192-wide keys
-//            fit only one K stage beside Q: there warp 4 alone loads K of
-//            tile j, then V of tile j - 1.)
-//   warp 5   MMA issuer (one thread) and TMEM owner: S = Q K^T (M=128, N=64,
-//            K=head_dim, bf16 in, fp32 in TMEM) into one of two S buffers,
-//            running a tile ahead of the softmax, then O += P V with P read
-//            from TMEM (N=head_dim, K=64, V read MN-major straight from its
-//            page layout);
+//            boxes {64 dims x 16 slots} (warp 4) and the V page boxes
+//            {16 slots x all dims} (warp 6) named by the block table, into
+//            rings of three K and two V tiles.  A TMA copy holds its issuing
+//            warp for about as long as the data takes to land (measured: some
+//            20 bytes per clock per warp, whatever the depth of the ring), so
+//            one warp could not load both for two CTAs' products.  (The
+//            192-wide keys fit only one K stage beside Q: there warp 4 alone
+//            loads K of tile j, then V of tile j - 1.)
+//   warps 7, 5  tcgen05 issue (one thread each; warp 5 owns TMEM): warp 7
+//            S = Q K^T (M=128, N=64, K=head_dim, bf16 in, fp32 in TMEM) into
+//            one of two S buffers, running a tile ahead of the softmax; warp
+//            5 O += P V with P read from TMEM (N=head_dim, K=64, V read
+//            MN-major straight from its page layout).  Issuing a tcgen05.mma
+//            holds the thread some 70 clocks, so one thread issuing both
+//            kinds held each PV product behind the next S.  (With one
+//            producer, warp 5 issues both.)
 //   warps 0-3  softmax: thread r owns row r (TMEM lane r): reads its S row
 //            (twice -- for the maximum, then for the weights -- where 128
 //            registers a thread leave no room to hold 64 scores),
