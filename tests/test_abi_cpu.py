@@ -80,6 +80,22 @@ def test_workspace_bytes_grow_with_splits(lib):
     assert 0 < small < big
 
 
+def test_workspace_holds_doubled_tile_splits(lib):
+    """Extend / prefill rows on the tensor-core path are cut into up to twice
+    the splits kv_split_tokens needs (equal splits, doubled when the batch's
+    tile work is small against the grid): the workspace holds a split partial
+    (head_dim fp32 + its log-sum-exp) per row, head and split for all of them."""
+    f = lib.pa_forward_workspace_bytes
+    f.restype = ctypes.c_size_t
+    f.argtypes = [ctypes.c_int] * 8
+    T, H, Hk, D, msl, kvs = 4100, 8, 1, 128, 131072, 32768
+    bf16 = 1
+    auto = f(bf16, 6, T, H, Hk, D, msl, 0)
+    chunked = f(bf16, 6, T, H, Hk, D, msl, kvs)
+    splits = 2 * (-(-msl // kvs))
+    assert chunked - auto >= T * H * splits * (D * 4 + 4)
+
+
 def _cache_write(lib, **kw):
     args = dict(kn=1 << 20, vn=1 << 20, kc=1 << 20, vc=1 << 20, bt=1 << 20, sl=1 << 20,
                 qsl=1 << 20, Hk=2, D=128, bs=16, stream=None, dtype=1, S=1, T=1, mbps=4, nb=4,
